@@ -1,0 +1,225 @@
+/*
+ * mxq.h -- C ABI of libmxq: MX block-scaled quantization and block-scaled
+ * MXFP8 GEMMs for GB300 (sm_103a).
+ *
+ * What the operations are (web pages, cited by title and section):
+ *  [TT]  "低精度训练特性（MXFP8 / HiFloat8）" (torchtitan-npu feature guide):
+ *        section "线性层低精度" MXFP8 mode -- per-block quantization of
+ *        activations and weights, block size 32, every 32 elements share one
+ *        scale, then a low-precision matmul for the forward, input-gradient and
+ *        weight-gradient products, output back in the original precision;
+ *        section "MoE 专家层低精度" MXFP8 mode -- the same for the experts'
+ *        grouped matmul, with the weight gradient's operands quantized per
+ *        group ("grouped dynamic MX quant").
+ *  [FB]  "Ascend/MindSpeed pull 3852" (the fb-split PR), change summary:
+ *        forward quantizes along one axis only and saves nothing; backward
+ *        recomputes the other axis (vs. dual-axis quant whose extra outputs are
+ *        saved for backward).
+ *  [AMCT] "AMCT FakeQuant 模拟伪量化工具包" article: section 2 (MXFP4 numeric
+ *        model), section 3.2-3.3 (the kernel's raw call and its Python
+ *        wrapper's padding convention), section 4.2 (config validation).
+ *
+ * Conventions for every entry point:
+ *  - All tensor arguments are DEVICE pointers to memory the caller owns and
+ *    keeps alive until the work on `stream` has finished.  The library never
+ *    allocates device memory; size queries tell the caller how much to give.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Argument checks run first, on the host, and return an
+ *    error before anything is launched; nothing is written on error.
+ *  - Pointers must be 16-byte aligned.  Row-major everywhere; `ld*` are
+ *    leading dimensions in elements.
+ *  - Codes are bytes: E4M3 (OCP FP8, max 448) or, for E2M1, two 4-bit codes
+ *    per byte (even element in the low nibble; nibble = sign<<3 | index into
+ *    {0, .5, 1, 1.5, 2, 3, 4, 6}).  Scales are E8M0 bytes (2^(byte-127)).
+ *  - Scale layout "swz(R, KB)": the logical R x KB scale matrix (KB = number
+ *    of 32-element blocks along the contraction axis) with R padded to 128 and
+ *    KB to 4, stored as 512-byte tiles of 128 rows x 4 blocks, tile (i, j) at
+ *    byte 512*(i*ceil(KB/4) + j), element (r, c) of a tile at
+ *    16*(r%32) + 4*(r/32) + c.  This is the layout the tcgen05 block-scaled
+ *    MMA reads; the quantizers write padding bytes as 0.
+ *  - "K-major": every GEMM operand is [rows x K] with the scale blocks along K;
+ *    a column quant writes its codes transposed ([C x R]) so that it too is
+ *    K-major.
+ *  - Errors: the return value; mxq_last_error_string() gives the reason
+ *    (thread-local).  No exception crosses the ABI.  MXQ_ERR_ARCH when the
+ *    current device is not compute capability 10.3.
+ */
+#ifndef MXQ_H
+#define MXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *mxq_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    MXQ_OK = 0,
+    MXQ_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or enum */
+    MXQ_ERR_UNSUPPORTED = 2, /* valid request this library does not implement */
+    MXQ_ERR_ARCH = 3,        /* current device is not sm_103 */
+    MXQ_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+    MXQ_ERR_TIMEOUT = 5      /* a kernel gave up waiting (see mxq_poll_device_error) */
+} mxq_status;
+
+typedef enum { MXQ_BF16 = 0, MXQ_F32 = 1 } mxq_dtype;
+typedef enum { MXQ_E4M3 = 0, MXQ_E2M1 = 1 } mxq_fmt;
+typedef enum { MXQ_SAVE_QUANT = 0, MXQ_RECOMPUTE = 1 } mxq_mode;
+typedef enum { MXQ_GG_FWD = 0, MXQ_GG_DX = 1, MXQ_GG_DW = 2 } mxq_gg_kind;
+
+/* ------------------------------------------------------------------ */
+/* Size queries (host only, no CUDA calls)                              */
+/* ------------------------------------------------------------------ */
+
+/* Bytes of swz(rows, k_blocks): ceil128(rows) * ceil4(k_blocks). */
+size_t mxq_scale_bytes(int64_t rows, int64_t k_blocks);
+
+/* Capacity of the padded token axis of a per-group column quant of T rows in
+ * E groups: 128 * (ceil(T/128) + E), an upper bound on
+ * sum_e ceil128(n_e) for any split of T rows into E groups. */
+int64_t mxq_grouped_padded_rows(int64_t T, int E);
+
+/* ------------------------------------------------------------------ */
+/* Quantization                                                         */
+/* ------------------------------------------------------------------ */
+
+/* Dynamic MX quantization of x[rows x cols] (leading dim ldx).
+ * [TT] MXFP8 mode (blocks of 32 sharing one scale; axis -1 or -2 of the
+ * dynamic MX quant op) and [FB] (the dual-axis variant returns both axes from
+ * one call).
+ *  fmt = MXQ_E4M3 (MXFP8): dtype must be MXQ_BF16.  Scale exponent
+ *      X = floor(log2 amax) - 8 clamped to [-127,127] (X = -127 for an
+ *      all-zero block); code = E4M3(x * 2^-X), round-to-nearest-even,
+ *      saturating to +-448.
+ *    axis = -1 (or dual_axis): blocks along cols; needs cols % 32 == 0.
+ *      q_row [rows x cols] u8, s_row swz(rows, cols/32).
+ *    axis = -2 (or dual_axis): blocks along rows (a ragged last block is
+ *      zero-padded); q_colT [cols x rows] u8 (transposed, leading dim rows),
+ *      s_colT swz(cols, ceil(rows/32)).  Needs cols % 8 == 0.
+ *    dual_axis != 0: both outputs from one read of x ([FB]).
+ *  fmt = MXQ_E2M1 (MXFP4, [AMCT] section 2 with scale_factor 6): dtype BF16
+ *      or F32, axis -1 only, dual_axis 0, cols % 32 == 0.  q_row holds
+ *      rows x cols/2 bytes, s_row swz(rows, cols/32), scale byte e + 127 with
+ *      e = round(log2(max(amax/6, 2^-30))).
+ * Pointers not needed by the chosen axis may be NULL.  ldx % 8 == 0.
+ * rows == 0 or cols == 0 is a no-op. */
+mxq_status mxq_quantize(const void *x, mxq_dtype dtype, int64_t rows, int64_t cols, int64_t ldx,
+                        int axis, mxq_fmt fmt, int dual_axis,
+                        void *q_row, void *s_row, void *q_colT, void *s_colT,
+                        mxq_stream_t stream);
+
+/* Per-group column MXFP8 quant for the grouped weight gradient ([TT] MoE
+ * MXFP8 mode, "grouped dynamic MX quant"): x bf16 [rows x cols] (leading
+ * dim cols), group e = rows [off[e], off[e+1]) with d_offsets a DEVICE array
+ * of E+1 int64 (non-decreasing, off[0] = 0, off[E] = rows; not checked on the
+ * device).  Blocks of 32 rows restart at every group start and a group's last
+ * block is zero-padded.  Group e is written at padded column P_e =
+ * sum_{j<e} ceil128(n_j) of q_colT [cols x t_pad] (leading dim t_pad) and its
+ * scales into s_colT swz(cols, t_pad/32).  Every byte of both outputs is
+ * written (padding = 0).  t_pad % 128 == 0 and
+ * t_pad >= mxq_grouped_padded_rows(rows, E) guarantees room; cols % 8 == 0;
+ * 1 <= E <= 4096. */
+mxq_status mxq_quantize_grouped_col(const void *x_bf16, int64_t rows, int64_t cols,
+                                    const int64_t *d_offsets, int E, int64_t t_pad,
+                                    void *q_colT, void *s_colT, mxq_stream_t stream);
+
+/* MXFP4 quant-dequant ([AMCT] sections 2, 3.2-3.3): fp32 x viewed as
+ * [rows x cols] with cols the tensor's last dim; blocks of 32 along each row,
+ * the last block of a row zero-padded (never spanning two rows);
+ * scale = 2^round(log2(max(amax/scale_factor, 2^-30))) (evaluated exactly),
+ * elements snapped to {0, +-.5, +-1, +-1.5, +-2, +-3, +-4, +-6} * scale with
+ * midpoints rounding away from zero.  y has x's shape; y may equal x.
+ * block_size must be 32 (else MXQ_ERR_UNSUPPORTED, as the Ascend kernel and
+ * its wrapper require); scale_factor must be finite and > 0 ([AMCT] 4.2) --
+ * scale_factor = 6 / inv_scale_factor_scale ([AMCT] 3.3). */
+mxq_status mxq_qdq_mxfp4(const float *x, float *y, int64_t rows, int64_t cols,
+                         int block_size, float scale_factor, mxq_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Block-scaled MXFP8 GEMMs ([TT] MXFP8 mode; output in bf16, fp32 accumulate) */
+/* ------------------------------------------------------------------ */
+
+/* C[M x N] (bf16, leading dim ldc) = deq(A) deq(B)^T with A [M x K] E4M3
+ * codes + swz(M, K/32) scales and B [N x K] E4M3 codes + swz(N, K/32).
+ * K % 32 == 0, K > 0, ldc >= N, ldc % 8 == 0.  M or N == 0 is a no-op. */
+mxq_status mxq_gemm(const uint8_t *a, const uint8_t *sa, const uint8_t *b, const uint8_t *sb,
+                    int64_t M, int64_t N, int64_t K, void *c_bf16, int64_t ldc,
+                    mxq_stream_t stream);
+
+/* Grouped (MoE) block-scaled GEMM over E experts ([TT] MoE MXFP8 mode),
+ * group offsets d_offsets (DEVICE, E+1 int64, as for
+ * mxq_quantize_grouped_col), T = off[E] token rows.
+ *  MXQ_GG_FWD: out[T x N] rows of group e = deq(A_e) deq(B_e)^T, A [T x K]
+ *      row-quantized (swz(T, K/32)), B [E*N x K] row-quantized as one matrix
+ *      (swz(E*N, K/32)); expert e's weight is rows [e*N, (e+1)*N).
+ *      N % 128 == 0.
+ *  MXQ_GG_DX: out[T x K] rows of group e = deq(A_e) deq(B_e)^T, A = dY
+ *      [T x N] row-quantized (swz(T, N/32)), B = the column quant of the
+ *      stacked weights [E*N x K] ([FB] op_dx: the weight re-quantized along the
+ *      other axis): codes [K x E*N], swz(K, E*N/32); expert e contracts over
+ *      columns [e*N, (e+1)*N).  N % 128 == 0.  (K here is the output width.)
+ *  MXQ_GG_DW: out[E x N x K]: out_e = deq(A_e) deq(B_e)^T contracted over the
+ *      rows of group e only, A = per-group column quant of dY (codes
+ *      [N x t_pad], swz(N, t_pad/32)), B = per-group column quant of X (codes
+ *      [K x t_pad], swz(K, t_pad/32)); a group with no rows gives zeros.
+ * K % 32 == 0 (FWD/DX), ldc is the output's row length (N for FWD/DW, K for
+ * DX). */
+mxq_status mxq_grouped_gemm(mxq_gg_kind kind, const uint8_t *a, const uint8_t *sa,
+                            const uint8_t *b, const uint8_t *sb, const int64_t *d_offsets, int E,
+                            int64_t T, int64_t N, int64_t K, int64_t t_pad, void *out_bf16,
+                            mxq_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* MXFP8 linear layer: Y = X W^T, dX = dY W, dW = dY^T X                */
+/* ------------------------------------------------------------------ */
+/* [TT] MXFP8 mode; [FB] for the two modes:
+ *  MXQ_SAVE_QUANT: forward dual-quantizes X and W and keeps their column
+ *      quants in ctx for the backward.
+ *  MXQ_RECOMPUTE: forward row-quantizes only and keeps nothing; backward
+ *      re-quantizes X and W along the other axis from the bf16 originals.
+ * Both modes give bitwise-identical Y, dX and dW.
+ * x bf16 [M x K], w bf16 [N x K], dy bf16 [M x N]; y bf16 [M x N],
+ * dx bf16 [M x K], dw bf16 [N x K].  M, N, K multiples of 32, K,N > 0.
+ * ctx (mxq_linear_ctx_bytes) carries state from fwd to bwd_dx to bwd_dw of
+ * the same step and must not be reused by another step in between; bwd_dx
+ * stores dY's column quant there for bwd_dw.  workspace
+ * (mxq_linear_workspace_bytes) is scratch for one call. */
+size_t mxq_linear_ctx_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode);
+/* Bytes of ctx that live from the forward to the backward (the memory the
+ * recompute mode saves): (M*K + N*K) codes + their scales for SAVE, 0 for
+ * RECOMPUTE. */
+size_t mxq_linear_saved_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode);
+size_t mxq_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode);
+
+mxq_status mxq_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, int64_t K,
+                          mxq_mode mode, void *ctx, void *y, void *workspace, size_t ws_bytes,
+                          mxq_stream_t stream);
+mxq_status mxq_linear_bwd_dx(const void *dy, const void *w, int64_t M, int64_t N, int64_t K,
+                             mxq_mode mode, void *ctx, void *dx, void *workspace, size_t ws_bytes,
+                             mxq_stream_t stream);
+mxq_status mxq_linear_bwd_dw(const void *dy, const void *x, int64_t M, int64_t N, int64_t K,
+                             mxq_mode mode, void *ctx, void *dw, void *workspace, size_t ws_bytes,
+                             mxq_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Diagnostics                                                          */
+/* ------------------------------------------------------------------ */
+
+/* Reason for the last non-OK status returned on this thread ("" if none). */
+const char *mxq_last_error_string(void);
+
+/* Synchronizes the current device, then reads and clears the device-side
+ * error word that kernels set when a wait gives up (bit 0: an mbarrier wait
+ * timed out; bit 1: a tensor-memory allocation failed).  Returns
+ * MXQ_ERR_TIMEOUT if any bit was set (*word receives the bits), MXQ_OK
+ * otherwise.  word may be NULL. */
+mxq_status mxq_poll_device_error(uint32_t *word);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXQ_H */

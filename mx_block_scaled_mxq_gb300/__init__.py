@@ -1,0 +1,223 @@
+"""Python binding of libmxq (MX block-scaled quantization and MXFP8 GEMMs for GB300).
+
+Argument marshalling only: every function named ``mxq_*`` here has the name,
+arguments and meaning of the C entry point declared in ``include/mxq.h`` and
+forwards to it through ctypes.  Tensor arguments are torch CUDA tensors (or raw
+device addresses as ints); ``stream`` defaults to torch's current stream.  A
+non-OK status raises :class:`MXQError` with the library's reason.
+
+The compute path is the CUDA library only: if ``libmxq.so`` cannot be built or
+loaded, every call raises -- there is no fallback.
+
+The ``alloc_*`` / ``quantize_*`` helpers at the bottom only size and allocate
+output tensors with the library's own size queries, then call the entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MXQError", "load", "BF16", "F32", "E4M3", "E2M1", "SAVE_QUANT", "RECOMPUTE", "GG_FWD", "GG_DX", "GG_DW",
+    "mxq_scale_bytes", "mxq_grouped_padded_rows", "mxq_quantize", "mxq_quantize_grouped_col", "mxq_qdq_mxfp4",
+    "mxq_gemm", "mxq_grouped_gemm", "mxq_linear_ctx_bytes", "mxq_linear_saved_bytes",
+    "mxq_linear_workspace_bytes", "mxq_linear_fwd", "mxq_linear_bwd_dx", "mxq_linear_bwd_dw",
+    "mxq_last_error_string", "mxq_poll_device_error",
+]
+
+BF16, F32 = 0, 1
+E4M3, E2M1 = 0, 1
+SAVE_QUANT, RECOMPUTE = 0, 1
+GG_FWD, GG_DX, GG_DW = 0, 1, 2
+_STATUS = {0: "MXQ_OK", 1: "MXQ_ERR_INVALID_ARG", 2: "MXQ_ERR_UNSUPPORTED", 3: "MXQ_ERR_ARCH",
+           4: "MXQ_ERR_CUDA", 5: "MXQ_ERR_TIMEOUT"}
+
+
+class MXQError(RuntimeError):
+    def __init__(self, msg: str, status: int):
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+
+_I64, _I32, _P, _SZ, _F32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+_SIGNATURES = {
+    "mxq_scale_bytes": (_SZ, [_I64, _I64]),
+    "mxq_grouped_padded_rows": (_I64, [_I64, _I32]),
+    "mxq_quantize": (_I32, [_P, _I32, _I64, _I64, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
+    "mxq_quantize_grouped_col": (_I32, [_P, _I64, _I64, _P, _I32, _I64, _P, _P, _P]),
+    "mxq_qdq_mxfp4": (_I32, [_P, _P, _I64, _I64, _I32, _F32, _P]),
+    "mxq_gemm": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P]),
+    "mxq_grouped_gemm": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I64, _P, _P]),
+    "mxq_linear_ctx_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
+    "mxq_linear_saved_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
+    "mxq_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
+    "mxq_linear_fwd": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
+    "mxq_linear_bwd_dx": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
+    "mxq_linear_bwd_dw": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
+    "mxq_last_error_string": (ctypes.c_char_p, []),
+    "mxq_poll_device_error": (_I32, [ctypes.POINTER(ctypes.c_uint32)]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_needed: bool = True):
+    """Load libmxq.so (compiling it in-tree first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        if not _build.up_to_date():
+            if not build_if_needed:
+                raise MXQError(f"libmxq is not built at {_build.LIB}", -1)
+            _build.build()
+        lib = ctypes.CDLL(_build.LIB)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return t.data_ptr()
+    return int(t)
+
+
+def _s(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, name: str) -> None:
+    if status != 0:
+        reason = _lib.mxq_last_error_string().decode(errors="replace")
+        raise MXQError(f"{name}: {_STATUS.get(status, status)}: {reason}", status)
+
+
+# ---------------------------------------------------------------- entry points
+
+def mxq_scale_bytes(rows: int, k_blocks: int) -> int:
+    return int(load().mxq_scale_bytes(rows, k_blocks))
+
+
+def mxq_grouped_padded_rows(T: int, E: int) -> int:
+    return int(load().mxq_grouped_padded_rows(T, E))
+
+
+def mxq_quantize(x, dtype, rows, cols, ldx, axis, fmt, dual_axis, q_row, s_row, q_colT, s_colT, stream=None):
+    _check(load().mxq_quantize(_p(x), dtype, rows, cols, ldx, axis, fmt, int(dual_axis), _p(q_row), _p(s_row),
+                               _p(q_colT), _p(s_colT), _s(stream)), "mxq_quantize")
+
+
+def mxq_quantize_grouped_col(x, rows, cols, d_offsets, E, t_pad, q_colT, s_colT, stream=None):
+    _check(load().mxq_quantize_grouped_col(_p(x), rows, cols, _p(d_offsets), E, t_pad, _p(q_colT), _p(s_colT),
+                                           _s(stream)), "mxq_quantize_grouped_col")
+
+
+def mxq_qdq_mxfp4(x, y, rows, cols, block_size=32, scale_factor=6.0, stream=None):
+    _check(load().mxq_qdq_mxfp4(_p(x), _p(y), rows, cols, block_size, scale_factor, _s(stream)), "mxq_qdq_mxfp4")
+
+
+def mxq_gemm(a, sa, b, sb, M, N, K, c, ldc, stream=None):
+    _check(load().mxq_gemm(_p(a), _p(sa), _p(b), _p(sb), M, N, K, _p(c), ldc, _s(stream)), "mxq_gemm")
+
+
+def mxq_grouped_gemm(kind, a, sa, b, sb, d_offsets, E, T, N, K, t_pad, out, stream=None):
+    _check(load().mxq_grouped_gemm(kind, _p(a), _p(sa), _p(b), _p(sb), _p(d_offsets), E, T, N, K, t_pad, _p(out),
+                                   _s(stream)), "mxq_grouped_gemm")
+
+
+def mxq_linear_ctx_bytes(M, N, K, mode) -> int:
+    return int(load().mxq_linear_ctx_bytes(M, N, K, mode))
+
+
+def mxq_linear_saved_bytes(M, N, K, mode) -> int:
+    return int(load().mxq_linear_saved_bytes(M, N, K, mode))
+
+
+def mxq_linear_workspace_bytes(M, N, K, mode) -> int:
+    return int(load().mxq_linear_workspace_bytes(M, N, K, mode))
+
+
+def mxq_linear_fwd(x, w, M, N, K, mode, ctx, y, workspace, ws_bytes, stream=None):
+    _check(load().mxq_linear_fwd(_p(x), _p(w), M, N, K, mode, _p(ctx), _p(y), _p(workspace), ws_bytes, _s(stream)),
+           "mxq_linear_fwd")
+
+
+def mxq_linear_bwd_dx(dy, w, M, N, K, mode, ctx, dx, workspace, ws_bytes, stream=None):
+    _check(load().mxq_linear_bwd_dx(_p(dy), _p(w), M, N, K, mode, _p(ctx), _p(dx), _p(workspace), ws_bytes,
+                                    _s(stream)), "mxq_linear_bwd_dx")
+
+
+def mxq_linear_bwd_dw(dy, x, M, N, K, mode, ctx, dw, workspace, ws_bytes, stream=None):
+    _check(load().mxq_linear_bwd_dw(_p(dy), _p(x), M, N, K, mode, _p(ctx), _p(dw), _p(workspace), ws_bytes,
+                                    _s(stream)), "mxq_linear_bwd_dw")
+
+
+def mxq_last_error_string() -> str:
+    return load().mxq_last_error_string().decode(errors="replace")
+
+
+def mxq_poll_device_error():
+    """Returns the device error bits (0 = none); raises on a CUDA failure."""
+    w = ctypes.c_uint32(0)
+    st = load().mxq_poll_device_error(ctypes.byref(w))
+    if st not in (0, 5):
+        _check(st, "mxq_poll_device_error")
+    return int(w.value)
+
+
+# ---------------------------------------------------------------- allocation helpers
+
+def _u8(n: int, device) -> torch.Tensor:
+    return torch.empty(max(int(n), 1), dtype=torch.uint8, device=device)
+
+
+def quantize_mxfp8(x: torch.Tensor, axis: int = -1, dual: bool = False, stream=None):
+    """MXFP8 quant of a 2-D bf16 CUDA tensor.  Returns (q_row, s_row, q_colT,
+    s_colT) with None for the axis not requested; scales in swz layout."""
+    R, C = x.shape
+    q_row = s_row = qT = sT = None
+    if dual or axis == -1:
+        q_row = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+        s_row = _u8(mxq_scale_bytes(R, C // 32), x.device)
+    if dual or axis == -2:
+        qT = torch.empty((C, R), dtype=torch.uint8, device=x.device)
+        sT = _u8(mxq_scale_bytes(C, (R + 31) // 32), x.device)
+    mxq_quantize(x, BF16, R, C, x.stride(0), axis, E4M3, dual, q_row, s_row, qT, sT, stream)
+    return q_row, s_row, qT, sT
+
+
+def quantize_mxfp4(x: torch.Tensor, stream=None):
+    """Packed MXFP4 quant (scale_factor 6) of a 2-D bf16/fp32 CUDA tensor:
+    returns (nibbles [R x C/2], scales swz(R, C/32))."""
+    R, C = x.shape
+    q = torch.empty((R, C // 2), dtype=torch.uint8, device=x.device)
+    s = _u8(mxq_scale_bytes(R, C // 32), x.device)
+    mxq_quantize(x, F32 if x.dtype == torch.float32 else BF16, R, C, x.stride(0), -1, E2M1, 0, q, s, None, None,
+                 stream)
+    return q, s
+
+
+def qdq_mxfp4(x: torch.Tensor, scale_factor: float = 6.0, stream=None) -> torch.Tensor:
+    """MXFP4 quant-dequant of a contiguous fp32 CUDA tensor (blocks along the last dim)."""
+    assert x.dtype == torch.float32 and x.is_contiguous()
+    y = torch.empty_like(x)
+    cols = x.shape[-1] if x.dim() else 1
+    rows = x.numel() // cols if cols else 0
+    mxq_qdq_mxfp4(x, y, rows, cols, 32, scale_factor, stream)
+    return y

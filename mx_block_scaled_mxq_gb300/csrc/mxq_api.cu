@@ -1,0 +1,378 @@
+// mxq_api.cu -- the C ABI of libmxq (declared in include/mxq.h): argument
+// validation, arch check, dispatch to the kernels, and the linear layer's
+// saved-quant / recompute orchestration.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "mxq.h"
+#include "mxq_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mxq_status fail(mxq_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+mxq_status ok() {
+    g_last_error.clear();
+    return MXQ_OK;
+}
+
+bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+
+mxq_status check_arch() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(MXQ_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    static int cc[kMaxDevices] = {0};  // major*10+minor, 0 = unknown
+    if (dev < 0 || dev >= kMaxDevices) return fail(MXQ_ERR_CUDA, "device index %d out of range", dev);
+    if (cc[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return fail(MXQ_ERR_CUDA, "cannot query compute capability of device %d", dev);
+        cc[dev] = major * 10 + minor;
+    }
+    if (cc[dev] != 103)
+        return fail(MXQ_ERR_ARCH, "libmxq is built for sm_103a (GB300); device %d is sm_%d", dev, cc[dev]);
+    return MXQ_OK;
+}
+
+mxq_status cuda_result(cudaError_t e, const char *what) {
+    if (e != cudaSuccess) return fail(MXQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+inline size_t scale_bytes(int64_t rows, int64_t kb) {
+    return static_cast<size_t>(ceil_div(rows, 128) * 128) * static_cast<size_t>(ceil_div(kb, 4) * 4);
+}
+// codes + scales of a K-major operand [rows x k]
+inline size_t operand_bytes(int64_t rows, int64_t k) {
+    return round256(static_cast<size_t>(rows) * static_cast<size_t>(k)) + round256(scale_bytes(rows, ceil_div(k, 32)));
+}
+
+struct Operand {
+    uint8_t *q, *s;
+};
+inline Operand carve(uint8_t *&p, int64_t rows, int64_t k) {
+    Operand o;
+    o.q = p;
+    p += round256(static_cast<size_t>(rows) * static_cast<size_t>(k));
+    o.s = p;
+    p += round256(scale_bytes(rows, ceil_div(k, 32)));
+    return o;
+}
+
+mxq_status dense_gemm(const Operand &A, const Operand &B, int64_t M, int64_t N, int64_t K, void *c, int64_t ldc,
+                      cudaStream_t st) {
+    if (M == 0 || N == 0) return ok();
+    mxq::GemmProblem g{};
+    g.mode = mxq::kDense;
+    g.a = A.q; g.sa = A.s; g.a_rows = M; g.a_k = K;
+    g.b = B.q; g.sb = B.s; g.b_rows = N; g.b_k = K;
+    g.c = c; g.M = M; g.N = N; g.ldc = ldc; g.K = K;
+    return cuda_result(mxq::launch_gemm(g, st), "mxq gemm launch");
+}
+
+// ---- linear-layer memory plan ----
+// ctx:  SAVE: [colT(X): K x M][colT(W): K x N][colT(dY): N x M];  RECOMPUTE: [colT(dY)]
+// ws :  fwd [row(X)][row(W)];  bwd_dx [row(dY)][colT(W) if RECOMPUTE];  bwd_dw [colT(X) if RECOMPUTE]
+size_t saved_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
+    return mode == MXQ_SAVE_QUANT ? operand_bytes(K, M) + operand_bytes(K, N) : 0;
+}
+size_t ctx_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
+    return saved_bytes(M, N, K, mode) + operand_bytes(N, M);
+}
+size_t ws_fwd(int64_t M, int64_t N, int64_t K) { return operand_bytes(M, K) + operand_bytes(N, K); }
+size_t ws_dx(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
+    return operand_bytes(M, N) + (mode == MXQ_RECOMPUTE ? operand_bytes(K, N) : 0);
+}
+size_t ws_dw(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
+    return mode == MXQ_RECOMPUTE ? operand_bytes(K, M) : 0;
+}
+
+mxq_status check_linear(const void *a, const void *b, int64_t M, int64_t N, int64_t K, mxq_mode mode, void *ctx,
+                        void *out, void *ws, size_t ws_bytes, size_t ws_need) {
+    if (!a || !b || !ctx || !out) return fail(MXQ_ERR_INVALID_ARG, "null tensor pointer");
+    if (!al16(a) || !al16(b) || !al16(ctx) || !al16(out) || (ws && !al16(ws)))
+        return fail(MXQ_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (mode != MXQ_SAVE_QUANT && mode != MXQ_RECOMPUTE) return fail(MXQ_ERR_INVALID_ARG, "bad mode %d", (int)mode);
+    if (M <= 0 || N <= 0 || K <= 0 || M % 32 || N % 32 || K % 32)
+        return fail(MXQ_ERR_INVALID_ARG, "M, N, K must be positive multiples of 32 (got %lld, %lld, %lld)",
+                    (long long)M, (long long)N, (long long)K);
+    if (M > (1ll << 31) || N > (1ll << 31) || K > (1ll << 31))
+        return fail(MXQ_ERR_UNSUPPORTED, "dimension above 2^31");
+    if (ws_need > 0 && (!ws || ws_bytes < ws_need))
+        return fail(MXQ_ERR_INVALID_ARG, "workspace too small: need %zu bytes, got %zu", ws_need, ws ? ws_bytes : 0);
+    return MXQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *mxq_last_error_string(void) { return g_last_error.c_str(); }
+
+size_t mxq_scale_bytes(int64_t rows, int64_t k_blocks) {
+    if (rows <= 0 || k_blocks <= 0) return 0;
+    return scale_bytes(rows, k_blocks);
+}
+
+int64_t mxq_grouped_padded_rows(int64_t T, int E) {
+    if (T < 0 || E < 0) return 0;
+    return 128 * (ceil_div(T, 128) + E);
+}
+
+mxq_status mxq_poll_device_error(uint32_t *word) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(MXQ_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+    unsigned int w = 0;
+    e = mxq::read_and_clear_device_error(&w);
+    if (e != cudaSuccess) return fail(MXQ_ERR_CUDA, "read device error word: %s", cudaGetErrorString(e));
+    if (word) *word = w;
+    if (w) return fail(MXQ_ERR_TIMEOUT, "a kernel reported device error bits 0x%x", w);
+    return ok();
+}
+
+mxq_status mxq_quantize(const void *x, mxq_dtype dtype, int64_t rows, int64_t cols, int64_t ldx, int axis,
+                        mxq_fmt fmt, int dual_axis, void *q_row, void *s_row, void *q_colT, void *s_colT,
+                        mxq_stream_t stream) {
+    if (rows < 0 || cols < 0) return fail(MXQ_ERR_INVALID_ARG, "negative size");
+    if (dtype != MXQ_BF16 && dtype != MXQ_F32) return fail(MXQ_ERR_INVALID_ARG, "bad dtype %d", (int)dtype);
+    if (fmt != MXQ_E4M3 && fmt != MXQ_E2M1) return fail(MXQ_ERR_INVALID_ARG, "bad fmt %d", (int)fmt);
+    if (!dual_axis && axis != -1 && axis != -2) return fail(MXQ_ERR_INVALID_ARG, "axis must be -1 or -2");
+    const bool want_row = dual_axis || axis == -1, want_col = dual_axis || axis == -2;
+    if (fmt == MXQ_E2M1 && (want_col || dual_axis))
+        return fail(MXQ_ERR_UNSUPPORTED, "E2M1 quantization is along the last axis only");
+    if (fmt == MXQ_E4M3 && dtype != MXQ_BF16) return fail(MXQ_ERR_UNSUPPORTED, "MXFP8 quantization takes bf16 input");
+    if (ldx < cols || ldx % 8) return fail(MXQ_ERR_INVALID_ARG, "ldx must be >= cols and a multiple of 8");
+    if (want_row && cols % 32) return fail(MXQ_ERR_INVALID_ARG, "cols must be a multiple of 32 along the block axis");
+    if (want_col && cols % 8) return fail(MXQ_ERR_INVALID_ARG, "column quant needs cols % 8 == 0");
+    if (rows > (1ll << 31) || cols > (1ll << 31) || ceil_div(rows, 128) > 65535)
+        return fail(MXQ_ERR_UNSUPPORTED, "tensor too large for one launch");
+    if (rows == 0 || cols == 0) return ok();
+    if (!x || !al16(x)) return fail(MXQ_ERR_INVALID_ARG, "x must be a non-null 16-byte aligned pointer");
+    if (want_row && (!q_row || !s_row || !al16(q_row) || !al16(s_row)))
+        return fail(MXQ_ERR_INVALID_ARG, "q_row/s_row must be non-null 16-byte aligned pointers");
+    if (want_col && (!q_colT || !s_colT || !al16(q_colT) || !al16(s_colT)))
+        return fail(MXQ_ERR_INVALID_ARG, "q_colT/s_colT must be non-null 16-byte aligned pointers");
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (want_col) {
+        e = mxq::launch_quant_cols(static_cast<const uint16_t *>(x), rows, cols, ldx,
+                                   want_row ? static_cast<uint8_t *>(q_row) : nullptr,
+                                   want_row ? static_cast<uint8_t *>(s_row) : nullptr, static_cast<uint8_t *>(q_colT),
+                                   static_cast<uint8_t *>(s_colT), st);
+    } else {
+        e = mxq::launch_quant_rows(x, dtype == MXQ_F32, fmt == MXQ_E2M1 ? 1 : 0, rows, cols, ldx,
+                                   static_cast<uint8_t *>(q_row), static_cast<uint8_t *>(s_row), st);
+    }
+    return cuda_result(e, "mxq_quantize launch");
+}
+
+mxq_status mxq_quantize_grouped_col(const void *x_bf16, int64_t rows, int64_t cols, const int64_t *d_offsets, int E,
+                                    int64_t t_pad, void *q_colT, void *s_colT, mxq_stream_t stream) {
+    if (rows < 0 || cols < 0) return fail(MXQ_ERR_INVALID_ARG, "negative size");
+    if (E < 1 || E > 4096) return fail(MXQ_ERR_INVALID_ARG, "E must be in [1, 4096]");
+    if (cols % 8) return fail(MXQ_ERR_INVALID_ARG, "cols must be a multiple of 8");
+    if (t_pad < 0 || t_pad % 128 || t_pad < mxq_grouped_padded_rows(rows, E))
+        return fail(MXQ_ERR_INVALID_ARG, "t_pad must be a multiple of 128 and >= mxq_grouped_padded_rows(rows, E) = %lld",
+                    (long long)mxq_grouped_padded_rows(rows, E));
+    if (t_pad / 128 > 65535 || cols > (1ll << 31)) return fail(MXQ_ERR_UNSUPPORTED, "tensor too large for one launch");
+    if (cols == 0) return ok();
+    if (!d_offsets || (reinterpret_cast<uintptr_t>(d_offsets) & 7))
+        return fail(MXQ_ERR_INVALID_ARG, "d_offsets must be a non-null 8-byte aligned device pointer");
+    if ((rows > 0 && (!x_bf16 || !al16(x_bf16))) || !q_colT || !s_colT || !al16(q_colT) || !al16(s_colT))
+        return fail(MXQ_ERR_INVALID_ARG, "tensor pointers must be non-null and 16-byte aligned");
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    return cuda_result(mxq::launch_quant_cols_grouped(static_cast<const uint16_t *>(x_bf16), rows, cols, d_offsets, E,
+                                                      t_pad, static_cast<uint8_t *>(q_colT),
+                                                      static_cast<uint8_t *>(s_colT),
+                                                      reinterpret_cast<cudaStream_t>(stream)),
+                       "mxq_quantize_grouped_col launch");
+}
+
+mxq_status mxq_qdq_mxfp4(const float *x, float *y, int64_t rows, int64_t cols, int block_size, float scale_factor,
+                         mxq_stream_t stream) {
+    if (block_size != 32) return fail(MXQ_ERR_UNSUPPORTED, "block_size must be 32 (got %d)", block_size);
+    if (!(scale_factor > 0.0f) || !(scale_factor <= 3.402823466e38f))
+        return fail(MXQ_ERR_INVALID_ARG, "scale_factor must be finite and > 0");
+    if (rows < 0 || cols < 0) return fail(MXQ_ERR_INVALID_ARG, "negative size");
+    if (rows == 0 || cols == 0) return ok();
+    if (!x || !y || (reinterpret_cast<uintptr_t>(x) & 3) || (reinterpret_cast<uintptr_t>(y) & 3))
+        return fail(MXQ_ERR_INVALID_ARG, "x and y must be non-null fp32 pointers");
+    if (rows > (1ll << 40) / (cols > 0 ? cols : 1)) return fail(MXQ_ERR_UNSUPPORTED, "tensor too large");
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    return cuda_result(mxq::launch_qdq_mxfp4(x, y, rows, cols, scale_factor, reinterpret_cast<cudaStream_t>(stream)),
+                       "mxq_qdq_mxfp4 launch");
+}
+
+mxq_status mxq_gemm(const uint8_t *a, const uint8_t *sa, const uint8_t *b, const uint8_t *sb, int64_t M, int64_t N,
+                    int64_t K, void *c_bf16, int64_t ldc, mxq_stream_t stream) {
+    if (M < 0 || N < 0) return fail(MXQ_ERR_INVALID_ARG, "negative size");
+    if (K <= 0 || K % 32) return fail(MXQ_ERR_INVALID_ARG, "K must be a positive multiple of 32 (got %lld)", (long long)K);
+    if (ldc < N || ldc % 8) return fail(MXQ_ERR_INVALID_ARG, "ldc must be >= N and a multiple of 8");
+    if (M > (1ll << 31) || N > (1ll << 31) || K > (1ll << 31)) return fail(MXQ_ERR_UNSUPPORTED, "dimension above 2^31");
+    if (M == 0 || N == 0) return ok();
+    if (!a || !sa || !b || !sb || !c_bf16 || !al16(a) || !al16(sa) || !al16(b) || !al16(sb) || !al16(c_bf16))
+        return fail(MXQ_ERR_INVALID_ARG, "tensor pointers must be non-null and 16-byte aligned");
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    Operand A{const_cast<uint8_t *>(a), const_cast<uint8_t *>(sa)}, B{const_cast<uint8_t *>(b), const_cast<uint8_t *>(sb)};
+    return dense_gemm(A, B, M, N, K, c_bf16, ldc, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mxq_status mxq_grouped_gemm(mxq_gg_kind kind, const uint8_t *a, const uint8_t *sa, const uint8_t *b, const uint8_t *sb,
+                            const int64_t *d_offsets, int E, int64_t T, int64_t N, int64_t K, int64_t t_pad,
+                            void *out_bf16, mxq_stream_t stream) {
+    if (kind != MXQ_GG_FWD && kind != MXQ_GG_DX && kind != MXQ_GG_DW) return fail(MXQ_ERR_INVALID_ARG, "bad kind");
+    if (E < 1 || E > 4096) return fail(MXQ_ERR_INVALID_ARG, "E must be in [1, 4096]");
+    if (T < 0 || N <= 0 || K <= 0) return fail(MXQ_ERR_INVALID_ARG, "bad sizes");
+    if (N > (1ll << 31) || K > (1ll << 31) || T > (1ll << 31) || static_cast<int64_t>(E) * N > (1ll << 31))
+        return fail(MXQ_ERR_UNSUPPORTED, "dimension above 2^31");
+    if (!d_offsets || (reinterpret_cast<uintptr_t>(d_offsets) & 7))
+        return fail(MXQ_ERR_INVALID_ARG, "d_offsets must be a non-null 8-byte aligned device pointer");
+    if (!a || !sa || !b || !sb || !out_bf16 || !al16(a) || !al16(sa) || !al16(b) || !al16(sb) || !al16(out_bf16))
+        return fail(MXQ_ERR_INVALID_ARG, "tensor pointers must be non-null and 16-byte aligned");
+    mxq::GemmProblem g{};
+    g.offsets = d_offsets;
+    g.E = E;
+    g.c = out_bf16;
+    if (kind == MXQ_GG_FWD || kind == MXQ_GG_DX) {
+        if (N % 128) return fail(MXQ_ERR_INVALID_ARG, "N must be a multiple of 128 for the grouped forward/dX");
+        if (K % 32) return fail(MXQ_ERR_INVALID_ARG, "K must be a multiple of 32");
+        if (T == 0) return ok();
+        g.mode = mxq::kGroupedRows;
+        g.T = T;
+        g.a = a; g.sa = sa; g.b = b; g.sb = sb;
+        if (kind == MXQ_GG_FWD) {  // out[T x N] = X[T x K] . W_e[N x K]^T
+            g.a_rows = T; g.a_k = K;
+            g.b_rows = static_cast<int64_t>(E) * N; g.b_k = K;
+            g.M = T; g.N = N; g.ldc = N; g.K = K;
+            g.b_row_per_expert = N; g.b_k_per_expert = 0;
+        } else {  // out[T x K] = dY[T x N] . colT(W)_e[K x N]^T
+            g.a_rows = T; g.a_k = N;
+            g.b_rows = K; g.b_k = static_cast<int64_t>(E) * N;
+            g.M = T; g.N = K; g.ldc = K; g.K = N;
+            g.b_row_per_expert = 0; g.b_k_per_expert = N;
+        }
+    } else {
+        if (t_pad <= 0 || t_pad % 128 || t_pad < mxq_grouped_padded_rows(T, E))
+            return fail(MXQ_ERR_INVALID_ARG, "t_pad must be a multiple of 128 and >= mxq_grouped_padded_rows(T, E)");
+        if (t_pad > (1ll << 31)) return fail(MXQ_ERR_UNSUPPORTED, "t_pad above 2^31");
+        g.mode = mxq::kGroupedK;
+        g.a = a; g.sa = sa; g.a_rows = N; g.a_k = t_pad;
+        g.b = b; g.sb = sb; g.b_rows = K; g.b_k = t_pad;
+        g.M = N; g.N = K; g.ldc = K;
+        g.c_expert_stride = N * K;
+    }
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    return cuda_result(mxq::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)), "mxq_grouped_gemm launch");
+}
+
+size_t mxq_linear_ctx_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return ctx_bytes(M, N, K, mode);
+}
+size_t mxq_linear_saved_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return saved_bytes(M, N, K, mode);
+}
+size_t mxq_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    size_t w = ws_fwd(M, N, K);
+    if (ws_dx(M, N, K, mode) > w) w = ws_dx(M, N, K, mode);
+    if (ws_dw(M, N, K, mode) > w) w = ws_dw(M, N, K, mode);
+    return w;
+}
+
+mxq_status mxq_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, int64_t K, mxq_mode mode, void *ctx,
+                          void *y, void *workspace, size_t ws_bytes, mxq_stream_t stream) {
+    mxq_status s = check_linear(x, w, M, N, K, mode, ctx, y, workspace, ws_bytes, ws_fwd(M, N, K));
+    if (s != MXQ_OK) return s;
+    if ((s = check_arch()) != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    const Operand xq = carve(wp, M, K), wq = carve(wp, N, K);
+    cudaError_t e;
+    if (mode == MXQ_SAVE_QUANT) {
+        uint8_t *cp = static_cast<uint8_t *>(ctx);
+        const Operand xT = carve(cp, K, M), wT = carve(cp, K, N);
+        e = mxq::launch_quant_cols(static_cast<const uint16_t *>(x), M, K, K, xq.q, xq.s, xT.q, xT.s, st);
+        if (e == cudaSuccess)
+            e = mxq::launch_quant_cols(static_cast<const uint16_t *>(w), N, K, K, wq.q, wq.s, wT.q, wT.s, st);
+    } else {
+        e = mxq::launch_quant_rows(x, false, 0, M, K, K, xq.q, xq.s, st);
+        if (e == cudaSuccess) e = mxq::launch_quant_rows(w, false, 0, N, K, K, wq.q, wq.s, st);
+    }
+    if (e != cudaSuccess) return cuda_result(e, "mxq_linear_fwd quant launch");
+    return dense_gemm(xq, wq, M, N, K, y, N, st);
+}
+
+mxq_status mxq_linear_bwd_dx(const void *dy, const void *w, int64_t M, int64_t N, int64_t K, mxq_mode mode, void *ctx,
+                             void *dx, void *workspace, size_t ws_bytes, mxq_stream_t stream) {
+    mxq_status s = check_linear(dy, w, M, N, K, mode, ctx, dx, workspace, ws_bytes, ws_dx(M, N, K, mode));
+    if (s != MXQ_OK) return s;
+    if ((s = check_arch()) != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *cp = static_cast<uint8_t *>(ctx);
+    Operand wT{};
+    if (mode == MXQ_SAVE_QUANT) {
+        (void)carve(cp, K, M);
+        wT = carve(cp, K, N);
+    }
+    const Operand dyT = carve(cp, N, M);
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    const Operand dyq = carve(wp, M, N);
+    cudaError_t e = mxq::launch_quant_cols(static_cast<const uint16_t *>(dy), M, N, N, dyq.q, dyq.s, dyT.q, dyT.s, st);
+    if (e == cudaSuccess && mode == MXQ_RECOMPUTE) {
+        wT = carve(wp, K, N);
+        e = mxq::launch_quant_cols(static_cast<const uint16_t *>(w), N, K, K, nullptr, nullptr, wT.q, wT.s, st);
+    }
+    if (e != cudaSuccess) return cuda_result(e, "mxq_linear_bwd_dx quant launch");
+    return dense_gemm(dyq, wT, M, K, N, dx, K, st);
+}
+
+mxq_status mxq_linear_bwd_dw(const void *dy, const void *x, int64_t M, int64_t N, int64_t K, mxq_mode mode, void *ctx,
+                             void *dw, void *workspace, size_t ws_bytes, mxq_stream_t stream) {
+    mxq_status s = check_linear(dy, x, M, N, K, mode, ctx, dw, workspace, ws_bytes, ws_dw(M, N, K, mode));
+    if (s != MXQ_OK) return s;
+    if ((s = check_arch()) != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *cp = static_cast<uint8_t *>(ctx);
+    Operand xT{};
+    if (mode == MXQ_SAVE_QUANT) {
+        xT = carve(cp, K, M);
+        (void)carve(cp, K, N);
+    }
+    const Operand dyT = carve(cp, N, M);
+    if (mode == MXQ_RECOMPUTE) {
+        uint8_t *wp = static_cast<uint8_t *>(workspace);
+        xT = carve(wp, K, M);
+        cudaError_t e = mxq::launch_quant_cols(static_cast<const uint16_t *>(x), M, K, K, nullptr, nullptr, xT.q, xT.s, st);
+        if (e != cudaSuccess) return cuda_result(e, "mxq_linear_bwd_dw quant launch");
+    }
+    return dense_gemm(dyT, xT, N, K, M, dw, K, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// mxq_internal.h -- kernel launchers shared between the libmxq translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxq {
+
+// ---- quantization (mxq_quant.cu) ----
+// fmt 0: MXFP8 (bf16 in), fmt 1: MXFP4 packed (bf16 or fp32 in).  cols % 32 == 0.
+cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, int64_t C, int64_t ldx,
+                              uint8_t *q, uint8_t *s, cudaStream_t st);
+// Column MXFP8 quant of bf16 x; q_row/s_row non-null adds the row quant (dual).
+cudaError_t launch_quant_cols(const uint16_t *x, int64_t R, int64_t C, int64_t ldx, uint8_t *q_row,
+                              uint8_t *s_row, uint8_t *qT, uint8_t *sT, cudaStream_t st);
+cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, const int64_t *d_off, int E,
+                                      int64_t t_pad, uint8_t *qT, uint8_t *sT, cudaStream_t st);
+cudaError_t launch_qdq_mxfp4(const float *x, float *y, int64_t rows, int64_t cols, float sf, cudaStream_t st);
+
+// ---- GEMM (mxq_gemm.cu) ----
+enum GemmMode { kDense = 0, kGroupedRows = 1, kGroupedK = 2 };
+
+struct GemmProblem {
+    GemmMode mode;
+    // A: [a_rows x a_k] E4M3 codes, K-major; scales swz(a_rows, a_k/32)
+    const uint8_t *a, *sa;
+    int64_t a_rows, a_k;
+    // B: [b_rows x b_k] E4M3 codes, K-major; scales swz(b_rows, b_k/32)
+    const uint8_t *b, *sb;
+    int64_t b_rows, b_k;
+    // output bf16: M x N per problem (per expert in kGroupedK), leading dim ldc
+    void *c;
+    int64_t M, N, ldc;
+    int64_t K;  // contraction length (kDense / kGroupedRows)
+    // grouped
+    const int64_t *offsets;   // device, E+1
+    int E;
+    int64_t b_row_per_expert; // kGroupedRows: B row offset of expert e = e * this
+    int64_t b_k_per_expert;   // kGroupedRows: B contraction offset of expert e = e * this
+    int64_t c_expert_stride;  // kGroupedK: elements between experts' outputs
+    int64_t T;                // kGroupedRows: token rows (= off[E])
+};
+cudaError_t launch_gemm(const GemmProblem &p, cudaStream_t st);
+// Reads the device error word set by bounded waits that gave up, then clears it.
+cudaError_t read_and_clear_device_error(unsigned int *word);
+
+}  // namespace mxq

@@ -1,0 +1,515 @@
+// mxq_quant.cu -- single-pass MX quantization kernels (HBM-bound).
+//
+// MXFP8 ("低精度训练特性（MXFP8 / HiFloat8）", section "线性层低精度", MXFP8 mode:
+// blocks of 32 elements share one scale) with the OCP MX rule: scale 2^X,
+// X = floor(log2 amax) - 8 clamped to [-127, 127] (-127 for an all-zero
+// block), codes E4M3(x * 2^-X) by cvt.rn.satfinite (nearest-even, saturating
+// to +-448).  MXFP4 ("AMCT FakeQuant 模拟伪量化工具包", section 2): scale
+// 2^round(log2(max(amax/sf, 2^-30))) decided exactly with integer arithmetic,
+// elements snapped to the E2M1 codebook with midpoints rounding away from zero.
+//
+// Layout of the work: a CTA owns a 128 x 128 tile of the input, which makes
+// exactly one 512-byte scale tile per output axis, so scales are staged in
+// shared memory and written with coalesced 16-byte stores directly in the
+// tcgen05 block-scale layout.  Data moves with 16-byte vector loads/stores;
+// the column (transposed) output goes through a shared-memory copy of the tile
+// read back as 32-bit column pairs (conflict-free).
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "mxq_device.cuh"
+#include "mxq_internal.h"
+
+namespace mxq {
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void stg_v4(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Two fp32 values -> two E4M3 codes (lo in the low byte), RNE + satfinite.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
+}
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------- MXFP8 scale
+// X from the magnitude bits of a bf16 amax; 128 marks a non-finite block.
+__device__ __forceinline__ int mx8_exp_from_bf16(uint32_t a) {
+    if (a >= 0x7F80u) return 128;
+    if (a == 0) return -127;
+    const int E = static_cast<int>(a >> 7);
+    const int fl = E ? E - 127 : -133 + (31 - __clz(static_cast<int>(a)));
+    return max(fl - 8, -127);  // fl <= 127 so X <= 119
+}
+__device__ __forceinline__ uint8_t mx8_scale_byte(int X) { return X > 127 ? 0xFF : static_cast<uint8_t>(X + 127); }
+// 2^-X as fp32 (a normal number for X in [-127, 119]).
+__device__ __forceinline__ float pow2_neg(int X) { return __uint_as_float(static_cast<uint32_t>(127 - X) << 23); }
+
+// E4M3 codes of 8 bf16 (4 packed words, element 2k in the low half of word k).
+__device__ __forceinline__ uint2 e4m3_codes8(const uint32_t (&w)[4], int X) {
+    uint2 out;
+    if (X > 127) {  // non-finite block: every code NaN, sign kept
+        uint32_t b[8];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            b[2 * k] = 0x7Fu | ((w[k] >> 8) & 0x80u);
+            b[2 * k + 1] = 0x7Fu | ((w[k] >> 24) & 0x80u);
+        }
+        out.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+        out.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+        return out;
+    }
+    const float inv = pow2_neg(X);
+    out.x = e4m3x4(bf16lo(w[0]) * inv, bf16hi(w[0]) * inv, bf16lo(w[1]) * inv, bf16hi(w[1]) * inv);
+    out.y = e4m3x4(bf16lo(w[2]) * inv, bf16hi(w[2]) * inv, bf16lo(w[3]) * inv, bf16hi(w[3]) * inv);
+    return out;
+}
+
+// Max over the 8 bf16 magnitudes of a 16-byte chunk (integer compare of |bits|).
+__device__ __forceinline__ uint32_t amax8_bf16(const uint32_t (&w)[4]) {
+    const uint32_t m = 0x7FFF7FFFu;
+    const uint32_t t = __vmaxu2(__vmaxu2(w[0] & m, w[1] & m), __vmaxu2(w[2] & m, w[3] & m));
+    return max(t & 0xFFFFu, t >> 16);
+}
+
+// ---------------------------------------------------------------- MXFP4 scale
+// e = round(log2(max(amax/sf, 2^-30))) exactly, capped at 127; amax finite
+// >= 0, sf finite > 0.
+__device__ __forceinline__ int mx4_exp(float amax, float sf) {
+    if (amax == 0.0f) return -30;
+    const uint32_t ab = __float_as_uint(amax), sb = __float_as_uint(sf);
+    int ea = static_cast<int>(ab >> 23), es = static_cast<int>(sb >> 23);
+    uint32_t ma = ab & 0x7FFFFFu, ms = sb & 0x7FFFFFu;
+    // value = M * 2^(e-150) with M in [2^23, 2^24)
+    if (ea == 0) { const int sh = __clz(static_cast<int>(ma)) - 8; ma <<= sh; ea = 1 - sh; } else { ma |= 0x800000u; }
+    if (es == 0) { const int sh = __clz(static_cast<int>(ms)) - 8; ms <<= sh; es = 1 - sh; } else { ms |= 0x800000u; }
+    const int d = ma < ms ? 1 : 0;
+    const int e0 = ea - es - d;                       // floor(log2(amax/sf))
+    if (e0 < -30) return -30;                         // clamp at 2^-30
+    // q = (ma/ms) * 2^d in [1, 2) is amax/sf / 2^e0: round up iff q^2 >= 2
+    const unsigned long long lhs = (static_cast<unsigned long long>(ma) * ma) << (2 * d);
+    const unsigned long long rhs = 2ull * ms * ms;
+    const int e = lhs >= rhs ? e0 + 1 : e0;
+    return min(e, 127);
+}
+__device__ __forceinline__ float pow2(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
+
+struct E2M1Thr {
+    float t[7];  // midpoints * 2^e
+    float s;     // 2^e
+};
+__device__ __forceinline__ E2M1Thr e2m1_thresholds(int e) {
+    E2M1Thr r;
+    r.s = pow2(e);
+    r.t[0] = 0.25f * r.s; r.t[1] = 0.75f * r.s; r.t[2] = 1.25f * r.s; r.t[3] = 1.75f * r.s;
+    r.t[4] = 2.5f * r.s;  r.t[5] = 3.5f * r.s;  r.t[6] = 5.0f * r.s;
+    return r;
+}
+// Codebook index of |x|: the number of midpoints <= |x| / 2^e (exact compare).
+__device__ __forceinline__ uint32_t e2m1_index(float ax, const E2M1Thr &T) {
+    uint32_t i = 0;
+#pragma unroll
+    for (int k = 0; k < 7; k++) i += ax >= T.t[k] ? 1u : 0u;
+    return i;
+}
+// {0, .5, 1, 1.5, 2, 3, 4, 6}
+__device__ __forceinline__ float e2m1_value(uint32_t i) {
+    return i < 5 ? 0.5f * static_cast<float>(i) : (i == 7 ? 6.0f : static_cast<float>(i) - 2.0f);
+}
+__device__ __forceinline__ float qdq_one(float x, const E2M1Thr &T) {
+    const float ax = fabsf(x);
+    return copysignf(e2m1_value(e2m1_index(ax, T)) * T.s, x);
+}
+
+// ============================================================================
+// Row quant: 128 x 128 tile per CTA, blocks along cols (cols % 32 == 0).
+//   FMT 0: bf16 -> E4M3 codes [R x C]      FMT 1: bf16/fp32 -> E2M1 [R x C/2]
+// Each thread owns 8 chunks of 8 elements; 4 lanes form one 32-block.
+// ============================================================================
+template <typename InT, int FMT>
+__global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__ x, int64_t R, int64_t C,
+                                                         int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
+                                                         uint8_t *__restrict__ s, int64_t kb_tiles) {
+    __shared__ __align__(16) uint8_t satom[512];
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile, c0 = static_cast<int64_t>(blockIdx.x) * kTile;
+#pragma unroll 2
+    for (int i = 0; i < 8; i++) {
+        const int id = tid + kThreads * i;
+        const int row = id >> 4, ch = id & 15, col = ch * 8;
+        const int64_t gr = r0 + row, gc = c0 + col;
+        const bool valid = gr < R && gc < C;
+        uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // bf16: 4 words used; fp32: 8 words
+        if (valid) {
+            const InT *src = x + gr * ldx + gc;
+            const uint4 a = ldg_nc_v4(src);
+            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+            if (sizeof(InT) == 4) {
+                const uint4 b = ldg_nc_v4(reinterpret_cast<const float *>(src) + 4);
+                w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+            }
+        }
+        uint8_t sbyte;
+        if (FMT == 0) {
+            const uint32_t (&w4)[4] = *reinterpret_cast<const uint32_t(*)[4]>(w);
+            uint32_t a = amax8_bf16(w4);
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            const int X = mx8_exp_from_bf16(a);
+            sbyte = mx8_scale_byte(X);
+            if (valid) {
+                const uint2 codes = e4m3_codes8(w4, X);
+                asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(q + gr * ldq + gc), "r"(codes.x), "r"(codes.y)
+                             : "memory");
+            }
+        } else {
+            float v[8];
+            uint32_t a = 0;
+            if (sizeof(InT) == 2) {
+#pragma unroll
+                for (int k = 0; k < 4; k++) { v[2 * k] = bf16lo(w[k]); v[2 * k + 1] = bf16hi(w[k]); }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; k++) v[k] = __uint_as_float(w[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; k++) a = max(a, __float_as_uint(v[k]) & 0x7FFFFFFFu);
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            const bool nonfinite = a >= 0x7F800000u;
+            const int e = nonfinite ? 0 : mx4_exp(__uint_as_float(a), 6.0f);
+            sbyte = nonfinite ? 0xFF : static_cast<uint8_t>(e + 127);
+            const E2M1Thr T = e2m1_thresholds(e);
+            uint32_t packed = 0;
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const uint32_t idx = nonfinite ? 7u : e2m1_index(fabsf(v[k]), T);
+                const uint32_t nib = ((__float_as_uint(v[k]) >> 28) & 8u) | idx;
+                packed |= nib << (4 * k);
+            }
+            if (valid) {
+                asm volatile("st.global.u32 [%0], %1;" ::"l"(q + gr * ldq + gc / 2), "r"(packed) : "memory");
+            }
+        }
+        if (!valid) sbyte = 0;  // padding rows / blocks of the scale tile
+        if ((lane & 3) == 0) satom[16 * (row & 31) + 4 * (row >> 5) + (ch >> 2)] = sbyte;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(satom + 16 * tid);
+        stg_v4(s + (static_cast<int64_t>(blockIdx.y) * kb_tiles + blockIdx.x) * 512 + 16 * tid, v);
+    }
+}
+
+// ============================================================================
+// Column quant (optionally dual): 128 x 128 bf16 tile per CTA.
+//   ROWS:    also emit the row quant (dual-axis, one read of x).
+//   GROUPED: tile rows come from one group of a per-group column quant; the
+//            padded tile index selects the group, blocks restart at the
+//            group start and padding rows are zero.
+// The column pass: thread (p, b) = (column pair 0..63, 32-row block 0..3)
+// reads 32 words of the shared tile, one per row.
+// ============================================================================
+struct ColParams {
+    const uint16_t *x;
+    int64_t R, C, ldx;
+    uint8_t *q_row;      // [R x C]               (ROWS)
+    uint8_t *s_row;      // swz(R, C/32)           (ROWS)
+    int64_t kb_row_tiles;
+    uint8_t *qT;         // [C x ldqT]
+    uint8_t *sT;         // swz(C, ldqT/32)
+    int64_t ldqT;
+    int64_t kb_col_tiles;
+    const int64_t *offsets;  // GROUPED: E+1 device offsets
+    int E;
+};
+
+template <bool ROWS, bool GROUPED>
+__global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
+    __shared__ __align__(16) uint8_t tile[kTile * kTile * 2];
+    __shared__ __align__(16) uint8_t srow_atom[512];
+    __shared__ __align__(16) uint8_t scol_atom[512];
+    __shared__ int64_t sh_src0;
+    __shared__ int sh_nvalid;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t rt = blockIdx.y, ct = blockIdx.x;
+    const int64_t c0 = ct * kTile;
+    int64_t src0 = rt * kTile;  // first source row of the tile
+    int nvalid;                 // rows of the tile that hold data
+    if (GROUPED) {
+        if (tid == 0) sh_nvalid = 0;
+        __syncwarp();
+        if (warp == 0) {
+            const int64_t t0 = rt * kTile;  // padded row of the tile
+            int64_t run = 0;
+            for (int base = 0; base < P.E; base += 32) {
+                const int e = base + lane;
+                int64_t n = 0;
+                if (e < P.E) n = P.offsets[e + 1] - P.offsets[e];
+                const int64_t padn = (n + 127) / 128 * 128;
+                int64_t incl = padn;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                const int64_t start = run + incl - padn;
+                if (e < P.E && padn > 0 && t0 >= start && t0 < start + padn) {
+                    sh_src0 = P.offsets[e] + (t0 - start);
+                    const int64_t left = n - (t0 - start);
+                    sh_nvalid = static_cast<int>(left < kTile ? left : kTile);
+                }
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+        __syncthreads();
+        src0 = sh_src0;
+        nvalid = sh_nvalid;
+    } else {
+        const int64_t left = P.R - src0;
+        nvalid = static_cast<int>(left < kTile ? left : kTile);
+    }
+
+    // ---- load the tile (and the row quant) ----
+#pragma unroll 2
+    for (int i = 0; i < 8; i++) {
+        const int id = tid + kThreads * i;
+        const int row = id >> 4, ch = id & 15, col = ch * 8;
+        const int64_t gc = c0 + col;
+        const bool valid = row < nvalid && gc < P.C;
+        uint32_t w[4] = {0, 0, 0, 0};
+        if (valid) {
+            const uint4 a = ldg_nc_v4(P.x + (src0 + row) * P.ldx + gc);
+            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        }
+        if (ROWS) {
+            uint32_t a = amax8_bf16(w);
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            const int X = mx8_exp_from_bf16(a);
+            if (valid) {
+                const uint2 codes = e4m3_codes8(w, X);
+                asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(P.q_row + (src0 + row) * P.C + gc),
+                             "r"(codes.x), "r"(codes.y)
+                             : "memory");
+            }
+            if ((lane & 3) == 0) srow_atom[16 * (row & 31) + 4 * (row >> 5) + (ch >> 2)] = mx8_scale_byte(X);
+        }
+        *reinterpret_cast<uint4 *>(tile + row * (kTile * 2) + ch * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+
+    // ---- column pass ----
+    {
+        const int p = tid & 63, b = tid >> 6;  // column pair, 32-row block
+        uint32_t col[32];
+#pragma unroll
+        for (int i = 0; i < 32; i++) col[i] = *reinterpret_cast<const uint32_t *>(tile + (32 * b + i) * (kTile * 2) + 4 * p);
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int i = 0; i < 32; i++) m2 = __vmaxu2(m2, col[i] & 0x7FFF7FFFu);
+        const int Xlo = mx8_exp_from_bf16(m2 & 0xFFFFu), Xhi = mx8_exp_from_bf16(m2 >> 16);
+        const int cl = 2 * p, ch2 = 2 * p + 1;
+        scol_atom[16 * (cl & 31) + 4 * (cl >> 5) + b] = mx8_scale_byte(Xlo);
+        scol_atom[16 * (ch2 & 31) + 4 * (ch2 >> 5) + b] = mx8_scale_byte(Xhi);
+
+        const int64_t gcol = c0 + cl;
+        if (gcol < P.C) {
+            uint32_t lo[8], hi[8];
+            const float ilo = pow2_neg(Xlo > 127 ? 0 : Xlo), ihi = pow2_neg(Xhi > 127 ? 0 : Xhi);
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const uint32_t a0 = col[4 * k], a1 = col[4 * k + 1], a2 = col[4 * k + 2], a3 = col[4 * k + 3];
+                lo[k] = e4m3x4(bf16lo(a0) * ilo, bf16lo(a1) * ilo, bf16lo(a2) * ilo, bf16lo(a3) * ilo);
+                hi[k] = e4m3x4(bf16hi(a0) * ihi, bf16hi(a1) * ihi, bf16hi(a2) * ihi, bf16hi(a3) * ihi);
+            }
+            if (Xlo > 127 || Xhi > 127) {  // non-finite blocks: NaN codes with the sign kept
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    uint32_t sl = 0, sh = 0;
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        sl |= (0x7Fu | ((col[4 * k + j] >> 8) & 0x80u)) << (8 * j);
+                        sh |= (0x7Fu | ((col[4 * k + j] >> 24) & 0x80u)) << (8 * j);
+                    }
+                    if (Xlo > 127) lo[k] = sl;
+                    if (Xhi > 127) hi[k] = sh;
+                }
+            }
+            const int64_t pos = rt * kTile + 32 * b;  // first output column (token) of the block
+            uint8_t *dlo = P.qT + gcol * P.ldqT + pos;
+            uint8_t *dhi = dlo + P.ldqT;
+            const int64_t limit = GROUPED ? P.ldqT : P.R;  // grouped tiles write padding zeros too
+            if (pos + 32 <= limit && (P.ldqT & 15) == 0) {
+                stg_v4(dlo, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+                stg_v4(dlo + 16, make_uint4(lo[4], lo[5], lo[6], lo[7]));
+                stg_v4(dhi, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+                stg_v4(dhi + 16, make_uint4(hi[4], hi[5], hi[6], hi[7]));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; j++) {
+                    if (pos + j < limit) {
+                        dlo[j] = static_cast<uint8_t>(lo[j >> 2] >> (8 * (j & 3)));
+                        dhi[j] = static_cast<uint8_t>(hi[j >> 2] >> (8 * (j & 3)));
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (ROWS && tid < 32) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(srow_atom + 16 * tid);
+        stg_v4(P.s_row + (rt * P.kb_row_tiles + ct) * 512 + 16 * tid, v);
+    } else if (tid >= 32 && tid < 64) {
+        const int l = tid - 32;
+        const uint4 v = *reinterpret_cast<const uint4 *>(scol_atom + 16 * l);
+        stg_v4(P.sT + (ct * P.kb_col_tiles + rt) * 512 + 16 * l, v);
+    }
+}
+
+// ============================================================================
+// MXFP4 quant-dequant.
+//  Vector path (cols % 32 == 0, 16-byte aligned): 8 floats per thread, 4
+//  lanes per block.  General path: one warp per block of 32 (ragged rows).
+// Warp-uniform grid-stride loops so that every shuffle has all 32 lanes.
+// ============================================================================
+__global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restrict__ x, float *y, int64_t nchunks,
+                                                            float sf) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t wstride = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+    for (int64_t wb = warp0 * 32; wb < nchunks; wb += wstride * 32) {
+        const int64_t g = wb + lane;
+        const bool valid = g < nchunks;
+        float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (valid) {
+            const uint4 a = ldg_nc_v4(x + 8 * g), b = ldg_nc_v4(x + 8 * g + 4);
+            v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+            v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+        }
+        uint32_t a = 0;
+#pragma unroll
+        for (int k = 0; k < 8; k++) a = max(a, __float_as_uint(v[k]) & 0x7FFFFFFFu);
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        if (!valid) continue;
+        float o[8];
+        if (a >= 0x7F800000u) {
+#pragma unroll
+            for (int k = 0; k < 8; k++) o[k] = __uint_as_float(0x7FC00000u);
+        } else {
+            const E2M1Thr T = e2m1_thresholds(mx4_exp(__uint_as_float(a), sf));
+#pragma unroll
+            for (int k = 0; k < 8; k++) o[k] = qdq_one(v[k], T);
+        }
+        stg_v4(y + 8 * g, make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3])));
+        stg_v4(y + 8 * g + 4, make_uint4(__float_as_uint(o[4]), __float_as_uint(o[5]), __float_as_uint(o[6]), __float_as_uint(o[7])));
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restrict__ x, float *y, int64_t rows,
+                                                            int64_t cols, float sf) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nb = (cols + 31) / 32;
+    const int64_t nblocks = rows * nb;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t wstride = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+    for (int64_t k = warp0; k < nblocks; k += wstride) {
+        const int64_t r = k / nb, b = k % nb;
+        const int64_t c = 32 * b + lane;
+        const bool valid = c < cols;
+        const float v = valid ? x[r * cols + c] : 0.0f;
+        uint32_t a = __float_as_uint(v) & 0x7FFFFFFFu;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if (!valid) continue;
+        float out;
+        if (a >= 0x7F800000u) {
+            out = __uint_as_float(0x7FC00000u);
+        } else {
+            const E2M1Thr T = e2m1_thresholds(mx4_exp(__uint_as_float(a), sf));
+            out = qdq_one(v, T);
+        }
+        y[r * cols + c] = out;
+    }
+}
+
+int grid_for(int64_t work_items, int per_cta) {
+    int64_t g = (work_items + per_cta - 1) / per_cta;
+    const int64_t cap = 152 * 16;
+    if (g > cap) g = cap;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, int64_t C, int64_t ldx, uint8_t *q,
+                              uint8_t *s, cudaStream_t st) {
+    const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((R + kTile - 1) / kTile));
+    const int64_t kb_tiles = ((C / 32) + 3) / 4;
+    if (fmt == 0) {
+        k_quant_rows<uint16_t, 0><<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(x), R, C, ldx, q, C, s, kb_tiles);
+    } else if (fp32_in) {
+        k_quant_rows<float, 1><<<grid, kThreads, 0, st>>>(static_cast<const float *>(x), R, C, ldx, q, C / 2, s, kb_tiles);
+    } else {
+        k_quant_rows<uint16_t, 1><<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(x), R, C, ldx, q, C / 2, s, kb_tiles);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_cols(const uint16_t *x, int64_t R, int64_t C, int64_t ldx, uint8_t *q_row, uint8_t *s_row,
+                              uint8_t *qT, uint8_t *sT, cudaStream_t st) {
+    ColParams P{};
+    P.x = x; P.R = R; P.C = C; P.ldx = ldx;
+    P.q_row = q_row; P.s_row = s_row; P.kb_row_tiles = ((C / 32) + 3) / 4;
+    P.qT = qT; P.sT = sT; P.ldqT = R; P.kb_col_tiles = (((R + 31) / 32) + 3) / 4;
+    const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((R + kTile - 1) / kTile));
+    if (q_row) k_quant_cols<true, false><<<grid, kThreads, 0, st>>>(P);
+    else k_quant_cols<false, false><<<grid, kThreads, 0, st>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, const int64_t *d_off, int E,
+                                      int64_t t_pad, uint8_t *qT, uint8_t *sT, cudaStream_t st) {
+    ColParams P{};
+    P.x = x; P.R = T; P.C = C; P.ldx = C;
+    P.qT = qT; P.sT = sT; P.ldqT = t_pad; P.kb_col_tiles = (t_pad / 32 + 3) / 4;
+    P.offsets = d_off; P.E = E;
+    const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>(t_pad / kTile));
+    k_quant_cols<false, true><<<grid, kThreads, 0, st>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qdq_mxfp4(const float *x, float *y, int64_t rows, int64_t cols, float sf, cudaStream_t st) {
+    const bool vec = (cols % 32 == 0) && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) == 0;
+    if (vec) {
+        const int64_t nchunks = rows * cols / 8;
+        k_qdq_mxfp4_vec<<<grid_for(nchunks, kThreads * 2), kThreads, 0, st>>>(x, y, nchunks, sf);
+    } else {
+        const int64_t nblocks = rows * ((cols + 31) / 32);
+        k_qdq_mxfp4_gen<<<grid_for(nblocks, kThreads / 32), kThreads, 0, st>>>(x, y, rows, cols, sf);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mxq

@@ -249,7 +249,11 @@ int oracle_mxfp4_scale_exp(double amax, double sf)
      * (24-bit significands squared, power-of-two scaling). */
     double lhs = amax * amax;
     double rhs = ldexp(sf * sf, 2 * e0 + 1);
-    return (lhs >= rhs) ? e0 + 1 : e0;
+    int e = (lhs >= rhs) ? e0 + 1 : e0;
+    /* Reading: capped at 2^127, the largest power of two an E8M0 byte holds
+     * (reached only when amax/sf > 2^126.5, i.e. scale_factor < ~2.8 with
+     * amax near the fp32 maximum; the pages give no upper clamp). */
+    return e > 127 ? 127 : e;
 }
 
 /* Index into the E2M1 codebook of |x| / 2^e: the number of midpoints <= y. */

@@ -1,0 +1,89 @@
+"""The C ABI library: builds, loads without a GPU, exports every symbol its
+header declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mx_block_scaled_mxq_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mxq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxq_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return m.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 15
+    raw = ctypes.CDLL(m.library_path())
+    for n in names:
+        assert hasattr(raw, n), n
+        assert n in m.__all__, f"binding lacks {n}"
+
+
+def test_size_queries(lib):
+    assert m.mxq_scale_bytes(128, 4) == 512
+    assert m.mxq_scale_bytes(130, 5) == 256 * 8
+    assert m.mxq_scale_bytes(0, 4) == 0
+    assert m.mxq_grouped_padded_rows(32768, 32) == 128 * (256 + 32)
+    M, N, K = 8192, 14336, 4096
+    saved = m.mxq_linear_saved_bytes(M, N, K, m.SAVE_QUANT)
+    # (M*K + N*K) codes + their scales, each rounded to 256 bytes
+    assert saved == M * K + K * (M // 32) + N * K + K * (N // 32)
+    assert m.mxq_linear_saved_bytes(M, N, K, m.RECOMPUTE) == 0
+    assert m.mxq_linear_ctx_bytes(M, N, K, m.RECOMPUTE) == N * M + N * (M // 32)
+    assert m.mxq_linear_workspace_bytes(M, N, K, m.RECOMPUTE) >= m.mxq_linear_workspace_bytes(M, N, K, m.SAVE_QUANT)
+
+
+def _status(fn, *args):
+    try:
+        fn(*args)
+    except m.MXQError as e:
+        return e.status
+    return 0
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced by a rejected call
+
+
+def test_host_validation_rejects_before_launch(lib):
+    INV, UNS = 1, 2
+    # GEMM: K must be a positive multiple of 32, ldc >= N, pointers aligned
+    assert _status(m.mxq_gemm, FAKE, FAKE, FAKE, FAKE, 128, 128, 33, FAKE, 128, 0) == INV
+    assert _status(m.mxq_gemm, FAKE, FAKE, FAKE, FAKE, 128, 128, 64, FAKE, 64, 0) == INV
+    assert _status(m.mxq_gemm, FAKE + 4, FAKE, FAKE, FAKE, 128, 128, 64, FAKE, 128, 0) == INV
+    assert _status(m.mxq_gemm, None, FAKE, FAKE, FAKE, 128, 128, 64, FAKE, 128, 0) == INV
+    # MXFP4 QDQ: block size 32 only, scale_factor > 0 (AMCT wrapper / config checks)
+    assert _status(m.mxq_qdq_mxfp4, FAKE, FAKE, 4, 64, 16, 6.0, 0) == UNS
+    assert _status(m.mxq_qdq_mxfp4, FAKE, FAKE, 4, 64, 32, 0.0, 0) == INV
+    assert _status(m.mxq_qdq_mxfp4, FAKE, FAKE, 4, 64, 32, -1.0, 0) == INV
+    assert _status(m.mxq_qdq_mxfp4, FAKE, FAKE, 4, 64, 32, float("nan"), 0) == INV
+    # quantize: MXFP8 needs bf16, E2M1 is last-axis only, block axis multiple of 32
+    assert _status(m.mxq_quantize, FAKE, m.F32, 64, 64, 64, -1, m.E4M3, 0, FAKE, FAKE, None, None, 0) == UNS
+    assert _status(m.mxq_quantize, FAKE, m.BF16, 64, 64, 64, -2, m.E2M1, 0, None, None, FAKE, FAKE, 0) == UNS
+    assert _status(m.mxq_quantize, FAKE, m.BF16, 64, 48, 48, -1, m.E4M3, 0, FAKE, FAKE, None, None, 0) == INV
+    assert _status(m.mxq_quantize, FAKE, m.BF16, 64, 64, 64, 0, m.E4M3, 0, FAKE, FAKE, None, None, 0) == INV
+    assert _status(m.mxq_quantize, FAKE, m.BF16, 64, 64, 64, -1, m.E4M3, 0, None, FAKE, None, None, 0) == INV
+    # empty input is a no-op that succeeds without touching the device
+    assert _status(m.mxq_quantize, None, m.BF16, 0, 64, 64, -1, m.E4M3, 0, None, None, None, None, 0) == 0
+    assert _status(m.mxq_gemm, None, None, None, None, 0, 0, 64, None, 0, 0) == 0
+    # grouped: E range, t_pad capacity, N multiple of 128 for FWD/DX
+    assert _status(m.mxq_quantize_grouped_col, FAKE, 100, 64, FAKE, 0, 1024, FAKE, FAKE, 0) == INV
+    assert _status(m.mxq_quantize_grouped_col, FAKE, 1000, 64, FAKE, 4, 1024, FAKE, FAKE, 0) == INV
+    assert _status(m.mxq_grouped_gemm, m.GG_FWD, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 192, 64, 0, FAKE, 0) == INV
+    assert _status(m.mxq_grouped_gemm, m.GG_DW, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 128, 64, 100, FAKE, 0) == INV
+    # linear: dimensions multiple of 32, workspace large enough
+    assert _status(m.mxq_linear_fwd, FAKE, FAKE, 100, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 1 << 30, 0) == INV
+    assert _status(m.mxq_linear_fwd, FAKE, FAKE, 64, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 16, 0) == INV
+    assert _status(m.mxq_linear_fwd, FAKE, FAKE, 64, 64, 64, 7, FAKE, FAKE, FAKE, 1 << 30, 0) == INV
+    assert "workspace" in m.mxq_last_error_string() or "mode" in m.mxq_last_error_string()

@@ -1,0 +1,151 @@
+"""GPU parity of the quantization kernels against the CPU oracle: codes and
+scales must be bit-identical (every byte of the padded scale buffers too)."""
+import numpy as np
+import pytest
+import torch
+
+import mxq_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _inputs(R, C, kind, seed):
+    if kind == "normal":
+        return mxq_inputs.normal_bf16((R, C), 1.0, seed=seed)
+    x = mxq_inputs.sweep_bf16(R, C, seed=seed)            # heavy tail, 1000x outliers
+    if R >= 4 and C >= 64:
+        x[1, :32] = 0                                      # an all-zero row block
+        x[2, 32:64] = -0.0                                 # negative zeros
+        x[:32, 3] = 0                                      # an all-zero column block
+        x[0, 0] = 3.0e38                                   # near the bf16 maximum
+        x[3, 5] = 1e-40                                    # a bf16 subnormal
+    return x
+
+
+ROW_SHAPES = [(256, 512), (512, 512), (100, 96), (1, 32), (129, 160), (384, 4096), (128, 128)]
+
+
+@pytest.mark.parametrize("R,C", ROW_SHAPES)
+@pytest.mark.parametrize("kind", ["normal", "heavy"])
+def test_row_quant_bit_exact(mxq, R, C, kind):
+    x = _inputs(R, C, kind, seed=R + C)
+    q, s, _, _ = mxq.quantize_mxfp8(x.to(DEV), axis=-1)
+    oq, os_ = oracle.mxfp8_quant_rows(x)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
+
+
+COL_SHAPES = [(256, 512), (96, 64), (100, 64), (130, 136), (33, 8), (1, 32), (4096, 384), (200, 1024)]
+
+
+@pytest.mark.parametrize("R,C", COL_SHAPES)
+@pytest.mark.parametrize("dual", [False, True])
+def test_col_and_dual_quant_bit_exact(mxq, R, C, dual):
+    if dual and C % 32:
+        pytest.skip("row axis needs cols % 32 == 0")
+    x = _inputs(R, C, "heavy", seed=3 * R + C)
+    q, s, qT, sT = mxq.quantize_mxfp8(x.to(DEV), axis=-2, dual=dual)
+    oqT, osT = oracle.mxfp8_quant_cols(x)
+    assert np.array_equal(qT.cpu().numpy(), oqT)
+    assert np.array_equal(sT.cpu().numpy(), oracle.swizzle_scales(osT))
+    if dual:
+        oq, os_ = oracle.mxfp8_quant_rows(x)
+        assert np.array_equal(q.cpu().numpy(), oq)
+        assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
+
+
+def _grouped(mxq, x, off):
+    T, C = x.shape
+    E = len(off) - 1
+    t_pad = mxq.mxq_grouped_padded_rows(T, E)
+    qT = torch.full((C, t_pad), 0xAB, dtype=torch.uint8, device=DEV)     # poison: every byte must be written
+    sT = torch.full((mxq.mxq_scale_bytes(C, t_pad // 32),), 0xAB, dtype=torch.uint8, device=DEV)
+    d_off = torch.from_numpy(off).to(DEV)
+    mxq.mxq_quantize_grouped_col(x.to(DEV), T, C, d_off, E, t_pad, qT, sT)
+    return qT.cpu().numpy(), sT.cpu().numpy(), t_pad
+
+
+@pytest.mark.parametrize("sizes", [[0, 5, 128, 33, 0, 200, 1], [300], [0, 0, 64], [1] * 40])
+def test_grouped_col_quant_bit_exact(mxq, sizes):
+    off = mxq_inputs.offsets_from_sizes(sizes)
+    x = _inputs(int(off[-1]), 136, "heavy", seed=len(sizes))
+    qT, sT, t_pad = _grouped(mxq, x, off)
+    oqT, osT = oracle.mxfp8_quant_cols_grouped(x, off, t_pad)
+    assert np.array_equal(qT, oqT)
+    assert np.array_equal(sT, oracle.swizzle_scales(osT))
+
+
+def test_grouped_col_quant_dirichlet(mxq):
+    n = mxq_inputs.dirichlet_group_sizes(32, 4096, 0.5, seed=0)
+    assert (n == 0).any() or n.min() < 40         # the recipe gives tiny / empty groups
+    off = mxq_inputs.offsets_from_sizes(n)
+    x = mxq_inputs.normal_bf16((4096, 512), 1e-3, seed=2)
+    qT, sT, t_pad = _grouped(mxq, x, off)
+    oqT, osT = oracle.mxfp8_quant_cols_grouped(x, off, t_pad)
+    assert np.array_equal(qT, oqT)
+    assert np.array_equal(sT, oracle.swizzle_scales(osT))
+
+
+# ------------------------------------------------------------------ MXFP4
+
+def _read_shapes():
+    import os
+    rows = []
+    with open(os.path.join(os.path.dirname(__file__), "golden", "mxfp4_ragged_shapes.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append(tuple(int(v) for v in line.split()))
+    return rows
+
+
+@pytest.mark.parametrize("shape", _read_shapes() + [(5, 64), (7, 1), (3, 95)])
+@pytest.mark.parametrize("sf", [6.0, 4.0, 6.0 / 1.3])
+def test_qdq_mxfp4_ragged_bit_exact(mxq, shape, sf):
+    a = mxq_inputs.mxfp4_small(shape, seed=sum(shape))
+    got = mxq.qdq_mxfp4(torch.from_numpy(a).to(DEV), np.float32(sf)).cpu().numpy()
+    ref = oracle.mxfp4_qdq(a, np.float32(sf))
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_qdq_mxfp4_large_bit_exact(mxq):
+    a = mxq_inputs.mxfp4_large(4096, 4096, seed=0)   # t(3) tails, x100 outliers, zero blocks
+    got = mxq.qdq_mxfp4(torch.from_numpy(a).to(DEV)).cpu().numpy()
+    ref = oracle.mxfp4_qdq(a)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_qdq_mxfp4_in_place(mxq):
+    a = mxq_inputs.mxfp4_small((64, 96), seed=9)
+    t = torch.from_numpy(a).to(DEV)
+    mxq.mxq_qdq_mxfp4(t, t, 64, 96, 32, 6.0)
+    assert np.array_equal(t.cpu().numpy().view(np.uint32), oracle.mxfp4_qdq(a).view(np.uint32))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("R,C", [(48, 160), (128, 128), (300, 4096)])
+def test_packed_mxfp4_bit_exact(mxq, dtype, R, C):
+    a = mxq_inputs.mxfp4_large(R, C, seed=R)
+    t = torch.from_numpy(a).to(dtype)
+    q, s = mxq.quantize_mxfp4(t.to(DEV))
+    oq, os_ = oracle.mxfp4_quant(t.to(torch.float32).numpy())
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
+
+
+# ------------------------------------------------------------------ full sizes
+
+def test_full_size_linear_operands_dual_quant(mxq):
+    """X[8192x4096], W[14336x4096], dY[8192x14336]: dual quant bit-exact in full."""
+    x, w, dy = mxq_inputs.linear_inputs(8192, 14336, 4096, seed=0)
+    for t in (x, w, dy):
+        q, s, qT, sT = mxq.quantize_mxfp8(t.to(DEV), dual=True)
+        oq, os_ = oracle.mxfp8_quant_rows(t)
+        assert np.array_equal(q.cpu().numpy(), oq)
+        assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
+        oqT, osT = oracle.mxfp8_quant_cols(t)
+        assert np.array_equal(qT.cpu().numpy(), oqT)
+        assert np.array_equal(sT.cpu().numpy(), oracle.swizzle_scales(osT))
+        del q, s, qT, sT

@@ -217,7 +217,7 @@ def test_ragged_shapes_are_per_row():
         assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
         # flattening first would let neighbouring rows share blocks: with rows of
         # very different magnitude the shared block's scale, hence the result, differs
-        z = (rows * (100.0 ** np.arange(rows.shape[0]))[:, None]).astype(np.float32).reshape(shp)
+        z = (rows * (100.0 ** (np.arange(rows.shape[0]) % 4))[:, None]).astype(np.float32).reshape(shp)
         per_row = oracle.mxfp4_qdq(z)
         flat = oracle.mxfp4_qdq(z.reshape(1, -1)).reshape(shp)
         assert not np.array_equal(flat, per_row)
