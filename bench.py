@@ -57,8 +57,8 @@ def dist_init():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if torch.cuda.is_available():
+        backend = os.environ.get("MXQ_BENCH_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
+        if backend == "nccl":
             torch.cuda.set_device(local)
         dist.init_process_group(backend)
     return world, rank, local
