@@ -64,8 +64,12 @@ def _oracle_w(w):
             np.stack([c[0] for c in cols]), np.stack([c[1] for c in cols]))
 
 
+# The Frobenius bound is a statistic over the output: bf16 output rounding alone
+# contributes ~1.1e-3 on average, and over a handful of elements it can exceed
+# 2e-3, so every case keeps >= 1024 elements per checked output (the one-row
+# group below has 1 x 1024 outputs).
 @pytest.mark.parametrize("sizes,K,N", [([3, 0, 200, 0, 97], 256, 256), ([128, 128], 160, 384),
-                                       ([0, 0, 1], 64, 128), ([700], 512, 128)])
+                                       ([0, 0, 1], 1024, 1024), ([700], 512, 128)])
 def test_grouped_fwd_dx_dw(mxq, sizes, K, N):
     off, x, w, dy = mxq_inputs.moe_inputs(len(sizes), sum(sizes), K, N, seed=len(sizes) + K, sizes=sizes)
     moe = MoE(mxq, off, x, w, dy)
