@@ -12,6 +12,7 @@
 //   kGroupedK    tiles (expert, m, n) whose contraction runs over the expert's
 //                padded token range only (weight gradient of the MoE layer).
 //
+// Persistent: one CTA per SM walks tiles blockIdx.x, +gridDim.x, ...
 // CTA = 6 warps, tile 128 x 256, K step 128 bytes, 4-stage mbarrier pipeline:
 //   warp 0     TMA producer: A/B code tiles (128B-swizzled) by
 //              cp.async.bulk.tensor, 512-byte scale tiles by cp.async.bulk;
@@ -20,7 +21,9 @@
 //              tcgen05.mma.kind::mxf8f6f4.block_scale (M128 N256 K32) per stage,
 //              then tcgen05.commit frees the stage;
 //   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane
-//              sub-partition each), RNE to bf16, 16-byte global stores.
+//              sub-partition each) into registers as bf16 (RNE), then release
+//              the accumulator to the MMA warp before the 16-byte global
+//              stores, which overlap the next tile's mainloop.
 // TMEM: columns [0, 256) accumulator; [256 + 16 s, +12) scale slots of stage s
 // (A: 4 columns, B: 2 x 4 columns).  Every wait is bounded (mxq_device.cuh).
 #include <cuda.h>
@@ -46,7 +49,7 @@ constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
 constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
 constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-constexpr uint32_t NUM_BARS = 2 * STAGES + 1;
+constexpr uint32_t NUM_BARS = 2 * STAGES + 3;
 constexpr uint32_t OFF_MISC = OFF_BAR + 128;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 256;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base to 1024
@@ -65,6 +68,7 @@ struct Params {
     int E;
     int64_t b_row_per_expert, b_k_per_expert, c_expert_stride;
     int m_tiles, n_tiles;
+    int64_t total_tiles;  // tile index space (an upper bound for grouped rows)
 };
 
 struct TileInfo {
@@ -73,7 +77,6 @@ struct TileInfo {
     int64_t a_ratom, b_ratom, a_katom0, b_katom0;
     int64_t row_lo, row_hi, out_row0, col0, col_hi, c_off;
 };
-static_assert(sizeof(TileInfo) + 16 <= 256, "misc area");
 
 // Instruction descriptor, kind::mxf8f6f4: E4M3 x E4M3, both K-major, N = 256,
 // M = 128, E8M0 scales, scale-factor byte `j` of the A and B scale columns.
@@ -83,9 +86,8 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t j) {
 }
 
 // Work decomposition: which tile this CTA computes (run by all lanes of warp 0).
-__device__ TileInfo resolve_tile(const Params &p, int lane) {
+__device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane) {
     TileInfo t{};
-    const int64_t bid = blockIdx.x;
     t.k_last = 4;
     if (p.mode == kDense) {
         const int64_t mt = bid % p.m_tiles, nt = bid / p.m_tiles;
@@ -184,25 +186,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    TileInfo *tip = reinterpret_cast<TileInfo *>(smem + OFF_MISC);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + sizeof(TileInfo));
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + sizeof(TileInfo) + 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t bar_full = sbase + OFF_BAR, bar_empty = bar_full + 8 * STAGES, bar_acc = bar_full + 16 * STAGES;
+    const uint32_t bar_full = sbase + OFF_BAR, bar_empty = bar_full + 8 * STAGES;
+    const uint32_t bar_accf = bar_full + 16 * STAGES, bar_acce = bar_accf + 8, bar_drain = bar_accf + 16;
 
-    if (warp == 0) {
-        TileInfo t = resolve_tile(p, lane);
-        if (lane == 0) {
-            // once any CTA has given up, the rest of the grid skips its tile
-            if (*reinterpret_cast<volatile unsigned int *>(&g_device_error) != 0) t.valid = 0;
-            *tip = t;
-            *abort_flag = 0;
-        }
-    }
+    // once any CTA has given up, the rest of the grid does no work
+    if (threadIdx.x == 0) *abort_flag = *reinterpret_cast<volatile unsigned int *>(&g_device_error) != 0 ? 1 : 0;
     __syncthreads();
-    const TileInfo ti = *tip;
-    if (!ti.valid) return;  // before any TMEM allocation
+    if (*abort_flag) return;  // before any TMEM allocation
 
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
@@ -214,7 +208,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_init(bar_full + 8 * s, 1);
                 mbar_init(bar_empty + 8 * s, 1);
             }
-            mbar_init(bar_acc, 1);
+            mbar_init(bar_accf, 1);
+            mbar_init(bar_acce, 4);  // one arrival per epilogue warp
+            mbar_init(bar_drain, 1);
             fence_mbar_init();
         }
         __syncwarp();
@@ -226,86 +222,129 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Persistent loop: every warp walks the same tile sequence and decodes each
+    // tile itself; the stage ring and the accumulator phases run across tiles.
     if (warp == 0) {
-        if (lane == 0 && ti.nkb > 0) {
-            // ------------------------------------------------ TMA producer
-            int issued = 0;
-            for (int kb = 0; kb < ti.nkb; kb++) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (kb / STAGES) & 1;
-                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_device_error)) break;
-                const uint32_t fb = bar_full + 8 * s;
-                mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + SFA_BYTES + 512u * ti.b_atoms);
-                tma_load_2d(sbase + OFF_A + s * A_BYTES, &tmA, fb, static_cast<int>(ti.a_k0 + kb * BK),
-                            static_cast<int>(ti.a_row0));
-                tma_load_2d(sbase + OFF_B + s * B_BYTES, &tmB, fb, static_cast<int>(ti.b_k0 + kb * BK),
-                            static_cast<int>(ti.b_row0));
-                bulk_load(sbase + OFF_SFA + s * SFA_BYTES, p.sa + (ti.a_ratom * p.sa_kt + ti.a_katom0 + kb) * 512,
-                          512, fb);
-                for (int h = 0; h < ti.b_atoms; h++)
-                    bulk_load(sbase + OFF_SFB + s * SFB_BYTES + 512 * h,
-                              p.sb + ((ti.b_ratom + h) * p.sb_kt + ti.b_katom0 + kb) * 512, 512, fb);
-                issued++;
+        // ---------------------------------------------------- TMA producer
+        uint32_t g = 0;  // k-blocks issued by this CTA (lane 0)
+        for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+            const TileInfo ti = resolve_tile(p, tile, lane);
+            if (!ti.valid) break;  // grouped-row tiles past the real count come last
+            int stop = 0;
+            if (lane == 0) {
+                for (int kb = 0; kb < ti.nkb; kb++, g++) {
+                    const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
+                    if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_device_error)) { stop = 1; break; }
+                    const uint32_t fb = bar_full + 8 * s;
+                    mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + SFA_BYTES + 512u * ti.b_atoms);
+                    tma_load_2d(sbase + OFF_A + s * A_BYTES, &tmA, fb, static_cast<int>(ti.a_k0 + kb * BK),
+                                static_cast<int>(ti.a_row0));
+                    tma_load_2d(sbase + OFF_B + s * B_BYTES, &tmB, fb, static_cast<int>(ti.b_k0 + kb * BK),
+                                static_cast<int>(ti.b_row0));
+                    bulk_load(sbase + OFF_SFA + s * SFA_BYTES,
+                              p.sa + (ti.a_ratom * p.sa_kt + ti.a_katom0 + kb) * 512, 512, fb);
+                    for (int h = 0; h < ti.b_atoms; h++)
+                        bulk_load(sbase + OFF_SFB + s * SFB_BYTES + 512 * h,
+                                  p.sb + ((ti.b_ratom + h) * p.sb_kt + ti.b_katom0 + kb) * 512, 512, fb);
+                }
             }
-            if (*abort_flag) {  // let this CTA's copies land before it exits
-                for (int j = max(0, issued - STAGES); j < issued; j++)
-                    mbar_wait_drain(bar_full + 8 * (j % STAGES), (j / STAGES) & 1);
-            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+        }
+        if (lane == 0 && *abort_flag) {  // let this CTA's copies land before it exits
+            for (uint32_t j = g > STAGES ? g - STAGES : 0; j < g; j++)
+                mbar_wait_drain(bar_full + 8 * (j % STAGES), (j / STAGES) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0 && ti.nkb > 0) {
-            // ------------------------------------------------ MMA issuer
-            for (int kb = 0; kb < ti.nkb; kb++) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (kb / STAGES) & 1;
-                if (!mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_device_error)) break;
+        // ---------------------------------------------------- MMA issuer
+        uint32_t g = 0, acc_it = 0;
+        bool issued_any = false;
+        for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+            const TileInfo ti = resolve_tile(p, tile, lane);
+            if (!ti.valid) break;
+            if (ti.nkb == 0) continue;  // empty group: the epilogue writes zeros
+            int stop = 0;
+            if (lane == 0) {
+                // the epilogue must have drained the previous accumulator
+                if (acc_it > 0 && !mbar_wait(bar_acce, (acc_it - 1) & 1, abort_flag, &g_device_error)) stop = 1;
                 tc_fence_after();
-                const uint32_t sfa_t = tmem + SF_COL0 + s * SF_STRIDE, sfb_t = sfa_t + 4;
-                tc_cp_32x128b_warpx4(sfa_t, smem_desc(sbase + OFF_SFA + s * SFA_BYTES, 0, 128, 0));
-                tc_cp_32x128b_warpx4(sfb_t, smem_desc(sbase + OFF_SFB + s * SFB_BYTES, 0, 128, 0));
-                tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sbase + OFF_SFB + s * SFB_BYTES + 512, 0, 128, 0));
-                const int kk = (kb == ti.nkb - 1) ? ti.k_last : 4;
-                for (int j = 0; j < kk; j++) {
-                    const uint64_t ad = smem_desc(sbase + OFF_A + s * A_BYTES + 32 * j, 0, 1024, 2);
-                    const uint64_t bd = smem_desc(sbase + OFF_B + s * B_BYTES + 32 * j, 0, 1024, 2);
-                    tc_mma_mxf8(tmem, ad, bd, make_idesc(static_cast<uint32_t>(j)), sfa_t, sfb_t,
-                                (kb | j) != 0 ? 1u : 0u);
+                for (int kb = 0; kb < ti.nkb && !stop; kb++, g++) {
+                    const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
+                    if (!mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_device_error)) { stop = 1; break; }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + SF_COL0 + s * SF_STRIDE, sfb_t = sfa_t + 4;
+                    tc_cp_32x128b_warpx4(sfa_t, smem_desc(sbase + OFF_SFA + s * SFA_BYTES, 0, 128, 0));
+                    tc_cp_32x128b_warpx4(sfb_t, smem_desc(sbase + OFF_SFB + s * SFB_BYTES, 0, 128, 0));
+                    tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sbase + OFF_SFB + s * SFB_BYTES + 512, 0, 128, 0));
+                    const int kk = (kb == ti.nkb - 1) ? ti.k_last : 4;
+                    for (int j = 0; j < kk; j++) {
+                        const uint64_t ad = smem_desc(sbase + OFF_A + s * A_BYTES + 32 * j, 0, 1024, 2);
+                        const uint64_t bd = smem_desc(sbase + OFF_B + s * B_BYTES + 32 * j, 0, 1024, 2);
+                        tc_mma_mxf8(tmem, ad, bd, make_idesc(static_cast<uint32_t>(j)), sfa_t, sfb_t,
+                                    (kb | j) != 0 ? 1u : 0u);
+                    }
+                    issued_any = true;
+                    tc_commit(bar_empty + 8 * s);
                 }
-                tc_commit(bar_empty + 8 * s);
+                if (!stop) tc_commit(bar_accf);
             }
-            tc_commit(bar_acc);
-            if (*abort_flag) mbar_wait_drain(bar_acc, 0);  // no MMA in flight at dealloc
+            acc_it++;
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+        }
+        if (lane == 0 && issued_any && *abort_flag) {  // no MMA in flight at dealloc
+            tc_commit(bar_drain);
+            mbar_wait_drain(bar_drain, 0);
         }
     } else {
         // ---------------------------------------------------- epilogue
+        // Drain the accumulator into registers (bf16), release it to the MMA
+        // warp, then store: the global stores overlap the next tile's mainloop.
         const int sub = warp & 3;
-        const int64_t grow = ti.out_row0 + 32 * sub + lane;
-        const bool row_ok = grow >= ti.row_lo && grow < ti.row_hi;
-        __nv_bfloat16 *crow = p.c + ti.c_off + grow * p.ldc;
-        if (ti.nkb == 0) {
-            if (row_ok)
-                for (int64_t col = ti.col0; col < ti.col_hi; col++) crow[col] = __float2bfloat16_rn(0.0f);
-        } else if (mbar_wait(bar_acc, 0, abort_flag, &g_device_error)) {
+        uint32_t acc_it = 0;
+        for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+            const TileInfo ti = resolve_tile(p, tile, lane);
+            if (!ti.valid) break;
+            const int64_t grow = ti.out_row0 + 32 * sub + lane;
+            const bool row_ok = grow >= ti.row_lo && grow < ti.row_hi;
+            __nv_bfloat16 *crow = p.c + ti.c_off + grow * p.ldc;
+            if (ti.nkb == 0) {
+                if (row_ok)
+                    for (int64_t col = ti.col0; col < ti.col_hi; col++) crow[col] = __float2bfloat16_rn(0.0f);
+                continue;
+            }
+            if (!mbar_wait(bar_accf, acc_it & 1, abort_flag, &g_device_error)) break;
             tc_fence_after();
+            uint32_t pk[BN / 2];
+#pragma unroll
+            for (int ch = 0; ch < BN / 32; ch++) {
+                if (ti.col0 + 32 * ch < ti.col_hi) {  // warp-uniform
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * sub) << 16) + 32 * ch, r);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; i++)
+                        pk[16 * ch + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acce);
+            acc_it++;
+            if (!row_ok) continue;
+#pragma unroll
             for (int ch = 0; ch < BN / 32; ch++) {
                 const int64_t col = ti.col0 + 32 * ch;
-                if (col >= ti.col_hi) break;  // warp-uniform
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * sub) << 16) + 32 * ch, r);
-                tc_wait_ld();
-                if (!row_ok) continue;
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; i++) pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
                 if (col + 32 <= ti.col_hi) {
                     uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
 #pragma unroll
-                    for (int i = 0; i < 4; i++) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                } else {
-                    for (int i = 0; i < 32 && col + i < ti.col_hi; i++) {
-                        const uint16_t h = static_cast<uint16_t>(pk[i >> 1] >> (16 * (i & 1)));
-                        reinterpret_cast<uint16_t *>(crow)[col + i] = h;
-                    }
+                    for (int i = 0; i < 4; i++)
+                        dst[i] = make_uint4(pk[16 * ch + 4 * i], pk[16 * ch + 4 * i + 1], pk[16 * ch + 4 * i + 2],
+                                            pk[16 * ch + 4 * i + 3]);
+                } else if (col < ti.col_hi) {
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        if (col + i < ti.col_hi)
+                            reinterpret_cast<uint16_t *>(crow)[col + i] =
+                                static_cast<uint16_t>(pk[16 * ch + (i >> 1)] >> (16 * (i & 1)));
                 }
             }
         }
@@ -386,11 +425,21 @@ cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
     p.c_expert_stride = g.c_expert_stride;
     p.m_tiles = static_cast<int>((g.M + BM - 1) / BM);
     p.n_tiles = static_cast<int>((g.N + BN - 1) / BN);
-    int64_t grid = 0;
-    if (g.mode == kDense) grid = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    else if (g.mode == kGroupedRows) grid = ((g.T + BM - 1) / BM + g.E) * p.n_tiles;
-    else grid = static_cast<int64_t>(g.E) * p.m_tiles * p.n_tiles;
-    if (grid <= 0) return cudaSuccess;
+    if (g.mode == kDense) p.total_tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    else if (g.mode == kGroupedRows) p.total_tiles = ((g.T + BM - 1) / BM + g.E) * p.n_tiles;
+    else p.total_tiles = static_cast<int64_t>(g.E) * p.m_tiles * p.n_tiles;
+    if (p.total_tiles <= 0) return cudaSuccess;
+    // persistent grid: one CTA per SM (the CTA needs ~200 KB of shared memory)
+    static int num_sms[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (num_sms[dev] == 0) {
+        e = cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t grid = p.total_tiles < num_sms[dev] ? p.total_tiles : num_sms[dev];
     k_gemm_mxf8<<<static_cast<unsigned>(grid), THREADS, SMEM_ALLOC, st>>>(tmA, tmB, p);
     return cudaGetLastError();
 }
