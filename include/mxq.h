@@ -206,6 +206,43 @@ mxq_status mxq_linear_bwd_dw(const void *dy, const void *x, int64_t M, int64_t N
                              mxq_stream_t stream);
 
 /* ------------------------------------------------------------------ */
+/* Linear forward without caller-provided scratch                       */
+/* ------------------------------------------------------------------ */
+
+/* Device memory the library holds for mxq_linear_fwd_noalloc: 64 MiB on every
+ * GPU that loads the library, kept until the process exits. */
+#define MXQ_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* Y = X W^T of the MXFP8 linear layer -- the same y as mxq_linear_fwd -- for
+ * callers that cannot allocate device memory.  The pages have no counterpart
+ * of this entry point.
+ *
+ * Who needs it: mxq_linear_fwd wants a caller-provided workspace for the
+ * quantized operands.  A plug-in running inside a host framework that owns
+ * the device memory pool and does not let plug-ins call cudaMalloc, or a
+ * service that reserves its memory once at start-up and must not allocate
+ * afterwards, has no workspace to give; this entry point uses scratch that
+ * lives inside the library instead.
+ *
+ * x bf16 [M x K], w bf16 [N x K], y bf16 [M x N]: device pointers the caller
+ * owns, 16-byte aligned.  M, N, K positive multiples of 32, and the row quants
+ * of X and W (M*K + N*K code bytes plus their scale tiles, each rounded up to
+ * 256 bytes) must fit in MXQ_NOALLOC_SCRATCH_BYTES -- otherwise
+ * MXQ_ERR_INVALID_ARG, with the sizes in mxq_last_error_string().  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ * The first call on a device looks up the scratch's device address
+ * (cudaGetSymbolAddress) with that device current: make that first call
+ * before any stream capture.  All calls share the one scratch array, which
+ * keeps the last call's contents; each call rewrites everything it reads, so
+ * nothing needs clearing.  Calls whose GPU work can overlap (on different
+ * streams, or from different host threads) race on the array and corrupt
+ * each other's results: issue them on one stream or otherwise serialize
+ * them. */
+mxq_status mxq_linear_fwd_noalloc(const void *x, const void *w, int64_t M, int64_t N, int64_t K, void *y,
+                                  mxq_stream_t stream);
+
+/* ------------------------------------------------------------------ */
 /* Diagnostics                                                          */
 /* ------------------------------------------------------------------ */
 

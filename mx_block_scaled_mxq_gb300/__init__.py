@@ -26,13 +26,14 @@ __all__ = [
     "mxq_scale_bytes", "mxq_grouped_padded_rows", "mxq_quantize", "mxq_quantize_grouped_col", "mxq_qdq_mxfp4",
     "mxq_gemm", "mxq_grouped_gemm", "mxq_linear_ctx_bytes", "mxq_linear_saved_bytes",
     "mxq_linear_workspace_bytes", "mxq_linear_fwd", "mxq_linear_bwd_dx", "mxq_linear_bwd_dw",
-    "mxq_last_error_string", "mxq_poll_device_error",
+    "mxq_last_error_string", "mxq_poll_device_error", "mxq_linear_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 BF16, F32 = 0, 1
 E4M3, E2M1 = 0, 1
 SAVE_QUANT, RECOMPUTE = 0, 1
 GG_FWD, GG_DX, GG_DW = 0, 1, 2
+NOALLOC_SCRATCH_BYTES = 64 << 20  # MXQ_NOALLOC_SCRATCH_BYTES in include/mxq.h
 _STATUS = {0: "MXQ_OK", 1: "MXQ_ERR_INVALID_ARG", 2: "MXQ_ERR_UNSUPPORTED", 3: "MXQ_ERR_ARCH",
            4: "MXQ_ERR_CUDA", 5: "MXQ_ERR_TIMEOUT"}
 
@@ -60,6 +61,7 @@ _SIGNATURES = {
     "mxq_linear_fwd": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
     "mxq_linear_bwd_dx": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
     "mxq_linear_bwd_dw": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
+    "mxq_linear_fwd_noalloc": (_I32, [_P, _P, _I64, _I64, _I64, _P, _P]),
     "mxq_last_error_string": (ctypes.c_char_p, []),
     "mxq_poll_device_error": (_I32, [ctypes.POINTER(ctypes.c_uint32)]),
 }
@@ -166,6 +168,12 @@ def mxq_linear_bwd_dx(dy, w, M, N, K, mode, ctx, dx, workspace, ws_bytes, stream
 def mxq_linear_bwd_dw(dy, x, M, N, K, mode, ctx, dw, workspace, ws_bytes, stream=None):
     _check(load().mxq_linear_bwd_dw(_p(dy), _p(x), M, N, K, mode, _p(ctx), _p(dw), _p(workspace), ws_bytes,
                                     _s(stream)), "mxq_linear_bwd_dw")
+
+
+def mxq_linear_fwd_noalloc(x, w, M, N, K, y, stream=None):
+    """Linear forward that allocates nothing: its scratch is a fixed array inside
+    the library (for callers that may not allocate device memory)."""
+    _check(load().mxq_linear_fwd_noalloc(_p(x), _p(w), M, N, K, _p(y), _s(stream)), "mxq_linear_fwd_noalloc")
 
 
 def mxq_last_error_string() -> str:

@@ -124,6 +124,14 @@ mxq_status check_linear(const void *a, const void *b, int64_t M, int64_t N, int6
 
 }  // namespace
 
+// Error reporting and the arch check for entry points defined in other
+// translation units (same behaviour as the helpers above).
+namespace mxq {
+mxq_status api_fail(mxq_status s, const char *msg) { return fail(s, "%s", msg); }
+mxq_status api_check_arch() { return check_arch(); }
+mxq_status api_cuda_result(cudaError_t e, const char *what) { return cuda_result(e, what); }
+}  // namespace mxq
+
 extern "C" {
 
 const char *mxq_last_error_string(void) { return g_last_error.c_str(); }

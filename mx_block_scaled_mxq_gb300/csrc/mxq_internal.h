@@ -3,6 +3,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "mxq.h"
+
 namespace mxq {
 
 // ---- quantization (mxq_quant.cu) ----
@@ -42,5 +44,10 @@ struct GemmProblem {
 cudaError_t launch_gemm(const GemmProblem &p, cudaStream_t st);
 // Reads the device error word set by bounded waits that gave up, then clears it.
 cudaError_t read_and_clear_device_error(unsigned int *word);
+
+// ---- error reporting shared by the C entry points (mxq_api.cu) ----
+mxq_status api_fail(mxq_status s, const char *msg);           // records msg, returns s
+mxq_status api_check_arch();                                   // MXQ_ERR_ARCH unless sm_103
+mxq_status api_cuda_result(cudaError_t e, const char *what);   // MXQ_OK or MXQ_ERR_CUDA
 
 }  // namespace mxq
