@@ -46,6 +46,12 @@ METRIC = "MXFP8 linear fwd+bwd + MoE grouped-GEMM fwd/dX/dW TFLOP/s (step incl. 
 WORKLOAD = ("linear M8192 N14336 K4096 fwd+bwd (saved-quant) + MoE E32 T32768 K7168 N4096 fwd+dX+dW "
             "+ MXFP4 QDQ/pack 4096x4096")
 PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f in ("mxq_gemm.cu", "mxq_device.cuh")]
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the GEMM
+# kernel for each launch the timed region brackets, from one ncu capture of the
+# full-size launches (profiles/k_gemm_mxf8__bench_launches_dram.md), keyed by a
+# hash of the kernel source; when the source has changed since, traffic is null.
+GEMM_DRAM_TRAFFIC = {}
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
 
@@ -268,6 +274,24 @@ def time_steps(fn, steps, world):
     return s.elapsed_time(e) / 1e3
 
 
+def gemm_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def gemm_traffic(per_kind):
+    """Average measured DRAM bytes per bracketed GEMM launch, or None."""
+    rec = GEMM_DRAM_TRAFFIC.get(gemm_source_hash())
+    if not rec or any(k not in rec for k in per_kind):
+        return None
+    n = sum(v[1] for v in per_kind.values())
+    return sum(rec[k] * v[1] for k, v in per_kind.items()) / n
+
+
 def read_peaks():
     try:
         with open(PEAKS) as f:
@@ -423,7 +447,8 @@ def main():
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / fp8_peak, 4) if achieved else None,
                      "peak_source": f"{peak_kind}: 2 x bf16_tflops_sustained (nominal fp8/bf16 ratio)",
-                     "launches_timed": len(ev), "traffic": None},
+                     "launches_timed": len(ev), "traffic": gemm_traffic(per_kind),
+                     "traffic_unit": "bytes per launch", "kernel_source": gemm_source_hash()},
         "e2e": {"value": round(world * STEP_FLOP * args.e2e_steps / e2e_t / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": hb_in, "d2h_bytes_per_step": hb_out,
                 "ms_per_step": round(e2e_t / args.e2e_steps * 1e3, 3)},

@@ -68,6 +68,7 @@ struct Params {
     int E;
     int64_t b_row_per_expert, b_k_per_expert, c_expert_stride;
     int m_tiles, n_tiles;
+    int n_fastest;        // kDense tile order: 1 = n fastest (A is the larger operand)
     int64_t total_tiles;  // tile index space (an upper bound for grouped rows)
 };
 
@@ -90,7 +91,10 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane) {
     TileInfo t{};
     t.k_last = 4;
     if (p.mode == kDense) {
-        const int64_t mt = bid % p.m_tiles, nt = bid / p.m_tiles;
+        // raster so that the smaller operand stays in L2 while the larger one
+        // streams through once: concurrent CTAs share the larger operand's tile
+        const int64_t mt = p.n_fastest ? bid / p.n_tiles : bid % p.m_tiles;
+        const int64_t nt = p.n_fastest ? bid % p.n_tiles : bid / p.m_tiles;
         t.valid = 1;
         t.a_row0 = mt * BM; t.b_row0 = nt * BN;
         t.a_ratom = mt; t.b_ratom = 2 * nt;
@@ -425,6 +429,7 @@ cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
     p.c_expert_stride = g.c_expert_stride;
     p.m_tiles = static_cast<int>((g.M + BM - 1) / BM);
     p.n_tiles = static_cast<int>((g.N + BN - 1) / BN);
+    p.n_fastest = g.mode == kDense && g.a_rows > g.b_rows ? 1 : 0;
     if (g.mode == kDense) p.total_tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     else if (g.mode == kGroupedRows) p.total_tiles = ((g.T + BM - 1) / BM + g.E) * p.n_tiles;
     else p.total_tiles = static_cast<int64_t>(g.E) * p.m_tiles * p.n_tiles;

@@ -151,21 +151,30 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
     __shared__ __align__(16) uint8_t satom[512];
     const int tid = threadIdx.x, lane = tid & 31;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile, c0 = static_cast<int64_t>(blockIdx.x) * kTile;
-#pragma unroll 2
+    // all of this thread's loads first (8 or 16 x 16 B in flight), then compute
+    constexpr int kVec = sizeof(InT) == 4 ? 2 : 1;
+    uint4 v[8][kVec];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int id = tid + kThreads * i;
+        const int64_t gr = r0 + (id >> 4), gc = c0 + (id & 15) * 8;
+#pragma unroll
+        for (int h = 0; h < kVec; h++) v[i][h] = make_uint4(0, 0, 0, 0);
+        if (gr < R && gc < C) {
+            const InT *src = x + gr * ldx + gc;
+#pragma unroll
+            for (int h = 0; h < kVec; h++) v[i][h] = ldg_nc_v4(reinterpret_cast<const uint32_t *>(src) + 4 * h);
+        }
+    }
+#pragma unroll
     for (int i = 0; i < 8; i++) {
         const int id = tid + kThreads * i;
         const int row = id >> 4, ch = id & 15, col = ch * 8;
         const int64_t gr = r0 + row, gc = c0 + col;
         const bool valid = gr < R && gc < C;
-        uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // bf16: 4 words used; fp32: 8 words
-        if (valid) {
-            const InT *src = x + gr * ldx + gc;
-            const uint4 a = ldg_nc_v4(src);
-            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-            if (sizeof(InT) == 4) {
-                const uint4 b = ldg_nc_v4(reinterpret_cast<const float *>(src) + 4);
-                w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-            }
+        uint32_t w[8] = {v[i][0].x, v[i][0].y, v[i][0].z, v[i][0].w, 0, 0, 0, 0};  // bf16: 4 words; fp32: 8
+        if (kVec == 2) {
+            w[4] = v[i][kVec - 1].x; w[5] = v[i][kVec - 1].y; w[6] = v[i][kVec - 1].z; w[7] = v[i][kVec - 1].w;
         }
         uint8_t sbyte;
         if (FMT == 0) {
@@ -290,17 +299,23 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
     }
 
     // ---- load the tile (and the row quant) ----
-#pragma unroll 2
+    // all 8 of this thread's 16-byte loads first, then compute
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int id = tid + kThreads * i;
+        const int row = id >> 4;
+        const int64_t gc = c0 + (id & 15) * 8;
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (row < nvalid && gc < P.C) v[i] = ldg_nc_v4(P.x + (src0 + row) * P.ldx + gc);
+    }
+#pragma unroll
     for (int i = 0; i < 8; i++) {
         const int id = tid + kThreads * i;
         const int row = id >> 4, ch = id & 15, col = ch * 8;
         const int64_t gc = c0 + col;
         const bool valid = row < nvalid && gc < P.C;
-        uint32_t w[4] = {0, 0, 0, 0};
-        if (valid) {
-            const uint4 a = ldg_nc_v4(P.x + (src0 + row) * P.ldx + gc);
-            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-        }
+        uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
         if (ROWS) {
             uint32_t a = amax8_bf16(w);
             a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
