@@ -52,8 +52,8 @@ GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f
 # full-size launches (profiles/k_gemm_mxf8__bench_launches_dram.md), keyed by a
 # hash of the kernel source; when the source has changed since, traffic is null.
 GEMM_DRAM_TRAFFIC = {
-    "f15a002b287eff2c": {"linear_dw_gemm": 253062400, "moe_fwd_gemm": 1523514368,
-                         "moe_dx_gemm": 1539495424, "moe_dw_gemm": 2240497408},
+    "09f75a733c8a93f1": {"linear_dw_gemm": 252425728, "moe_fwd_gemm": 1491229184,
+                         "moe_dx_gemm": 1528273152, "moe_dw_gemm": 2261080832},
 }
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 

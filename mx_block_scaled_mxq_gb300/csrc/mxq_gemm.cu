@@ -6,29 +6,39 @@
 // matmul run on MXFP8 operands, output in bf16).  One kernel serves the dense
 // GEMM and both grouped forms:
 //   kDense       tiles (m, n) of one problem;
-//   kGroupedRows tiles (expert, 128-row tile overlapping the expert's token
-//                rows, n); rows outside the expert are computed but not stored
+//   kGroupedRows tiles (expert, row tile overlapping the expert's token rows,
+//                n); rows outside the expert are computed but not stored
 //                (forward and input gradient of the MoE layer);
 //   kGroupedK    tiles (expert, m, n) whose contraction runs over the expert's
 //                padded token range only (weight gradient of the MoE layer).
 //
-// Persistent: one CTA per SM walks tiles blockIdx.x, +gridDim.x, ...
-// CTA = 6 warps, tile 128 x 256, K step 128 bytes, 4-stage mbarrier pipeline:
+// Persistent: each CTA (CG = 1) or CTA pair (CG = 2) walks its share of the
+// tiles; the stage ring and the accumulator phases run across tiles.
+// A CTA has 6 warps; the output tile is (128 * CG) x 256, K steps of 128 bytes:
 //   warp 0     TMA producer: A/B code tiles (128B-swizzled) by
-//              cp.async.bulk.tensor, 512-byte scale tiles by cp.async.bulk;
-//   warp 1     allocates 512 TMEM columns; one lane copies the scale tiles to
-//              TMEM (tcgen05.cp 32x128b.warpx4) and issues 4
-//              tcgen05.mma.kind::mxf8f6f4.block_scale (M128 N256 K32) per stage,
-//              then tcgen05.commit frees the stage;
+//              cp.async.bulk.tensor, 512-byte scale tiles (cp.async.bulk for
+//              CG = 1, 2-D TMA for CG = 2);
+//   warp 1     allocates 512 TMEM columns; one lane (of the even CTA for
+//              CG = 2) copies the scale tiles to TMEM (tcgen05.cp
+//              32x128b.warpx4) and issues 4 tcgen05.mma.kind::mxf8f6f4.block_scale
+//              (M = 128 * CG, N = 256, K = 32) per stage; tcgen05.commit frees
+//              the stage (in both CTAs of a pair);
 //   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane
-//              sub-partition each) into registers as bf16 (RNE), then release
-//              the accumulator to the MMA warp before the 16-byte global
-//              stores, which overlap the next tile's mainloop.
+//              sub-partition each) into registers as bf16 (RNE), release of the
+//              accumulator to the MMA warp, then 16-byte global stores that
+//              overlap the next tile's mainloop.
+// CG = 2 pairs two SMs on one 256 x 256 tile: each CTA loads 128 rows of A and
+// 128 of the 256 rows of B (32 KB per stage, 6 stages), so per SM the operand
+// traffic and the shared memory per stage are two thirds of CG = 1's, and the
+// deeper ring hides more load latency.  Each CTA holds its own rows' A scales
+// and all of B's scales; every load of both CTAs completes on the even CTA's
+// stage barrier.
 // TMEM: columns [0, 256) accumulator; [256 + 16 s, +12) scale slots of stage s
 // (A: 4 columns, B: 2 x 4 columns).  Every wait is bounded (mxq_device.cuh).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "mxq_device.cuh"
@@ -42,20 +52,28 @@ __device__ unsigned int g_device_error = 0;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4, THREADS = 192;
-constexpr uint32_t A_BYTES = BM * BK, B_BYTES = BN * BK, SFA_BYTES = 512, SFB_BYTES = 1024;
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
-constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-constexpr uint32_t NUM_BARS = 2 * STAGES + 3;
-constexpr uint32_t OFF_MISC = OFF_BAR + 128;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 256;
-constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base to 1024
+constexpr int BN = 256, BK = 128, THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512, SF_COL0 = 256, SF_STRIDE = 16;
-static_assert(NUM_BARS * 8 <= 128, "barrier area");
-static_assert(SF_COL0 + STAGES * SF_STRIDE <= TMEM_COLS, "tmem budget");
+
+template <int CG>
+struct Cfg {
+    static constexpr int BM = 128;           // rows of A per CTA (one TMEM lane each)
+    static constexpr int TILE_M = 128 * CG;  // rows of one output tile
+    static constexpr int B_ROWS = BN / CG;   // rows of B each CTA loads
+    static constexpr int STAGES = CG == 1 ? 4 : 6;
+    static constexpr uint32_t A_BYTES = BM * BK, B_BYTES = B_ROWS * BK, SFA_BYTES = 512, SFB_BYTES = 1024;
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 3;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + 128;
+    static constexpr uint32_t SMEM_ALLOC = OFF_MISC + 256 + 1024;  // + slack to align the base to 1024
+    static_assert(NUM_BARS * 8 <= 128, "barrier area");
+    static_assert(SF_COL0 + STAGES * SF_STRIDE <= TMEM_COLS, "tmem budget");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
 
 struct Params {
     GemmMode mode;
@@ -67,41 +85,47 @@ struct Params {
     const int64_t *offsets;
     int E;
     int64_t b_row_per_expert, b_k_per_expert, c_expert_stride;
-    int m_tiles, n_tiles;
-    int n_fastest;        // kDense tile order: 1 = n fastest (A is the larger operand)
-    int64_t total_tiles;  // tile index space (an upper bound for grouped rows)
+    int m_tiles, n_tiles;  // tile counts (m in units of 128 * CG rows)
+    int n_fastest;         // kDense tile order: 1 = n fastest (A is the larger operand)
+    int64_t total_tiles;   // tile index space (an upper bound for grouped rows)
 };
 
 struct TileInfo {
     int valid, nkb, k_last, b_atoms;
-    int64_t a_row0, b_row0, a_k0, b_k0;   // TMA coordinates of k-block 0
+    int64_t a_row0, b_row0, a_k0, b_k0;   // this CTA's TMA coordinates of k-block 0
     int64_t a_ratom, b_ratom, a_katom0, b_katom0;
     int64_t row_lo, row_hi, out_row0, col0, col_hi, c_off;
 };
 
 // Instruction descriptor, kind::mxf8f6f4: E4M3 x E4M3, both K-major, N = 256,
-// M = 128, E8M0 scales, scale-factor byte `j` of the A and B scale columns.
+// M = 128 * CG, E8M0 scales, scale-factor byte `j` of the A and B scale columns.
+template <int CG>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t j) {
     return (j << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-           (static_cast<uint32_t>(BM >> 4) << 24) | (j << 29);
+           (static_cast<uint32_t>(Cfg<CG>::TILE_M >> 4) << 24) | (j << 29);
 }
 
-// Work decomposition: which tile this CTA computes (run by all lanes of warp 0).
-__device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane) {
+// Work decomposition: which tile this CTA computes (run by all lanes of a warp).
+// `rank` is the CTA's position in its pair (0 for CG = 1).
+template <int CG>
+__device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_t rank) {
+    constexpr int TM = Cfg<CG>::TILE_M, BR = Cfg<CG>::B_ROWS;
     TileInfo t{};
     t.k_last = 4;
+    int64_t tile_row0 = 0, bn0 = 0;  // first row of the tile; first row of B for the tile
     if (p.mode == kDense) {
         // raster so that the smaller operand stays in L2 while the larger one
         // streams through once: concurrent CTAs share the larger operand's tile
         const int64_t mt = p.n_fastest ? bid / p.n_tiles : bid % p.m_tiles;
         const int64_t nt = p.n_fastest ? bid % p.n_tiles : bid / p.m_tiles;
         t.valid = 1;
-        t.a_row0 = mt * BM; t.b_row0 = nt * BN;
-        t.a_ratom = mt; t.b_ratom = 2 * nt;
-        t.row_lo = t.a_row0; t.row_hi = min(p.M, t.a_row0 + BM); t.out_row0 = t.a_row0;
-        t.col0 = nt * BN; t.col_hi = min(p.N, t.col0 + BN);
+        tile_row0 = mt * TM;
+        bn0 = nt * BN;
+        t.col0 = nt * BN;
+        t.row_lo = tile_row0 + 128 * rank;
+        t.row_hi = min(p.M, t.row_lo + 128);
     } else if (p.mode == kGroupedRows) {
-        // tiles of expert e: every 128-row tile overlapping [o_e, o_e+1), times n_tiles
+        // tiles of expert e: every TM-row tile overlapping [o_e, o_e+1), times n_tiles
         int64_t run = 0;
         int fe = -1;
         int64_t fstart = 0, fo0 = 0, fo1 = 0;
@@ -109,7 +133,7 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane) {
             const int e = base + lane;
             int64_t o0 = 0, o1 = 0;
             if (e < p.E) { o0 = p.offsets[e]; o1 = p.offsets[e + 1]; }
-            const int64_t cnt = (o1 > o0) ? ((o1 - 1) / BM - o0 / BM + 1) * p.n_tiles : 0;
+            const int64_t cnt = (o1 > o0) ? ((o1 - 1) / TM - o0 / TM + 1) * p.n_tiles : 0;
             int64_t incl = cnt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -130,15 +154,16 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane) {
             run += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (fe < 0) { t.valid = 0; return t; }
-        const int64_t mtiles_e = (fo1 - 1) / BM - fo0 / BM + 1;
+        const int64_t mtiles_e = (fo1 - 1) / TM - fo0 / TM + 1;
         const int64_t local = bid - fstart;
-        const int64_t nt = local / mtiles_e, mt = fo0 / BM + local % mtiles_e;
+        const int64_t nt = local / mtiles_e, mt = fo0 / TM + local % mtiles_e;
         t.valid = 1;
-        t.a_row0 = mt * BM; t.a_ratom = mt;
-        t.b_row0 = fe * p.b_row_per_expert + nt * BN; t.b_ratom = t.b_row0 / BM;
+        tile_row0 = mt * TM;
+        bn0 = fe * p.b_row_per_expert + nt * BN;
         t.b_k0 = fe * p.b_k_per_expert; t.b_katom0 = t.b_k0 / BK;
-        t.row_lo = max(fo0, t.a_row0); t.row_hi = min(fo1, t.a_row0 + BM); t.out_row0 = t.a_row0;
-        t.col0 = nt * BN; t.col_hi = min(p.N, t.col0 + BN);
+        t.col0 = nt * BN;
+        t.row_lo = max(fo0, tile_row0 + 128 * rank);
+        t.row_hi = min(fo1, tile_row0 + 128 * rank + 128);
     } else {  // kGroupedK
         const int64_t per = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
         const int e = static_cast<int>(bid / per);
@@ -152,13 +177,21 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane) {
         for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
         const int64_t ne = p.offsets[e + 1] - p.offsets[e];
         t.valid = 1;
-        t.a_row0 = mt * BM; t.b_row0 = nt * BN; t.a_ratom = mt; t.b_ratom = 2 * nt;
+        tile_row0 = mt * TM;
+        bn0 = nt * BN;
         t.a_k0 = t.b_k0 = pe; t.a_katom0 = t.b_katom0 = pe / BK;
         t.nkb = static_cast<int>((ne + 127) / 128);
-        t.row_lo = t.a_row0; t.row_hi = min(p.M, t.a_row0 + BM); t.out_row0 = t.a_row0;
-        t.col0 = nt * BN; t.col_hi = min(p.N, t.col0 + BN);
+        t.col0 = nt * BN;
+        t.row_lo = tile_row0 + 128 * rank;
+        t.row_hi = min(p.M, t.row_lo + 128);
         t.c_off = static_cast<int64_t>(e) * p.c_expert_stride;
     }
+    t.a_row0 = tile_row0 + 128 * rank;  // this CTA's 128 rows of A (and of the output)
+    t.a_ratom = t.a_row0 / 128;
+    t.out_row0 = t.a_row0;
+    t.b_row0 = bn0 + BR * rank;         // this CTA's share of B's rows
+    t.b_ratom = bn0 / 128;              // the tile's B scale tiles (all of them)
+    t.col_hi = min(p.N, t.col0 + BN);
     if (p.mode != kGroupedK) {
         t.nkb = static_cast<int>((p.K + BK - 1) / BK);
         t.k_last = static_cast<int>((p.K - static_cast<int64_t>(t.nkb - 1) * BK) / 32);
@@ -185,26 +218,90 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// Four K = 32 MMAs of one stage and the commit that frees the stage, with a
+// non-blocking test of the NEXT stage's barrier issued first and its result
+// read last, so the barrier check's latency overlaps the MMA issue instead of
+// adding to it.  Returns whether the next stage's data has landed.
+template <int CG>
+__device__ __forceinline__ bool mma4_commit_peek(uint32_t d_tmem, const uint64_t (&ad)[4], const uint64_t (&bd)[4],
+                                                 const uint32_t (&id)[4], uint32_t sfa, uint32_t sfb,
+                                                 uint32_t accumulate, uint32_t bar_empty_s, uint32_t bar_full_next,
+                                                 uint32_t parity_next) {
+    uint32_t ready;
+    if constexpr (CG == 2) {
+        asm volatile(
+            "{\n\t.reg .pred pn, pa, p1;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n\t"
+            "setp.ne.b32 pa, %3, 0;\n\t"
+            "setp.eq.u32 p1, 0, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], %5, %6, %7, [%8], [%9], pa;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], %10, %11, %12, [%8], [%9], p1;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], %13, %14, %15, [%8], [%9], p1;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], %16, %17, %18, [%8], [%9], p1;\n\t"
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%19], %20;\n\t"
+            "selp.u32 %0, 1, 0, pn;\n\t}"
+            : "=r"(ready)
+            : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "l"(ad[0]), "l"(bd[0]), "r"(id[0]),
+              "r"(sfa), "r"(sfb), "l"(ad[1]), "l"(bd[1]), "r"(id[1]), "l"(ad[2]), "l"(bd[2]), "r"(id[2]), "l"(ad[3]),
+              "l"(bd[3]), "r"(id[3]), "r"(bar_empty_s), "h"(static_cast<uint16_t>(3))
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred pn, pa, p1;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n\t"
+            "setp.ne.b32 pa, %3, 0;\n\t"
+            "setp.eq.u32 p1, 0, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], %5, %6, %7, [%8], [%9], pa;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], %10, %11, %12, [%8], [%9], p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], %13, %14, %15, [%8], [%9], p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], %16, %17, %18, [%8], [%9], p1;\n\t"
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%19];\n\t"
+            "selp.u32 %0, 1, 0, pn;\n\t}"
+            : "=r"(ready)
+            : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "l"(ad[0]), "l"(bd[0]), "r"(id[0]),
+              "r"(sfa), "r"(sfb), "l"(ad[1]), "l"(bd[1]), "r"(id[1]), "l"(ad[2]), "l"(bd[2]), "r"(id[2]), "l"(ad[3]),
+              "l"(bd[3]), "r"(id[3]), "r"(bar_empty_s)
+            : "memory");
+    }
+    return ready != 0;
+}
+
+template <int CG>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_gemm_mxf8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+    k_gemm_mxf8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const Params p) {
+    using C = Cfg<CG>;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t bar_full = sbase + OFF_BAR, bar_empty = bar_full + 8 * STAGES;
+    const uint32_t bar_full = sbase + C::OFF_BAR, bar_empty = bar_full + 8 * STAGES;
     const uint32_t bar_accf = bar_full + 16 * STAGES, bar_acce = bar_accf + 8, bar_drain = bar_accf + 16;
+    uint32_t rank = 0;
+    if constexpr (CG == 2) rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int64_t first = CG == 2 ? blockIdx.x >> 1 : blockIdx.x;
+    const int64_t step = CG == 2 ? gridDim.x >> 1 : gridDim.x;
 
     // once any CTA has given up, the rest of the grid does no work
     if (threadIdx.x == 0) *abort_flag = *reinterpret_cast<volatile unsigned int *>(&g_device_error) != 0 ? 1 : 0;
     __syncthreads();
-    if (*abort_flag) return;  // before any TMEM allocation
+    // (a CTA pair must pass its cluster barriers together, so only CG = 1 returns here)
+    if constexpr (CG == 1) {
+        if (*abort_flag) return;  // before any TMEM allocation
+    }
 
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if constexpr (CG == 2) {
+            prefetch_tmap(&tmSA);
+            prefetch_tmap(&tmSB);
+        }
     }
     if (warp == 1) {
         if (lane == 0) {
@@ -213,90 +310,157 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_init(bar_empty + 8 * s, 1);
             }
             mbar_init(bar_accf, 1);
-            mbar_init(bar_acce, 4);  // one arrival per epilogue warp
+            mbar_init(bar_acce, 4 * CG);  // one arrival per epilogue warp (of both CTAs)
             mbar_init(bar_drain, 1);
             fence_mbar_init();
         }
         __syncwarp();
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (CG == 2) {
+            tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // stage barriers and the accumulator-release barrier of the even CTA
+    uint32_t lead_full = bar_full, lead_acce = bar_acce;
+    if constexpr (CG == 2) {
+        lead_full = mapa_shared(bar_full, 0);
+        lead_acce = mapa_shared(bar_acce, 0);
+    }
+    const bool run = *abort_flag == 0;
 
-    // Persistent loop: every warp walks the same tile sequence and decodes each
-    // tile itself; the stage ring and the accumulator phases run across tiles.
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         uint32_t g = 0;  // k-blocks issued by this CTA (lane 0)
-        for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
-            const TileInfo ti = resolve_tile(p, tile, lane);
+        for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
+            const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank);
             if (!ti.valid) break;  // grouped-row tiles past the real count come last
             int stop = 0;
             if (lane == 0) {
                 for (int kb = 0; kb < ti.nkb; kb++, g++) {
                     const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
                     if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, &g_device_error)) { stop = 1; break; }
-                    const uint32_t fb = bar_full + 8 * s;
-                    mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + SFA_BYTES + 512u * ti.b_atoms);
-                    tma_load_2d(sbase + OFF_A + s * A_BYTES, &tmA, fb, static_cast<int>(ti.a_k0 + kb * BK),
-                                static_cast<int>(ti.a_row0));
-                    tma_load_2d(sbase + OFF_B + s * B_BYTES, &tmB, fb, static_cast<int>(ti.b_k0 + kb * BK),
-                                static_cast<int>(ti.b_row0));
-                    bulk_load(sbase + OFF_SFA + s * SFA_BYTES,
-                              p.sa + (ti.a_ratom * p.sa_kt + ti.a_katom0 + kb) * 512, 512, fb);
-                    for (int h = 0; h < ti.b_atoms; h++)
-                        bulk_load(sbase + OFF_SFB + s * SFB_BYTES + 512 * h,
-                                  p.sb + ((ti.b_ratom + h) * p.sb_kt + ti.b_katom0 + kb) * 512, 512, fb);
+                    const uint32_t sa_s = sbase + C::OFF_A + s * C::A_BYTES, sb_s = sbase + C::OFF_B + s * C::B_BYTES;
+                    const uint32_t sfa_s = sbase + C::OFF_SFA + s * C::SFA_BYTES;
+                    const uint32_t sfb_s = sbase + C::OFF_SFB + s * C::SFB_BYTES;
+                    const int ka = static_cast<int>(ti.a_k0 + kb * BK), kb_ = static_cast<int>(ti.b_k0 + kb * BK);
+                    if constexpr (CG == 1) {
+                        const uint32_t fb = bar_full + 8 * s;
+                        mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + C::SFA_BYTES + 512u * ti.b_atoms);
+                        tma_load_2d(sa_s, &tmA, fb, ka, static_cast<int>(ti.a_row0));
+                        tma_load_2d(sb_s, &tmB, fb, kb_, static_cast<int>(ti.b_row0));
+                        bulk_load(sfa_s, p.sa + (ti.a_ratom * p.sa_kt + ti.a_katom0 + kb) * 512, 512, fb);
+                        for (int h = 0; h < ti.b_atoms; h++)
+                            bulk_load(sfb_s + 512 * h, p.sb + ((ti.b_ratom + h) * p.sb_kt + ti.b_katom0 + kb) * 512,
+                                      512, fb);
+                    } else {
+                        // both CTAs' loads complete on the even CTA's barrier, which
+                        // expects the bytes of both (scale tiles past the buffer are
+                        // zero-filled by TMA and still counted)
+                        const uint32_t fb = lead_full + 8 * s;
+                        if (leader)
+                            mbar_arrive_expect_tx(bar_full + 8 * s,
+                                                  2 * (C::A_BYTES + C::B_BYTES + C::SFA_BYTES + C::SFB_BYTES));
+                        tma_load_2d_pair(sa_s, &tmA, fb, ka, static_cast<int>(ti.a_row0));
+                        tma_load_2d_pair(sb_s, &tmB, fb, kb_, static_cast<int>(ti.b_row0));
+                        tma_load_2d_pair(sfa_s, &tmSA, fb, 0,
+                                         static_cast<int>((ti.a_ratom * p.sa_kt + ti.a_katom0 + kb) * 4));
+                        for (int h = 0; h < 2; h++)
+                            tma_load_2d_pair(sfb_s + 512 * h, &tmSB, fb, 0,
+                                             static_cast<int>(((ti.b_ratom + h) * p.sb_kt + ti.b_katom0 + kb) * 4));
+                    }
                 }
             }
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
         }
         if (lane == 0 && *abort_flag) {  // let this CTA's copies land before it exits
-            for (uint32_t j = g > STAGES ? g - STAGES : 0; j < g; j++)
-                mbar_wait_drain(bar_full + 8 * (j % STAGES), (j / STAGES) & 1);
+            if constexpr (CG == 1) {
+                for (uint32_t j = g > STAGES ? g - STAGES : 0; j < g; j++)
+                    mbar_wait_drain(bar_full + 8 * (j % STAGES), (j / STAGES) & 1);
+            } else {
+                spin_ns(2000000);  // the pair's loads complete on the other CTA's barriers
+            }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer
-        uint32_t g = 0, acc_it = 0;
-        bool issued_any = false;
-        for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
-            const TileInfo ti = resolve_tile(p, tile, lane);
-            if (!ti.valid) break;
-            if (ti.nkb == 0) continue;  // empty group: the epilogue writes zeros
-            int stop = 0;
-            if (lane == 0) {
-                // the epilogue must have drained the previous accumulator
-                if (acc_it > 0 && !mbar_wait(bar_acce, (acc_it - 1) & 1, abort_flag, &g_device_error)) stop = 1;
-                tc_fence_after();
-                for (int kb = 0; kb < ti.nkb && !stop; kb++, g++) {
-                    const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
-                    if (!mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_device_error)) { stop = 1; break; }
+        if (CG == 1 || leader) {
+            uint32_t g = 0, acc_it = 0;
+            bool issued_any = false;
+            for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
+                const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank);
+                if (!ti.valid) break;
+                if (ti.nkb == 0) continue;  // empty group: the epilogue writes zeros
+                int stop = 0;
+                if (lane == 0) {
+                    // the epilogue must have drained the previous accumulator
+                    if (acc_it > 0 && !mbar_wait(bar_acce, (acc_it - 1) & 1, abort_flag, &g_device_error)) stop = 1;
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem + SF_COL0 + s * SF_STRIDE, sfb_t = sfa_t + 4;
-                    tc_cp_32x128b_warpx4(sfa_t, smem_desc(sbase + OFF_SFA + s * SFA_BYTES, 0, 128, 0));
-                    tc_cp_32x128b_warpx4(sfb_t, smem_desc(sbase + OFF_SFB + s * SFB_BYTES, 0, 128, 0));
-                    tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sbase + OFF_SFB + s * SFB_BYTES + 512, 0, 128, 0));
-                    const int kk = (kb == ti.nkb - 1) ? ti.k_last : 4;
-                    for (int j = 0; j < kk; j++) {
-                        const uint64_t ad = smem_desc(sbase + OFF_A + s * A_BYTES + 32 * j, 0, 1024, 2);
-                        const uint64_t bd = smem_desc(sbase + OFF_B + s * B_BYTES + 32 * j, 0, 1024, 2);
-                        tc_mma_mxf8(tmem, ad, bd, make_idesc(static_cast<uint32_t>(j)), sfa_t, sfb_t,
-                                    (kb | j) != 0 ? 1u : 0u);
+                    bool ready = false;  // stage g known to have landed (from the previous stage's peek)
+                    for (int kb = 0; kb < ti.nkb && !stop; kb++, g++) {
+                        const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
+                        if (!ready && !mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_device_error)) { stop = 1; break; }
+                        tc_fence_after();
+                        const uint32_t sfa_t = tmem + SF_COL0 + s * SF_STRIDE, sfb_t = sfa_t + 4;
+                        const uint64_t dA = smem_desc(sbase + C::OFF_SFA + s * C::SFA_BYTES, 0, 128, 0);
+                        const uint64_t dB0 = smem_desc(sbase + C::OFF_SFB + s * C::SFB_BYTES, 0, 128, 0);
+                        const uint64_t dB1 = smem_desc(sbase + C::OFF_SFB + s * C::SFB_BYTES + 512, 0, 128, 0);
+                        if constexpr (CG == 2) {
+                            tc_cp_32x128b_warpx4_pair(sfa_t, dA);
+                            tc_cp_32x128b_warpx4_pair(sfb_t, dB0);
+                            tc_cp_32x128b_warpx4_pair(sfb_t + 4, dB1);
+                        } else {
+                            tc_cp_32x128b_warpx4(sfa_t, dA);
+                            tc_cp_32x128b_warpx4(sfb_t, dB0);
+                            tc_cp_32x128b_warpx4(sfb_t + 4, dB1);
+                        }
+                        const int kk = (kb == ti.nkb - 1) ? ti.k_last : 4;
+                        issued_any = true;
+                        if (kk == 4 && kb + 1 < ti.nkb) {
+                            uint64_t ad[4], bd[4];
+                            uint32_t id[4];
+#pragma unroll
+                            for (int j = 0; j < 4; j++) {
+                                ad[j] = smem_desc(sbase + C::OFF_A + s * C::A_BYTES + 32 * j, 0, 1024, 2);
+                                bd[j] = smem_desc(sbase + C::OFF_B + s * C::B_BYTES + 32 * j, 0, 1024, 2);
+                                id[j] = make_idesc<CG>(j);
+                            }
+                            const uint32_t s1 = (g + 1) % STAGES, ph1 = ((g + 1) / STAGES) & 1;
+                            ready = mma4_commit_peek<CG>(tmem, ad, bd, id, sfa_t, sfb_t, kb != 0 ? 1u : 0u,
+                                                         bar_empty + 8 * s, bar_full + 8 * s1, ph1);
+                            continue;
+                        }
+                        for (int j = 0; j < kk; j++) {
+                            const uint64_t ad = smem_desc(sbase + C::OFF_A + s * C::A_BYTES + 32 * j, 0, 1024, 2);
+                            const uint64_t bd = smem_desc(sbase + C::OFF_B + s * C::B_BYTES + 32 * j, 0, 1024, 2);
+                            const uint32_t acc = (kb | j) != 0 ? 1u : 0u;
+                            if constexpr (CG == 2)
+                                tc_mma_mxf8_pair(tmem, ad, bd, make_idesc<CG>(j), sfa_t, sfb_t, acc);
+                            else
+                                tc_mma_mxf8(tmem, ad, bd, make_idesc<CG>(j), sfa_t, sfb_t, acc);
+                        }
+                        if constexpr (CG == 2) tc_commit_pair_mc(bar_empty + 8 * s, 3);
+                        else tc_commit(bar_empty + 8 * s);
+                        ready = false;
                     }
-                    issued_any = true;
-                    tc_commit(bar_empty + 8 * s);
+                    if (!stop) {
+                        if constexpr (CG == 2) tc_commit_pair_mc(bar_accf, 3);
+                        else tc_commit(bar_accf);
+                    }
                 }
-                if (!stop) tc_commit(bar_accf);
+                acc_it++;
+                if (__shfl_sync(0xffffffffu, stop, 0)) break;
             }
-            acc_it++;
-            if (__shfl_sync(0xffffffffu, stop, 0)) break;
-        }
-        if (lane == 0 && issued_any && *abort_flag) {  // no MMA in flight at dealloc
-            tc_commit(bar_drain);
-            mbar_wait_drain(bar_drain, 0);
+            if (lane == 0 && issued_any && *abort_flag) {  // no MMA in flight at dealloc
+                if constexpr (CG == 2) tc_commit_pair_mc(bar_drain, 1);
+                else tc_commit(bar_drain);
+                mbar_wait_drain(bar_drain, 0);
+            }
         }
     } else {
         // ---------------------------------------------------- epilogue
@@ -304,8 +468,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // warp, then store: the global stores overlap the next tile's mainloop.
         const int sub = warp & 3;
         uint32_t acc_it = 0;
-        for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
-            const TileInfo ti = resolve_tile(p, tile, lane);
+        for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
+            const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank);
             if (!ti.valid) break;
             const int64_t grow = ti.out_row0 + 32 * sub + lane;
             const bool row_ok = grow >= ti.row_lo && grow < ti.row_hi;
@@ -317,21 +481,35 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!mbar_wait(bar_accf, acc_it & 1, abort_flag, &g_device_error)) break;
             tc_fence_after();
+            // four quarters of 2 x 32 columns: two TMEM loads in flight per wait
             uint32_t pk[BN / 2];
 #pragma unroll
-            for (int ch = 0; ch < BN / 32; ch++) {
-                if (ti.col0 + 32 * ch < ti.col_hi) {  // warp-uniform
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * sub) << 16) + 32 * ch, r);
-                    tc_wait_ld();
+            for (int h = 0; h < 4; h++) {
+                uint32_t r[2][32];
 #pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        pk[16 * ch + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                for (int q = 0; q < 2; q++) {
+                    const int ch = 2 * h + q;
+                    if (ti.col0 + 32 * ch < ti.col_hi)  // warp-uniform
+                        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * sub) << 16) + 32 * ch, r[q]);
+                }
+                tc_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 2; q++) {
+                    const int ch = 2 * h + q;
+                    if (ti.col0 + 32 * ch < ti.col_hi) {
+#pragma unroll
+                        for (int i = 0; i < 16; i++)
+                            pk[16 * ch + i] =
+                                pack_bf16x2(__uint_as_float(r[q][2 * i]), __uint_as_float(r[q][2 * i + 1]));
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acce);
+            if (lane == 0) {
+                if constexpr (CG == 2) mbar_arrive_cluster(lead_acce);
+                else mbar_arrive(bar_acce);
+            }
             acc_it++;
             if (!row_ok) continue;
 #pragma unroll
@@ -355,10 +533,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        if constexpr (CG == 2) tmem_dealloc_pair(tmem, TMEM_COLS);
+        else tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -394,6 +573,99 @@ bool make_tmap(CUtensorMap *m, const uint8_t *base, int64_t rows, int64_t k, uin
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A swz scale buffer of `bytes` bytes seen as rows of 128 bytes; one box of
+// 4 rows is one 512-byte scale tile.
+bool make_scale_tmap(CUtensorMap *m, const uint8_t *base, int64_t bytes) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(bytes / 128)};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, 4};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int64_t scale_bytes_of(int64_t rows, int64_t k) { return (rows + 127) / 128 * 128 * ((k / 32 + 3) / 4 * 4); }
+
+// CTAs per tile.  Single-CTA tiles are the default: on GB300 the pair tile
+// moves a third less operand data per SM but measured slower (1440 vs 1493
+// TFLOP/s over the bench step), because the kernel is bound by the issue
+// chain of its single MMA thread, not by operand delivery.
+// MXQ_GEMM_CTA_GROUP=2 selects pair tiles (read once per process).
+int cta_group_for(const GemmProblem &) {
+    static int forced = [] {
+        const char *v = getenv("MXQ_GEMM_CTA_GROUP");
+        return v ? atoi(v) : 0;
+    }();
+    return forced == 2 ? 2 : 1;
+}
+
+template <int CG>
+cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
+    using C = Cfg<CG>;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(k_gemm_mxf8<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    CUtensorMap tmA, tmB, tmSA, tmSB;
+    if (!make_tmap(&tmA, g.a, g.a_rows, g.a_k, C::BM) || !make_tmap(&tmB, g.b, g.b_rows, g.b_k, C::B_ROWS))
+        return cudaErrorInvalidValue;
+    if (CG == 2) {
+        if (!make_scale_tmap(&tmSA, g.sa, scale_bytes_of(g.a_rows, g.a_k)) ||
+            !make_scale_tmap(&tmSB, g.sb, scale_bytes_of(g.b_rows, g.b_k)))
+            return cudaErrorInvalidValue;
+    } else {
+        tmSA = tmA;  // unused
+        tmSB = tmB;
+    }
+    p.m_tiles = static_cast<int>((g.M + C::TILE_M - 1) / C::TILE_M);
+    if (g.mode == kDense) p.total_tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    else if (g.mode == kGroupedRows) p.total_tiles = ((g.T + C::TILE_M - 1) / C::TILE_M + g.E) * p.n_tiles;
+    else p.total_tiles = static_cast<int64_t>(g.E) * p.m_tiles * p.n_tiles;
+    if (p.total_tiles <= 0) return cudaSuccess;
+
+    // persistent grid: as many CTAs (CTA pairs) as can be resident at once, one
+    // per SM (a CTA needs ~200 KB of shared memory)
+    static int resident[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = st;
+    if (CG == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (resident[dev] == 0) {
+        if (CG == 2) {
+            cfg.gridDim = dim3(2);
+            int clusters = 0;
+            e = cudaOccupancyMaxActiveClusters(&clusters, k_gemm_mxf8<CG>, &cfg);
+            if (e != cudaSuccess) return e;
+            resident[dev] = clusters > 0 ? clusters : 1;
+        } else {
+            e = cudaDeviceGetAttribute(&resident[dev], cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    const int64_t units = p.total_tiles < resident[dev] ? p.total_tiles : resident[dev];
+    cfg.gridDim = dim3(static_cast<unsigned>(units * CG));
+    return cudaLaunchKernelEx(&cfg, k_gemm_mxf8<CG>, tmA, tmB, tmSA, tmSB, p);
+}
+
 }  // namespace
 
 cudaError_t read_and_clear_device_error(unsigned int *word) {
@@ -404,17 +676,6 @@ cudaError_t read_and_clear_device_error(unsigned int *word) {
 }
 
 cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(k_gemm_mxf8, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
-
-    CUtensorMap tmA, tmB;
-    if (!make_tmap(&tmA, g.a, g.a_rows, g.a_k, BM) || !make_tmap(&tmB, g.b, g.b_rows, g.b_k, BN))
-        return cudaErrorInvalidValue;
-
     Params p{};
     p.mode = g.mode;
     p.sa = g.sa; p.sb = g.sb;
@@ -427,26 +688,9 @@ cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
     p.b_row_per_expert = g.b_row_per_expert;
     p.b_k_per_expert = g.b_k_per_expert;
     p.c_expert_stride = g.c_expert_stride;
-    p.m_tiles = static_cast<int>((g.M + BM - 1) / BM);
     p.n_tiles = static_cast<int>((g.N + BN - 1) / BN);
     p.n_fastest = g.mode == kDense && g.a_rows > g.b_rows ? 1 : 0;
-    if (g.mode == kDense) p.total_tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    else if (g.mode == kGroupedRows) p.total_tiles = ((g.T + BM - 1) / BM + g.E) * p.n_tiles;
-    else p.total_tiles = static_cast<int64_t>(g.E) * p.m_tiles * p.n_tiles;
-    if (p.total_tiles <= 0) return cudaSuccess;
-    // persistent grid: one CTA per SM (the CTA needs ~200 KB of shared memory)
-    static int num_sms[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (num_sms[dev] == 0) {
-        e = cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
-    const int64_t grid = p.total_tiles < num_sms[dev] ? p.total_tiles : num_sms[dev];
-    k_gemm_mxf8<<<static_cast<unsigned>(grid), THREADS, SMEM_ALLOC, st>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    return cta_group_for(g) == 2 ? launch_cg<2>(g, p, st) : launch_cg<1>(g, p, st);
 }
 
 }  // namespace mxq
