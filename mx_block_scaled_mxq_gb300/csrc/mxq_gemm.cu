@@ -54,6 +54,7 @@ namespace {
 
 constexpr int BN = 256, BK = 128, THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512, SF_COL0 = 256, SF_STRIDE = 16;
+constexpr int kMaxTableE = 1024;  // experts whose group tables are kept in shared memory
 
 template <int CG>
 struct Cfg {
@@ -69,7 +70,8 @@ struct Cfg {
     static constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
     static constexpr uint32_t NUM_BARS = 2 * STAGES + 3;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 128;
-    static constexpr uint32_t SMEM_ALLOC = OFF_MISC + 256 + 1024;  // + slack to align the base to 1024
+    static constexpr uint32_t OFF_GRP = OFF_MISC + 256;  // group tables (grouped modes, E <= kMaxTableE)
+    static constexpr uint32_t SMEM_ALLOC = OFF_GRP + 2 * 8 * (kMaxTableE + 1) + 1024;  // + slack to align the base
     static_assert(NUM_BARS * 8 <= 128, "barrier area");
     static_assert(SF_COL0 + STAGES * SF_STRIDE <= TMEM_COLS, "tmem budget");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
@@ -107,13 +109,81 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t j) {
 
 // Work decomposition: which tile this CTA computes (run by all lanes of a warp).
 // `rank` is the CTA's position in its pair (0 for CG = 1).
+// Group tables a CTA builds once in shared memory (grouped modes with
+// E <= kMaxTableE): off[e] = group offsets, pre[e] = exclusive prefix of the
+// per-expert tile counts (kGroupedRows) or of the padded group lengths
+// (kGroupedK).  Tiles are then decoded without touching global memory.
+struct GroupTables {
+    const int64_t *off, *pre;
+};
+
 template <int CG>
-__device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_t rank) {
+__device__ void build_group_tables(const Params &p, int64_t *off, int64_t *pre, int warp, int lane) {
+    constexpr int TM = Cfg<CG>::TILE_M;
+    if (warp != 0) return;
+    int64_t run = 0;
+    for (int base = 0; base <= p.E; base += 32) {
+        const int e = base + lane;
+        int64_t o0 = 0, o1 = 0;
+        if (e <= p.E) { o0 = p.offsets[e]; off[e] = o0; }
+        if (e < p.E) o1 = p.offsets[e + 1];
+        int64_t v = 0;
+        if (e < p.E) {
+            if (p.mode == kGroupedRows) v = (o1 > o0) ? ((o1 - 1) / TM - o0 / TM + 1) * p.n_tiles : 0;
+            else v = (o1 - o0 + 127) / 128 * 128;
+        }
+        int64_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        if (e <= p.E) pre[e] = run + incl - v;
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+}
+
+template <int CG>
+__device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_t rank, const GroupTables &gt) {
     constexpr int TM = Cfg<CG>::TILE_M, BR = Cfg<CG>::B_ROWS;
     TileInfo t{};
     t.k_last = 4;
     int64_t tile_row0 = 0, bn0 = 0;  // first row of the tile; first row of B for the tile
-    if (p.mode == kDense) {
+    if (p.mode == kGroupedRows && gt.off != nullptr) {
+        // the expert whose tile range [pre[e], pre[e+1]) holds bid (binary search)
+        if (bid >= gt.pre[p.E]) { t.valid = 0; return t; }
+        int lo = 0, hi = p.E;  // pre[lo] <= bid < pre[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (gt.pre[mid] <= bid) lo = mid; else hi = mid;
+        }
+        const int fe = lo;
+        const int64_t fo0 = gt.off[fe], fo1 = gt.off[fe + 1];
+        const int64_t mtiles_e = (fo1 - 1) / TM - fo0 / TM + 1;
+        const int64_t local = bid - gt.pre[fe];
+        const int64_t nt = local / mtiles_e, mt = fo0 / TM + local % mtiles_e;
+        t.valid = 1;
+        tile_row0 = mt * TM;
+        bn0 = fe * p.b_row_per_expert + nt * BN;
+        t.b_k0 = fe * p.b_k_per_expert; t.b_katom0 = t.b_k0 / BK;
+        t.col0 = nt * BN;
+        t.row_lo = max(fo0, tile_row0 + 128 * rank);
+        t.row_hi = min(fo1, tile_row0 + 128 * rank + 128);
+    } else if (p.mode == kGroupedK && gt.off != nullptr) {
+        const int64_t per = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+        const int e = static_cast<int>(bid / per);
+        const int64_t local = bid % per, mt = local % p.m_tiles, nt = local / p.m_tiles;
+        const int64_t pe = gt.pre[e], ne = gt.off[e + 1] - gt.off[e];
+        t.valid = 1;
+        tile_row0 = mt * TM;
+        bn0 = nt * BN;
+        t.a_k0 = t.b_k0 = pe; t.a_katom0 = t.b_katom0 = pe / BK;
+        t.nkb = static_cast<int>((ne + 127) / 128);
+        t.col0 = nt * BN;
+        t.row_lo = tile_row0 + 128 * rank;
+        t.row_hi = min(p.M, t.row_lo + 128);
+        t.c_off = static_cast<int64_t>(e) * p.c_expert_stride;
+    } else if (p.mode == kDense) {
         // raster so that the smaller operand stays in L2 while the larger one
         // streams through once: concurrent CTAs share the larger operand's tile
         const int64_t mt = p.n_fastest ? bid / p.n_tiles : bid % p.m_tiles;
@@ -327,6 +397,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    GroupTables gt{nullptr, nullptr};
+    if (p.mode != kDense && p.E <= kMaxTableE) {
+        int64_t *off = reinterpret_cast<int64_t *>(smem + C::OFF_GRP), *pre = off + kMaxTableE + 1;
+        build_group_tables<CG>(p, off, pre, warp, lane);
+        __syncthreads();
+        gt.off = off;
+        gt.pre = pre;
+    }
     // stage barriers and the accumulator-release barrier of the even CTA
     uint32_t lead_full = bar_full, lead_acce = bar_acce;
     if constexpr (CG == 2) {
@@ -339,7 +417,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------------------------------------------- TMA producer
         uint32_t g = 0;  // k-blocks issued by this CTA (lane 0)
         for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
-            const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank);
+            const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
             if (!ti.valid) break;  // grouped-row tiles past the real count come last
             int stop = 0;
             if (lane == 0) {
@@ -393,7 +471,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t g = 0, acc_it = 0;
             bool issued_any = false;
             for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
-                const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank);
+                const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
                 if (!ti.valid) break;
                 if (ti.nkb == 0) continue;  // empty group: the epilogue writes zeros
                 int stop = 0;
@@ -469,7 +547,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int sub = warp & 3;
         uint32_t acc_it = 0;
         for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
-            const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank);
+            const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
             if (!ti.valid) break;
             const int64_t grow = ti.out_row0 + 32 * sub + lane;
             const bool row_ok = grow >= ti.row_lo && grow < ti.row_hi;
