@@ -58,9 +58,12 @@ def _load():
         lib.oracle_swizzle_scales.argtypes = [p, i64, i64, i64, p]
         lib.oracle_mxfp4_qdq.argtypes = [p, p, i64, i64, f32]
         lib.oracle_mxfp4_quant.argtypes = [p, i64, i64, i64, f32, p, i64, p, i64]
+        lib.oracle_mxfp4_saturation_mask.argtypes = [p, i64, i64, f32, p]
+        lib.oracle_mxfp4_ste_backward.argtypes = [p, p, i64, i64, p]
         for name in ("oracle_mxfp8_quant_rows", "oracle_mxfp8_quant_cols",
                      "oracle_mxfp8_quant_cols_grouped", "oracle_swizzle_scales",
-                     "oracle_mxfp4_qdq", "oracle_mxfp4_quant"):
+                     "oracle_mxfp4_qdq", "oracle_mxfp4_quant", "oracle_mxfp4_saturation_mask",
+                     "oracle_mxfp4_ste_backward"):
             getattr(lib, name).restype = None
         _lib = lib
     return _lib
@@ -213,12 +216,41 @@ def mxfp4_quant(x: np.ndarray, scale_factor: float = 6.0):
     return p, s
 
 
+def mxfp4_saturation_mask(x: np.ndarray, scale_factor: float = 6.0) -> np.ndarray:
+    """Packed saturation mask of MXFP4 quant-dequant (AMCT FakeQuant article,
+    section 4.1, clipped STE): uint32 [rows x ceil(cols/32)], bit i of word
+    (r, b) set when |x[r, 32b+i]| > 6 * (the block's scale)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    cols = x.shape[-1] if x.ndim else 1
+    rows = x.size // cols if cols else 0
+    m = np.zeros((rows, (cols + 31) // 32), np.uint32)
+    if x.size:
+        _load().oracle_mxfp4_saturation_mask(_ptr(x), rows, cols, float(scale_factor), _ptr(m))
+    return m
+
+
+def mxfp4_ste_backward(gy: np.ndarray, mask: np.ndarray) -> np.ndarray:
+    """Clipped-STE gradient (AMCT FakeQuant article, section 4.1): gy with
+    the saturated elements (mask bits, as from mxfp4_saturation_mask) set to
+    +0.0."""
+    gy = np.ascontiguousarray(gy, dtype=np.float32)
+    mask = np.ascontiguousarray(mask, dtype=np.uint32)
+    cols = gy.shape[-1] if gy.ndim else 1
+    rows = gy.size // cols if cols else 0
+    assert mask.shape == (rows, (cols + 31) // 32)
+    gx = np.empty_like(gy)
+    if gy.size:
+        _load().oracle_mxfp4_ste_backward(_ptr(gy), _ptr(mask), rows, cols, _ptr(gx))
+    return gx
+
+
 from .gemm import (dequant_mxfp8, dequant_mxfp4, gemm_ref, grouped_fwd_ref,  # noqa: E402
                    grouped_dw_ref, linear_ref)
 
 __all__ = [
     "build", "e4m3_encode", "e4m3_decode_table", "e2m1_decode_table", "mxfp8_scale_exp",
     "mxfp4_scale_exp", "mxfp8_quant_rows", "mxfp8_quant_cols", "mxfp8_quant_cols_grouped",
-    "padded_group_starts", "swizzle_scales", "mxfp4_qdq", "mxfp4_quant", "dequant_mxfp8",
+    "padded_group_starts", "swizzle_scales", "mxfp4_qdq", "mxfp4_quant", "mxfp4_saturation_mask",
+    "mxfp4_ste_backward", "dequant_mxfp8",
     "dequant_mxfp4", "gemm_ref", "grouped_fwd_ref", "grouped_dw_ref", "linear_ref",
 ]

@@ -332,6 +332,53 @@ void oracle_mxfp4_quant(const float *x, int64_t rows, int64_t cols, int64_t ldx,
     }
 }
 
+/* Saturation mask of MXFP4 quant-dequant ("AMCT FakeQuant" article, section
+ * 4.1 "STE 与 clipped STE"): element x of a block with scale 2^e is saturated
+ * when |x| > 6 * 2^e, i.e. when the codebook's top value 6 had to clip it.
+ * Packed as one 32-bit word per block: mask[r*nb + b] bit i is element
+ * (r, 32b + i); bits past the end of a ragged row are 0.  Reading: a block
+ * with a non-finite element has an Inf/NaN scale, so |x| > 6*scale is false
+ * for all of its elements and its word is 0. */
+void oracle_mxfp4_saturation_mask(const float *x, int64_t rows, int64_t cols, float sf, uint32_t *mask)
+{
+    int64_t nb = (cols + 31) / 32;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t b = 0; b < nb; b++) {
+            int64_t c0 = 32 * b, c1 = (c0 + 32 < cols) ? c0 + 32 : cols;
+            double amax = 0.0;
+            int nonfinite = 0;
+            for (int64_t c = c0; c < c1; c++) {
+                double v = x[r * cols + c];
+                if (!isfinite(v))
+                    nonfinite = 1;
+                else if (fabs(v) > amax)
+                    amax = fabs(v);
+            }
+            uint32_t word = 0;
+            if (!nonfinite) {
+                double limit = 6.0 * ldexp(1.0, oracle_mxfp4_scale_exp(amax, (double)sf));
+                for (int64_t c = c0; c < c1; c++)
+                    if (fabs((double)x[r * cols + c]) > limit)
+                        word |= 1u << (c - c0);
+            }
+            mask[r * nb + b] = word;
+        }
+    }
+}
+
+/* Clipped straight-through estimator, backward (same section): the gradient
+ * passes through unchanged except at saturated elements, where it is set to
+ * +0.0 (a masked fill with zero). */
+void oracle_mxfp4_ste_backward(const float *gy, const uint32_t *mask, int64_t rows, int64_t cols, float *gx)
+{
+    int64_t nb = (cols + 31) / 32;
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c < cols; c++) {
+            int sat = (mask[r * nb + c / 32] >> (c % 32)) & 1u;
+            gx[r * cols + c] = sat ? 0.0f : gy[r * cols + c];
+        }
+}
+
 double oracle_e2m1_decode(uint8_t nib)
 {
     double v = kE2M1Val[nib & 7];
