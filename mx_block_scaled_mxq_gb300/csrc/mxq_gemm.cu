@@ -54,7 +54,7 @@ namespace {
 
 constexpr int BN = 256, BK = 128, THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512, SF_COL0 = 256, SF_STRIDE = 16;
-constexpr int kMaxTableE = 1024;  // experts whose group tables are kept in shared memory
+constexpr int kMaxTableE = 256;  // experts whose group tables are kept in shared memory
 
 template <int CG>
 struct Cfg {
@@ -71,7 +71,9 @@ struct Cfg {
     static constexpr uint32_t NUM_BARS = 2 * STAGES + 3;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 128;
     static constexpr uint32_t OFF_GRP = OFF_MISC + 256;  // group tables (grouped modes, E <= kMaxTableE)
-    static constexpr uint32_t SMEM_ALLOC = OFF_GRP + 2 * 8 * (kMaxTableE + 1) + 1024;  // + slack to align the base
+    // epilogue store staging: 4 warps x 2 slots x (32 rows x 64 bytes), 1024-aligned
+    static constexpr uint32_t OFF_STORE = (OFF_GRP + 2 * 8 * (kMaxTableE + 1) + 1023) / 1024 * 1024;
+    static constexpr uint32_t SMEM_ALLOC = OFF_STORE + 4 * 2 * 2048 + 1024;  // + slack to align the base
     static_assert(NUM_BARS * 8 <= 128, "barrier area");
     static_assert(SF_COL0 + STAGES * SF_STRIDE <= TMEM_COLS, "tmem budget");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
@@ -89,6 +91,7 @@ struct Params {
     int64_t b_row_per_expert, b_k_per_expert, c_expert_stride;
     int m_tiles, n_tiles;  // tile counts (m in units of 128 * CG rows)
     int n_fastest;         // kDense tile order: 1 = n fastest (A is the larger operand)
+    int tma_store;         // epilogue stores whole 32 x 32 blocks with TMA (no row masking needed)
     int64_t total_tiles;   // tile index space (an upper bound for grouped rows)
 };
 
@@ -339,7 +342,8 @@ __device__ __forceinline__ bool mma4_commit_peek(uint32_t d_tmem, const uint64_t
 template <int CG>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_mxf8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const Params p) {
+                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                const __grid_constant__ CUtensorMap tmC, const Params p) {
     using C = Cfg<CG>;
     constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -546,15 +550,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         // warp, then store: the global stores overlap the next tile's mainloop.
         const int sub = warp & 3;
         uint32_t acc_it = 0;
+        const uint32_t st_slots = sbase + C::OFF_STORE + 2 * 2048 * sub;  // this warp's two staging slots
+        uint32_t st_count = 0;                                            // blocks this warp has stored
         for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
             const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
             if (!ti.valid) break;
             const int64_t grow = ti.out_row0 + 32 * sub + lane;
             const bool row_ok = grow >= ti.row_lo && grow < ti.row_hi;
             __nv_bfloat16 *crow = p.c + ti.c_off + grow * p.ldc;
-            if (ti.nkb == 0) {
-                if (row_ok)
-                    for (int64_t col = ti.col0; col < ti.col_hi; col++) crow[col] = __float2bfloat16_rn(0.0f);
+            if (ti.nkb == 0) {  // empty group: its weight gradient is zero
+                if (row_ok) {
+                    int64_t col = ti.col0;
+                    for (; col + 8 <= ti.col_hi; col += 8) *reinterpret_cast<uint4 *>(crow + col) = make_uint4(0, 0, 0, 0);
+                    for (; col < ti.col_hi; col++) crow[col] = __float2bfloat16_rn(0.0f);
+                }
                 continue;
             }
             if (!mbar_wait(bar_accf, acc_it & 1, abort_flag, &g_device_error)) break;
@@ -589,6 +598,37 @@ __global__ void __launch_bounds__(THREADS, 1)
                 else mbar_arrive(bar_acce);
             }
             acc_it++;
+            if (p.tma_store) {
+                // Stage each 32 x 32 block in a 64-byte-swizzled slot (conflict-free
+                // 16-byte writes) and store it with TMA; rows and columns outside the
+                // output are clipped by the tensor map.
+                const int64_t trow = ti.c_off / p.ldc + ti.out_row0 + 32 * sub;
+#pragma unroll
+                for (int ch = 0; ch < BN / 32; ch++) {
+                    const int64_t col = ti.col0 + 32 * ch;
+                    if (col >= ti.col_hi) break;  // warp-uniform
+                    const uint32_t slot = st_slots + 2048 * (st_count & 1);
+                    if (st_count >= 2) {
+                        if (lane == 0) bulk_wait_read_le1();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const uint32_t dst = slot + 64 * lane + 16 * (q ^ ((lane >> 1) & 3));
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[16 * ch + 4 * q]),
+                                     "r"(pk[16 * ch + 4 * q + 1]), "r"(pk[16 * ch + 4 * q + 2]), "r"(pk[16 * ch + 4 * q + 3])
+                                     : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, slot, static_cast<int>(col), static_cast<int>(trow));
+                        bulk_commit_group();
+                    }
+                    st_count++;
+                }
+                continue;
+            }
             if (!row_ok) continue;
 #pragma unroll
             for (int ch = 0; ch < BN / 32; ch++) {
@@ -610,6 +650,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
 
+    if (warp >= 2 && lane == 0) bulk_wait_all();  // staged stores done before shared memory goes away
     tc_fence_before();
     if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     if (warp == 1) {
@@ -665,6 +706,19 @@ bool make_scale_tmap(CUtensorMap *m, const uint8_t *base, int64_t bytes) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 output [rows x n] with leading dimension ld (elements); 32 x 32 boxes,
+// 64-byte swizzle (the staging slots' layout).
+bool make_out_tmap(CUtensorMap *m, void *base, int64_t rows, int64_t n, int64_t ld) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int64_t scale_bytes_of(int64_t rows, int64_t k) { return (rows + 127) / 128 * 128 * ((k / 32 + 3) / 4 * 4); }
 
 // CTAs per tile.  Single-CTA tiles are the default: on GB300 the pair tile
@@ -690,7 +744,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     });
     if (attr_err != cudaSuccess) return attr_err;
 
-    CUtensorMap tmA, tmB, tmSA, tmSB;
+    CUtensorMap tmA, tmB, tmSA, tmSB, tmC;
     if (!make_tmap(&tmA, g.a, g.a_rows, g.a_k, C::BM) || !make_tmap(&tmB, g.b, g.b_rows, g.b_k, C::B_ROWS))
         return cudaErrorInvalidValue;
     if (CG == 2) {
@@ -702,6 +756,13 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         tmSB = tmB;
     }
     p.m_tiles = static_cast<int>((g.M + C::TILE_M - 1) / C::TILE_M);
+    // TMA stores need whole tiles to belong to one output: always for dense
+    // problems, for the grouped weight gradient when each expert's rows fill
+    // whole 128-row tiles; the grouped forward / input gradient mask rows.
+    const int64_t c_rows = g.mode == kGroupedK ? static_cast<int64_t>(g.E) * g.M : g.M;
+    p.tma_store = (g.mode == kDense || (g.mode == kGroupedK && g.M % C::TILE_M == 0)) && c_rows < (1ll << 31) &&
+                  make_out_tmap(&tmC, g.c, c_rows, g.N, g.ldc) ? 1 : 0;
+    if (!p.tma_store) tmC = tmA;  // unused
     if (g.mode == kDense) p.total_tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     else if (g.mode == kGroupedRows) p.total_tiles = ((g.T + C::TILE_M - 1) / C::TILE_M + g.E) * p.n_tiles;
     else p.total_tiles = static_cast<int64_t>(g.E) * p.m_tiles * p.n_tiles;
@@ -741,7 +802,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     }
     const int64_t units = p.total_tiles < resident[dev] ? p.total_tiles : resident[dev];
     cfg.gridDim = dim3(static_cast<unsigned>(units * CG));
-    return cudaLaunchKernelEx(&cfg, k_gemm_mxf8<CG>, tmA, tmB, tmSA, tmSB, p);
+    return cudaLaunchKernelEx(&cfg, k_gemm_mxf8<CG>, tmA, tmB, tmSA, tmSB, tmC, p);
 }
 
 }  // namespace
