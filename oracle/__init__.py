@@ -245,7 +245,7 @@ def mxfp4_ste_backward(gy: np.ndarray, mask: np.ndarray) -> np.ndarray:
 
 
 from .gemm import (dequant_mxfp8, dequant_mxfp4, gemm_ref, grouped_fwd_ref,  # noqa: E402
-                   grouped_dw_ref, linear_ref)
+                   grouped_dw_ref, linear_ref, qat_linear_ref)
 
 __all__ = [
     "build", "e4m3_encode", "e4m3_decode_table", "e2m1_decode_table", "mxfp8_scale_exp",
@@ -253,4 +253,5 @@ __all__ = [
     "padded_group_starts", "swizzle_scales", "mxfp4_qdq", "mxfp4_quant", "mxfp4_saturation_mask",
     "mxfp4_ste_backward", "dequant_mxfp8",
     "dequant_mxfp4", "gemm_ref", "grouped_fwd_ref", "grouped_dw_ref", "linear_ref",
+    "qat_linear_ref",
 ]

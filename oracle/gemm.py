@@ -112,3 +112,25 @@ def linear_ref(x, w, dy):
     dx = gemm_ref(qdy, sdy, qwT, swT)
     dw = gemm_ref(qdyT, sdyT, qxT, sxT)
     return y, dx, dw
+
+
+def qat_linear_ref(x, w, bias=None, quantize_input: bool = True, scale_factor: float = 6.0):
+    """Forward of the MXFP4 QAT linear layer ("AMCT FakeQuant" article,
+    section 4.3): Y = F.linear(Q(x), Q(W), b) with Q the MXFP4 quant-dequant
+    (blocks of 32 along the input-feature dim K) and the bias not quantized;
+    quantize_input=False leaves x unquantized (W4A16).  x: bf16 [M x K],
+    w: bf16 [N x K], bias: bf16 [N] or None.  bf16 values widen exactly to
+    fp32 for the quant-dequant, whose outputs (codebook value x 2^e, e >= -30)
+    are again exact; the product is binary64.  Returns binary64 [M x N]."""
+    from . import _bf16_bits, mxfp4_qdq
+
+    def widen(t):
+        return (_bf16_bits(t).astype(np.uint32) << 16).view(np.float32)
+
+    xf, wf = widen(x), widen(w)
+    qx = mxfp4_qdq(xf, scale_factor) if quantize_input else xf
+    qw = mxfp4_qdq(wf, scale_factor)
+    y = qx.astype(np.float64) @ qw.astype(np.float64).T
+    if bias is not None:
+        y = y + widen(bias).astype(np.float64)[None, :]
+    return y

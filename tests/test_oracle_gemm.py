@@ -95,3 +95,60 @@ def test_grouped_refs_are_per_slice_and_zero_for_empty_groups():
         a, sa = oracle.mxfp8_quant_cols(dy[r0:r1])
         b, sb = oracle.mxfp8_quant_cols(x[r0:r1])
         assert np.array_equal(dw[e], oracle.gemm_ref(a, sa, b, sb))
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 QAT linear forward (AMCT FakeQuant article, section 4.3)
+# ---------------------------------------------------------------------------
+
+def _bf16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _on_mxfp4_grid(R, K, seed):
+    """bf16 [R x K] whose every 32-block along K holds +-6 * 2^e (so that the
+    block's scale is exactly 2^e) and otherwise codebook values x 2^e, e
+    varying per block: a fixed point of the MXFP4 quant-dequant along K only."""
+    rng = np.random.default_rng(seed)
+    book = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    v = rng.choice(book, size=(R, K)) * rng.choice([-1.0, 1.0], size=(R, K))
+    v[:, ::32] = 6.0 * rng.choice([-1.0, 1.0], size=(R, K // 32))
+    e = rng.integers(-8, 8, size=(R, K // 32))
+    return v * np.repeat(np.exp2(e), 32, axis=1)
+
+
+def test_qat_ref_is_exact_product_on_the_mxfp4_grid():
+    """Inputs already on the MXFP4 grid along K are left unchanged by Q, so Y
+    is their plain product; quantizing along any other axis would move them."""
+    x, w = _on_mxfp4_grid(48, 128, 1), _on_mxfp4_grid(40, 128, 2)
+    y = oracle.qat_linear_ref(_bf16(x), _bf16(w))
+    assert np.array_equal(y, x @ w.T)
+    assert not np.array_equal(oracle.mxfp4_qdq(x.T.astype(np.float32).copy()), x.T.astype(np.float32))
+
+
+def test_qat_ref_w4a16_leaves_the_input_unquantized():
+    rng = np.random.default_rng(3)
+    x = _bf16(rng.standard_normal((32, 96)))
+    w = _on_mxfp4_grid(24, 96, 4)
+    xf = x.to(torch.float64).numpy()
+    assert np.array_equal(oracle.qat_linear_ref(x, _bf16(w), quantize_input=False), xf @ w.T)
+    assert not np.array_equal(oracle.qat_linear_ref(x, _bf16(w), quantize_input=True), xf @ w.T)
+
+
+def test_qat_ref_bias_is_not_quantized():
+    rng = np.random.default_rng(5)
+    x = _bf16(rng.standard_normal((8, 64)))
+    b = _bf16(0.1 + 0.01 * rng.standard_normal(16))  # off the MXFP4 grid
+    y = oracle.qat_linear_ref(x, _bf16(np.zeros((16, 64))), b)
+    assert np.array_equal(y, np.broadcast_to(b.to(torch.float64).numpy(), (8, 16)))
+
+
+def test_qat_ref_matches_packed_mxfp4_route():
+    """Q via packed MXFP4 codes + scales, dequantized, gives the same product."""
+    x = mxq_inputs.mxfp4_large(64, 256, seed=6)
+    w = mxq_inputs.mxfp4_large(32, 256, seed=7)
+    xb, wb = _bf16(x), _bf16(w)
+    px, sx = oracle.mxfp4_quant(xb.to(torch.float32).numpy())
+    pw, sw = oracle.mxfp4_quant(wb.to(torch.float32).numpy())
+    ref = oracle.dequant_mxfp4(px, sx) @ oracle.dequant_mxfp4(pw, sw).T
+    assert np.array_equal(oracle.qat_linear_ref(xb, wb), ref)
