@@ -49,11 +49,11 @@ PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f in ("mxq_gemm.cu", "mxq_device.cuh")]
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the GEMM
 # kernel for each launch the timed region brackets, from one ncu capture of the
-# full-size launches (profiles/k_gemm_mxf8__bench_launches_dram.md), keyed by a
+# full-size launches (profiles/k_gemm__bench_launches_dram.md), keyed by a
 # hash of the kernel source; when the source has changed since, traffic is null.
 GEMM_DRAM_TRAFFIC = {
-    "09f75a733c8a93f1": {"linear_dw_gemm": 252425728, "moe_fwd_gemm": 1491229184,
-                         "moe_dx_gemm": 1528273152, "moe_dw_gemm": 2261080832},
+    "5fedab98aa70dec5": {"linear_dw_gemm": 261166592, "moe_fwd_gemm": 1521294848,
+                         "moe_dx_gemm": 1531592192, "moe_dw_gemm": 2234944768},
 }
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
@@ -277,6 +277,24 @@ def time_steps(fn, steps, world):
     return s.elapsed_time(e) / 1e3
 
 
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+
+
+def time_flushed(fn, n, flush):
+    """Mean CUDA-event time (ms) of fn over n calls, each after writing a buffer
+    twice the size of L2 so that no call finds its inputs cached."""
+    total = 0.0
+    for _ in range(n):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        total += a.elapsed_time(b)
+    return total / n
+
+
 def gemm_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -445,7 +463,7 @@ def main():
         "data": "synthetic (seeded: N(0,1) X, N(0,0.02) W, N(0,1e-3) dY; Dirichlet(0.5) groups; t(3) MXFP4 input)",
         "config": {"workload": WORKLOAD, "mode": args.mode, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (step touches > 8 GB)", "step_gemm_flop": STEP_FLOP},
-        "roofline": {"bound": "tensor", "kernel": "k_gemm_mxf8 (tcgen05 kind::mxf8f6f4)",
+        "roofline": {"bound": "tensor", "kernel": "k_gemm<1,MXF8,0> (tcgen05 kind::mxf8f6f4)",
                      "achieved": round(achieved, 1) if achieved else None,
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / fp8_peak, 4) if achieved else None,
@@ -475,6 +493,23 @@ def component_timings(wl, world):
     ds = torch.empty(m.mxq_scale_bytes(M, N // 32), dtype=torch.uint8, device=wl.dev)
     dqT = torch.empty((N, M), dtype=torch.uint8, device=wl.dev)
     dsT = torch.empty(m.mxq_scale_bytes(N, M // 32), dtype=torch.uint8, device=wl.dev)
+    R4, C4 = FP4["R"], FP4["C"]
+    m4 = torch.empty((R4, C4 // 32), dtype=torch.int32, device=wl.dev)
+    g4 = torch.empty_like(wl.a4)
+    qat_ws_bytes = m.mxq_qat_linear_workspace_bytes(M, N, K, 1)
+    qat_ws = torch.empty(qat_ws_bytes, dtype=torch.uint8, device=wl.dev)
+    wc_bytes = m.mxq_linear_weight_cache_bytes(N, K)
+    wcache = torch.empty(wc_bytes, dtype=torch.uint8, device=wl.dev)
+
+    def layer_wq():  # one micro-batch with W's quantization taken from the cache (ctx layouts share a prefix)
+        m.mxq_linear_fwd_wq(wl.x, wcache, M, N, K, wl.mode, wl.lctx, wl.y, wl.lws, wl.lwsb)
+        m.mxq_linear_bwd_dx_wq(wl.dy, wcache, M, N, K, wl.mode, wl.lctx, wl.dx, wl.lws, wl.lwsb)
+        m.mxq_linear_bwd_dw(wl.dy, wl.x, M, N, K, wl.mode, wl.lctx, wl.dw, wl.lws, wl.lwsb)
+
+    def layer_plain():
+        m.mxq_linear_fwd(wl.x, wl.w, M, N, K, wl.mode, wl.lctx, wl.y, wl.lws, wl.lwsb)
+        m.mxq_linear_bwd_dx(wl.dy, wl.w, M, N, K, wl.mode, wl.lctx, wl.dx, wl.lws, wl.lwsb)
+        m.mxq_linear_bwd_dw(wl.dy, wl.x, M, N, K, wl.mode, wl.lctx, wl.dw, wl.lws, wl.lwsb)
     parts = {
         "linear_fwd": lambda: m.mxq_linear_fwd(wl.x, wl.w, M, N, K, wl.mode, wl.lctx, wl.y, wl.lws, wl.lwsb),
         "linear_bwd_dx": lambda: m.mxq_linear_bwd_dx(wl.dy, wl.w, M, N, K, wl.mode, wl.lctx, wl.dx, wl.lws, wl.lwsb),
@@ -483,13 +518,20 @@ def component_timings(wl, world):
         "moe_grouped_col_quant_X": lambda: m.mxq_quantize_grouped_col(wl.xm, T, Km, wl.off, E, wl.t_pad, wl.xmqT,
                                                                       wl.xmsT),
         "moe_fwd": lambda: m.mxq_grouped_gemm(m.GG_FWD, wl.xmq, wl.xms, wl.wmq, wl.wms, wl.off, E, T, Nm, Km, 0, wl.ym),
-        "mxfp4_qdq": lambda: m.mxq_qdq_mxfp4(wl.a4, wl.y4, FP4["R"], FP4["C"], 32, 6.0),
+        "mxfp4_qdq": lambda: m.mxq_qdq_mxfp4(wl.a4, wl.y4, R4, C4, 32, 6.0),
+        "mxfp4_ste_fwd": lambda: m.mxq_mxfp4_ste_forward(wl.a4, wl.y4, m4, R4, C4, 32, 6.0),
+        "mxfp4_ste_bwd": lambda: m.mxq_mxfp4_ste_backward(wl.y4, m4, R4, C4, g4),
+        "linear_weight_quant": lambda: m.mxq_linear_quantize_weight(wl.w, N, K, wcache, wc_bytes),
+        "linear_layer": layer_plain,
+        "linear_wq": layer_wq,
+        "qat_linear_fwd_w4a4": lambda: m.mxq_qat_linear_fwd(wl.x, wl.w, None, M, N, K, 1, 6.0, wl.y, qat_ws,
+                                                            qat_ws_bytes),
     }
     out = {}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=wl.dev)
     for name, fn in parts.items():
         fn()
-        t = time_steps(fn, 5, 1) / 5 * 1e3
-        out[name + "_ms"] = round(t, 4)
+        out[name + "_ms"] = round(time_flushed(fn, 5, flush), 4)
     # derived throughputs
     out["linear_tflops"] = round(LIN_FLOP / ((out["linear_fwd_ms"] + out["linear_bwd_dx_ms"] + out["linear_bwd_dw_ms"])
                                              / 1e3) / 1e12, 1)
@@ -498,7 +540,11 @@ def component_timings(wl, world):
     tp = wl.t_pad
     gcol_bytes = T * Km * 2 + Km * tp * (1 + 1 / 32)
     out["moe_grouped_col_quant_X_gbs"] = round(gcol_bytes / (out["moe_grouped_col_quant_X_ms"] / 1e3) / 1e9, 1)
-    out["mxfp4_qdq_gbs"] = round(FP4["R"] * FP4["C"] * 8 / (out["mxfp4_qdq_ms"] / 1e3) / 1e9, 1)
+    out["mxfp4_qdq_gbs"] = round(R4 * C4 * 8 / (out["mxfp4_qdq_ms"] / 1e3) / 1e9, 1)
+    # clipped STE: 4 B in + 4 B out + 1/8 B of mask per element, both directions
+    out["mxfp4_ste_fwd_gbs"] = round(R4 * C4 * 8.125 / (out["mxfp4_ste_fwd_ms"] / 1e3) / 1e9, 1)
+    out["mxfp4_ste_bwd_gbs"] = round(R4 * C4 * 8.125 / (out["mxfp4_ste_bwd_ms"] / 1e3) / 1e9, 1)
+    out["qat_linear_fwd_w4a4_tflops"] = round(2 * M * N * K / (out["qat_linear_fwd_w4a4_ms"] / 1e3) / 1e12, 1)
     out["moe_fwd_tflops"] = round(2 * T * Nm * Km / (out["moe_fwd_ms"] / 1e3) / 1e12, 1)
     # the other linear mode on the same buffers
     other = m.RECOMPUTE if wl.mode == m.SAVE_QUANT else m.SAVE_QUANT
@@ -517,7 +563,7 @@ def component_timings(wl, world):
     out[f"linear_{name}_ms"] = round(t, 4)
     out["linear_saved_bytes"] = {"save": m.mxq_linear_saved_bytes(M, N, K, m.SAVE_QUANT),
                                  "recompute": m.mxq_linear_saved_bytes(M, N, K, m.RECOMPUTE)}
-    del ctx, ws, dq, ds, dqT, dsT
+    del ctx, ws, dq, ds, dqT, dsT, m4, g4, flush, qat_ws, wcache
     return out
 
 

@@ -139,6 +139,62 @@ mxq_status mxq_quantize_grouped_col(const void *x_bf16, int64_t rows, int64_t co
 mxq_status mxq_qdq_mxfp4(const float *x, float *y, int64_t rows, int64_t cols,
                          int block_size, float scale_factor, mxq_stream_t stream);
 
+/* MXFP4 quant-dequant of a bf16 tensor to bf16 ([AMCT] section 3.4: the
+ * result has the input's dtype): the same rule as mxq_qdq_mxfp4 on the
+ * exactly widened values; every result is exact in bf16 (a non-finite block
+ * gives NaN).  x, y bf16 [rows x cols], DEVICE, 16-byte aligned, y may equal
+ * x; cols % 32 == 0 (else MXQ_ERR_UNSUPPORTED). */
+mxq_status mxq_qdq_mxfp4_bf16(const void *x_bf16, void *y_bf16, int64_t rows, int64_t cols,
+                              int block_size, float scale_factor, mxq_stream_t stream);
+
+/* Forward of the clipped straight-through estimator ([AMCT] section 4.1,
+ * "STE and clipped STE"): y = MXFP4 quant-dequant of x exactly as
+ * mxq_qdq_mxfp4, and the saturation mask the backward needs.  An element is
+ * saturated when |x| > 6 * (its block's scale), i.e. when the codebook's top
+ * value clipped it.  sat_mask (DEVICE, uint32 [rows x ceil(cols/32)], written
+ * in full) holds one word per block: bit i of word (r, b) is element
+ * (r, 32b + i); bits past the end of a ragged row are 0; a block with a
+ * non-finite element has no saturated elements.  Arguments and errors as for
+ * mxq_qdq_mxfp4; sat_mask must be non-null and 4-byte aligned. */
+mxq_status mxq_mxfp4_ste_forward(const float *x, float *y, uint32_t *sat_mask, int64_t rows,
+                                 int64_t cols, int block_size, float scale_factor,
+                                 mxq_stream_t stream);
+
+/* Backward of the clipped straight-through estimator ([AMCT] section 4.1):
+ * grad_x = grad_y with every element whose sat_mask bit is set replaced by
+ * +0.0 and every other element copied bit for bit.  grad_y, grad_x fp32
+ * [rows x cols] (DEVICE, 4-byte aligned; grad_x may equal grad_y); sat_mask
+ * as written by mxq_mxfp4_ste_forward for the same shape.  The plain STE is
+ * the identity and needs no call. */
+mxq_status mxq_mxfp4_ste_backward(const float *grad_y, const uint32_t *sat_mask, int64_t rows,
+                                  int64_t cols, float *grad_x, mxq_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* MXFP4 quantization-aware training: linear-layer forward                */
+/* ------------------------------------------------------------------ */
+
+/* Workspace of mxq_qat_linear_fwd: W4A4 (quantize_input != 0) holds both
+ * quantized operands (codes + scales, each rounded up to 256 bytes); W4A16
+ * holds Q(w) in bf16. */
+size_t mxq_qat_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int quantize_input);
+
+/* Forward of the MXFP4 QAT linear layer ([AMCT] section 4.3):
+ * y = F.linear(Q(x), Q(w), bias) with Q the MXFP4 quant-dequant along K
+ * (blocks of 32, scale_factor as in mxq_qdq_mxfp4) and the bias not
+ * quantized.  x bf16 [M x K], w bf16 [N x K] (the layer's high-precision
+ * master weight, left unchanged), bias bf16 [N] or NULL, y bf16 [M x N]; all
+ * DEVICE, 16-byte aligned.  Q(x) and Q(w) are held exactly as E4M3 codes
+ * under the MXFP4 E8M0 scales, and the product is accumulated in fp32 on the
+ * block-scaled tensor cores; the bias is added in fp32 before the one
+ * rounding to bf16.  quantize_input = 0 (W4A16) leaves x unquantized: Q(w)
+ * is formed in bf16 (exact) and the product runs on the bf16 tensor cores.
+ * M, N, K positive multiples of 32; workspace >=
+ * mxq_qat_linear_workspace_bytes(M, N, K, quantize_input). */
+mxq_status mxq_qat_linear_fwd(const void *x_bf16, const void *w_bf16, const void *bias_bf16,
+                              int64_t M, int64_t N, int64_t K, int quantize_input,
+                              float scale_factor, void *y_bf16, void *workspace,
+                              size_t ws_bytes, mxq_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* Block-scaled MXFP8 GEMMs ([TT] MXFP8 mode; output in bf16, fp32 accumulate) */
 /* ------------------------------------------------------------------ */
@@ -204,6 +260,30 @@ mxq_status mxq_linear_bwd_dx(const void *dy, const void *w, int64_t M, int64_t N
 mxq_status mxq_linear_bwd_dw(const void *dy, const void *x, int64_t M, int64_t N, int64_t K,
                              mxq_mode mode, void *ctx, void *dw, void *workspace, size_t ws_bytes,
                              mxq_stream_t stream);
+
+/* ---- Quantized-weight reuse ([FB]: the reuse flags of the MXFP8 matmul
+ * path) ----
+ * Within one optimizer step W does not change, so its quantization can be
+ * made once and reused by every micro-batch's forward and input gradient:
+ * mxq_linear_quantize_weight reads W once and writes row(W) and colT(W)
+ * into a caller-owned cache (mxq_linear_weight_cache_bytes); the _wq entry
+ * points then take W's quantization from the cache instead of from W.
+ * Results are bitwise identical to mxq_linear_fwd / mxq_linear_bwd_dx (the
+ * quantization is deterministic); the cache is valid until W changes.
+ * `mode` then applies to X only (SAVE keeps colT(X) in ctx, RECOMPUTE
+ * re-quantizes it in mxq_linear_bwd_dw, which serves both paths).  ctx of
+ * the _wq path is mxq_linear_wq_ctx_bytes (no copy of colT(W)); workspace
+ * needs at most mxq_linear_workspace_bytes. */
+size_t mxq_linear_weight_cache_bytes(int64_t N, int64_t K);
+size_t mxq_linear_wq_ctx_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode);
+mxq_status mxq_linear_quantize_weight(const void *w, int64_t N, int64_t K, void *wcache,
+                                      size_t cache_bytes, mxq_stream_t stream);
+mxq_status mxq_linear_fwd_wq(const void *x, const void *wcache, int64_t M, int64_t N, int64_t K,
+                             mxq_mode mode, void *ctx, void *y, void *workspace, size_t ws_bytes,
+                             mxq_stream_t stream);
+mxq_status mxq_linear_bwd_dx_wq(const void *dy, const void *wcache, int64_t M, int64_t N, int64_t K,
+                                mxq_mode mode, void *ctx, void *dx, void *workspace,
+                                size_t ws_bytes, mxq_stream_t stream);
 
 /* ------------------------------------------------------------------ */
 /* Linear forward without caller-provided scratch                       */

@@ -27,6 +27,10 @@ __all__ = [
     "mxq_gemm", "mxq_grouped_gemm", "mxq_linear_ctx_bytes", "mxq_linear_saved_bytes",
     "mxq_linear_workspace_bytes", "mxq_linear_fwd", "mxq_linear_bwd_dx", "mxq_linear_bwd_dw",
     "mxq_last_error_string", "mxq_poll_device_error", "mxq_linear_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "mxq_mxfp4_ste_forward", "mxq_mxfp4_ste_backward", "mxfp4_ste_forward", "mxfp4_ste_backward",
+    "mxq_qat_linear_workspace_bytes", "mxq_qat_linear_fwd", "qat_linear_fwd", "mxq_qdq_mxfp4_bf16",
+    "mxq_linear_weight_cache_bytes", "mxq_linear_wq_ctx_bytes", "mxq_linear_quantize_weight", "mxq_linear_fwd_wq",
+    "mxq_linear_bwd_dx_wq",
 ]
 
 BF16, F32 = 0, 1
@@ -53,6 +57,11 @@ _SIGNATURES = {
     "mxq_quantize": (_I32, [_P, _I32, _I64, _I64, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "mxq_quantize_grouped_col": (_I32, [_P, _I64, _I64, _P, _I32, _I64, _P, _P, _P]),
     "mxq_qdq_mxfp4": (_I32, [_P, _P, _I64, _I64, _I32, _F32, _P]),
+    "mxq_qdq_mxfp4_bf16": (_I32, [_P, _P, _I64, _I64, _I32, _F32, _P]),
+    "mxq_mxfp4_ste_forward": (_I32, [_P, _P, _P, _I64, _I64, _I32, _F32, _P]),
+    "mxq_mxfp4_ste_backward": (_I32, [_P, _P, _I64, _I64, _P, _P]),
+    "mxq_qat_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
+    "mxq_qat_linear_fwd": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I32, _F32, _P, _P, _SZ, _P]),
     "mxq_gemm": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P]),
     "mxq_grouped_gemm": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I64, _P, _P]),
     "mxq_linear_ctx_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
@@ -62,6 +71,11 @@ _SIGNATURES = {
     "mxq_linear_bwd_dx": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
     "mxq_linear_bwd_dw": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
     "mxq_linear_fwd_noalloc": (_I32, [_P, _P, _I64, _I64, _I64, _P, _P]),
+    "mxq_linear_weight_cache_bytes": (_SZ, [_I64, _I64]),
+    "mxq_linear_wq_ctx_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
+    "mxq_linear_quantize_weight": (_I32, [_P, _I64, _I64, _P, _SZ, _P]),
+    "mxq_linear_fwd_wq": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
+    "mxq_linear_bwd_dx_wq": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
     "mxq_last_error_string": (ctypes.c_char_p, []),
     "mxq_poll_device_error": (_I32, [ctypes.POINTER(ctypes.c_uint32)]),
 }
@@ -134,6 +148,21 @@ def mxq_qdq_mxfp4(x, y, rows, cols, block_size=32, scale_factor=6.0, stream=None
     _check(load().mxq_qdq_mxfp4(_p(x), _p(y), rows, cols, block_size, scale_factor, _s(stream)), "mxq_qdq_mxfp4")
 
 
+def mxq_qdq_mxfp4_bf16(x, y, rows, cols, block_size=32, scale_factor=6.0, stream=None):
+    _check(load().mxq_qdq_mxfp4_bf16(_p(x), _p(y), rows, cols, block_size, scale_factor, _s(stream)),
+           "mxq_qdq_mxfp4_bf16")
+
+
+def mxq_mxfp4_ste_forward(x, y, sat_mask, rows, cols, block_size=32, scale_factor=6.0, stream=None):
+    _check(load().mxq_mxfp4_ste_forward(_p(x), _p(y), _p(sat_mask), rows, cols, block_size, scale_factor,
+                                        _s(stream)), "mxq_mxfp4_ste_forward")
+
+
+def mxq_mxfp4_ste_backward(grad_y, sat_mask, rows, cols, grad_x, stream=None):
+    _check(load().mxq_mxfp4_ste_backward(_p(grad_y), _p(sat_mask), rows, cols, _p(grad_x), _s(stream)),
+           "mxq_mxfp4_ste_backward")
+
+
 def mxq_gemm(a, sa, b, sb, M, N, K, c, ldc, stream=None):
     _check(load().mxq_gemm(_p(a), _p(sa), _p(b), _p(sb), M, N, K, _p(c), ldc, _s(stream)), "mxq_gemm")
 
@@ -168,6 +197,29 @@ def mxq_linear_bwd_dx(dy, w, M, N, K, mode, ctx, dx, workspace, ws_bytes, stream
 def mxq_linear_bwd_dw(dy, x, M, N, K, mode, ctx, dw, workspace, ws_bytes, stream=None):
     _check(load().mxq_linear_bwd_dw(_p(dy), _p(x), M, N, K, mode, _p(ctx), _p(dw), _p(workspace), ws_bytes,
                                     _s(stream)), "mxq_linear_bwd_dw")
+
+
+def mxq_linear_weight_cache_bytes(N, K) -> int:
+    return load().mxq_linear_weight_cache_bytes(N, K)
+
+
+def mxq_linear_wq_ctx_bytes(M, N, K, mode) -> int:
+    return load().mxq_linear_wq_ctx_bytes(M, N, K, mode)
+
+
+def mxq_linear_quantize_weight(w, N, K, wcache, cache_bytes, stream=None):
+    _check(load().mxq_linear_quantize_weight(_p(w), N, K, _p(wcache), cache_bytes, _s(stream)),
+           "mxq_linear_quantize_weight")
+
+
+def mxq_linear_fwd_wq(x, wcache, M, N, K, mode, ctx, y, workspace, ws_bytes, stream=None):
+    _check(load().mxq_linear_fwd_wq(_p(x), _p(wcache), M, N, K, mode, _p(ctx), _p(y), _p(workspace), ws_bytes,
+                                    _s(stream)), "mxq_linear_fwd_wq")
+
+
+def mxq_linear_bwd_dx_wq(dy, wcache, M, N, K, mode, ctx, dx, workspace, ws_bytes, stream=None):
+    _check(load().mxq_linear_bwd_dx_wq(_p(dy), _p(wcache), M, N, K, mode, _p(ctx), _p(dx), _p(workspace), ws_bytes,
+                                       _s(stream)), "mxq_linear_bwd_dx_wq")
 
 
 def mxq_linear_fwd_noalloc(x, w, M, N, K, y, stream=None):
@@ -221,11 +273,60 @@ def quantize_mxfp4(x: torch.Tensor, stream=None):
     return q, s
 
 
-def qdq_mxfp4(x: torch.Tensor, scale_factor: float = 6.0, stream=None) -> torch.Tensor:
-    """MXFP4 quant-dequant of a contiguous fp32 CUDA tensor (blocks along the last dim)."""
+def mxq_qat_linear_workspace_bytes(M, N, K, quantize_input=1):
+    return load().mxq_qat_linear_workspace_bytes(M, N, K, quantize_input)
+
+
+def mxq_qat_linear_fwd(x, w, bias, M, N, K, quantize_input, scale_factor, y, workspace, ws_bytes, stream=None):
+    _check(load().mxq_qat_linear_fwd(_p(x), _p(w), _p(bias), M, N, K, quantize_input, scale_factor, _p(y),
+                                     _p(workspace), ws_bytes, _s(stream)), "mxq_qat_linear_fwd")
+
+
+def qat_linear_fwd(x: torch.Tensor, w: torch.Tensor, bias=None, quantize_input: bool = True,
+                   scale_factor: float = 6.0, stream=None) -> torch.Tensor:
+    """MXFP4 QAT linear forward of contiguous bf16 CUDA tensors x [M x K],
+    w [N x K], bias [N] or None: returns bf16 [M x N]."""
+    M, K = x.shape
+    N = w.shape[0]
+    ws_bytes = mxq_qat_linear_workspace_bytes(M, N, K, int(quantize_input))
+    ws = _u8(ws_bytes, x.device)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    mxq_qat_linear_fwd(x, w, bias, M, N, K, int(quantize_input), scale_factor, y, ws, ws_bytes, stream)
+    return y
+
+
+def mxfp4_ste_forward(x: torch.Tensor, scale_factor: float = 6.0, stream=None):
+    """Clipped-STE forward of a contiguous fp32 CUDA tensor: returns (y, sat_mask)
+    with sat_mask int32 [rows x ceil(cols/32)] holding the packed mask words."""
     assert x.dtype == torch.float32 and x.is_contiguous()
     y = torch.empty_like(x)
     cols = x.shape[-1] if x.dim() else 1
     rows = x.numel() // cols if cols else 0
-    mxq_qdq_mxfp4(x, y, rows, cols, 32, scale_factor, stream)
+    m = torch.empty((rows, (cols + 31) // 32), dtype=torch.int32, device=x.device)
+    mxq_mxfp4_ste_forward(x, y, m, rows, cols, 32, scale_factor, stream)
+    return y, m
+
+
+def mxfp4_ste_backward(grad_y: torch.Tensor, sat_mask: torch.Tensor, stream=None) -> torch.Tensor:
+    """Clipped-STE backward: grad_y with the saturated elements set to +0.0."""
+    assert grad_y.dtype == torch.float32 and grad_y.is_contiguous() and sat_mask.is_contiguous()
+    gx = torch.empty_like(grad_y)
+    cols = grad_y.shape[-1] if grad_y.dim() else 1
+    rows = grad_y.numel() // cols if cols else 0
+    assert tuple(sat_mask.shape) == (rows, (cols + 31) // 32)
+    mxq_mxfp4_ste_backward(grad_y, sat_mask, rows, cols, gx, stream)
+    return gx
+
+
+def qdq_mxfp4(x: torch.Tensor, scale_factor: float = 6.0, stream=None) -> torch.Tensor:
+    """MXFP4 quant-dequant of a contiguous fp32 or bf16 CUDA tensor (blocks
+    along the last dim); the result has x's dtype."""
+    assert x.dtype in (torch.float32, torch.bfloat16) and x.is_contiguous()
+    y = torch.empty_like(x)
+    cols = x.shape[-1] if x.dim() else 1
+    rows = x.numel() // cols if cols else 0
+    if x.dtype == torch.bfloat16:
+        mxq_qdq_mxfp4_bf16(x, y, rows, cols, 32, scale_factor, stream)
+    else:
+        mxq_qdq_mxfp4(x, y, rows, cols, 32, scale_factor, stream)
     return y

@@ -79,24 +79,31 @@ inline Operand carve(uint8_t *&p, int64_t rows, int64_t k) {
 }
 
 mxq_status dense_gemm(const Operand &A, const Operand &B, int64_t M, int64_t N, int64_t K, void *c, int64_t ldc,
-                      cudaStream_t st) {
+                      cudaStream_t st, const void *bias = nullptr) {
     if (M == 0 || N == 0) return ok();
     mxq::GemmProblem g{};
     g.mode = mxq::kDense;
     g.a = A.q; g.sa = A.s; g.a_rows = M; g.a_k = K;
     g.b = B.q; g.sb = B.s; g.b_rows = N; g.b_k = K;
     g.c = c; g.M = M; g.N = N; g.ldc = ldc; g.K = K;
+    g.bias = bias;
     return cuda_result(mxq::launch_gemm(g, st), "mxq gemm launch");
 }
 
 // ---- linear-layer memory plan ----
-// ctx:  SAVE: [colT(X): K x M][colT(W): K x N][colT(dY): N x M];  RECOMPUTE: [colT(dY)]
+// ctx:  SAVE: [colT(X): K x M][colT(dY): N x M][colT(W): K x N];  RECOMPUTE: [colT(dY)]
+//       (the backward dW reads only the prefix [colT(X)][colT(dY)], which the
+//       cached-weight entry points share; they keep colT(W) in the cache)
 // ws :  fwd [row(X)][row(W)];  bwd_dx [row(dY)][colT(W) if RECOMPUTE];  bwd_dw [colT(X) if RECOMPUTE]
+// weight cache: [row(W): N x K][colT(W): K x N]
 size_t saved_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
     return mode == MXQ_SAVE_QUANT ? operand_bytes(K, M) + operand_bytes(K, N) : 0;
 }
 size_t ctx_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
     return saved_bytes(M, N, K, mode) + operand_bytes(N, M);
+}
+size_t wq_ctx_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
+    return (mode == MXQ_SAVE_QUANT ? operand_bytes(K, M) : 0) + operand_bytes(N, M);
 }
 size_t ws_fwd(int64_t M, int64_t N, int64_t K) { return operand_bytes(M, K) + operand_bytes(N, K); }
 size_t ws_dx(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
@@ -230,8 +237,61 @@ mxq_status mxq_qdq_mxfp4(const float *x, float *y, int64_t rows, int64_t cols, i
     if (rows > (1ll << 40) / (cols > 0 ? cols : 1)) return fail(MXQ_ERR_UNSUPPORTED, "tensor too large");
     mxq_status s = check_arch();
     if (s != MXQ_OK) return s;
-    return cuda_result(mxq::launch_qdq_mxfp4(x, y, rows, cols, scale_factor, reinterpret_cast<cudaStream_t>(stream)),
-                       "mxq_qdq_mxfp4 launch");
+    return cuda_result(
+        mxq::launch_qdq_mxfp4(x, y, nullptr, rows, cols, scale_factor, reinterpret_cast<cudaStream_t>(stream)),
+        "mxq_qdq_mxfp4 launch");
+}
+
+mxq_status mxq_qdq_mxfp4_bf16(const void *x, void *y, int64_t rows, int64_t cols, int block_size, float scale_factor,
+                              mxq_stream_t stream) {
+    if (block_size != 32) return fail(MXQ_ERR_UNSUPPORTED, "block_size must be 32 (got %d)", block_size);
+    if (!(scale_factor > 0.0f) || !(scale_factor <= 3.402823466e38f))
+        return fail(MXQ_ERR_INVALID_ARG, "scale_factor must be finite and > 0");
+    if (rows < 0 || cols < 0) return fail(MXQ_ERR_INVALID_ARG, "negative size");
+    if (rows == 0 || cols == 0) return ok();
+    if (!x || !y || !al16(x) || !al16(y)) return fail(MXQ_ERR_INVALID_ARG, "x and y must be 16-byte aligned bf16 pointers");
+    if (cols % 32) return fail(MXQ_ERR_UNSUPPORTED, "bf16 quant-dequant needs cols %% 32 == 0 (got %lld)", (long long)cols);
+    if (rows > (1ll << 40) / cols) return fail(MXQ_ERR_UNSUPPORTED, "tensor too large");
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    return cuda_result(mxq::launch_qdq_mxfp4_bf16(static_cast<const uint16_t *>(x), static_cast<uint16_t *>(y), rows,
+                                                  cols, scale_factor, reinterpret_cast<cudaStream_t>(stream)),
+                       "mxq_qdq_mxfp4_bf16 launch");
+}
+
+mxq_status mxq_mxfp4_ste_forward(const float *x, float *y, uint32_t *sat_mask, int64_t rows, int64_t cols,
+                                 int block_size, float scale_factor, mxq_stream_t stream) {
+    if (block_size != 32) return fail(MXQ_ERR_UNSUPPORTED, "block_size must be 32 (got %d)", block_size);
+    if (!(scale_factor > 0.0f) || !(scale_factor <= 3.402823466e38f))
+        return fail(MXQ_ERR_INVALID_ARG, "scale_factor must be finite and > 0");
+    if (rows < 0 || cols < 0) return fail(MXQ_ERR_INVALID_ARG, "negative size");
+    if (rows == 0 || cols == 0) return ok();
+    if (!x || !y || (reinterpret_cast<uintptr_t>(x) & 3) || (reinterpret_cast<uintptr_t>(y) & 3))
+        return fail(MXQ_ERR_INVALID_ARG, "x and y must be non-null fp32 pointers");
+    if (!sat_mask || (reinterpret_cast<uintptr_t>(sat_mask) & 3))
+        return fail(MXQ_ERR_INVALID_ARG, "sat_mask must be a non-null uint32 pointer");
+    if (rows > (1ll << 40) / cols) return fail(MXQ_ERR_UNSUPPORTED, "tensor too large");
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    return cuda_result(
+        mxq::launch_qdq_mxfp4(x, y, sat_mask, rows, cols, scale_factor, reinterpret_cast<cudaStream_t>(stream)),
+        "mxq_mxfp4_ste_forward launch");
+}
+
+mxq_status mxq_mxfp4_ste_backward(const float *grad_y, const uint32_t *sat_mask, int64_t rows, int64_t cols,
+                                  float *grad_x, mxq_stream_t stream) {
+    if (rows < 0 || cols < 0) return fail(MXQ_ERR_INVALID_ARG, "negative size");
+    if (rows == 0 || cols == 0) return ok();
+    if (!grad_y || !grad_x || (reinterpret_cast<uintptr_t>(grad_y) & 3) || (reinterpret_cast<uintptr_t>(grad_x) & 3))
+        return fail(MXQ_ERR_INVALID_ARG, "grad_y and grad_x must be non-null fp32 pointers");
+    if (!sat_mask || (reinterpret_cast<uintptr_t>(sat_mask) & 3))
+        return fail(MXQ_ERR_INVALID_ARG, "sat_mask must be a non-null uint32 pointer");
+    if (rows > (1ll << 40) / cols) return fail(MXQ_ERR_UNSUPPORTED, "tensor too large");
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    return cuda_result(
+        mxq::launch_ste_backward(grad_y, sat_mask, grad_x, rows, cols, reinterpret_cast<cudaStream_t>(stream)),
+        "mxq_mxfp4_ste_backward launch");
 }
 
 mxq_status mxq_gemm(const uint8_t *a, const uint8_t *sa, const uint8_t *b, const uint8_t *sb, int64_t M, int64_t N,
@@ -325,7 +385,9 @@ mxq_status mxq_linear_fwd(const void *x, const void *w, int64_t M, int64_t N, in
     cudaError_t e;
     if (mode == MXQ_SAVE_QUANT) {
         uint8_t *cp = static_cast<uint8_t *>(ctx);
-        const Operand xT = carve(cp, K, M), wT = carve(cp, K, N);
+        const Operand xT = carve(cp, K, M);
+        (void)carve(cp, N, M);  // colT(dY), written by bwd_dx
+        const Operand wT = carve(cp, K, N);
         e = mxq::launch_quant_cols(static_cast<const uint16_t *>(x), M, K, K, xq.q, xq.s, xT.q, xT.s, st);
         if (e == cudaSuccess)
             e = mxq::launch_quant_cols(static_cast<const uint16_t *>(w), N, K, K, wq.q, wq.s, wT.q, wT.s, st);
@@ -344,12 +406,10 @@ mxq_status mxq_linear_bwd_dx(const void *dy, const void *w, int64_t M, int64_t N
     if ((s = check_arch()) != MXQ_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *cp = static_cast<uint8_t *>(ctx);
-    Operand wT{};
-    if (mode == MXQ_SAVE_QUANT) {
-        (void)carve(cp, K, M);
-        wT = carve(cp, K, N);
-    }
+    if (mode == MXQ_SAVE_QUANT) (void)carve(cp, K, M);
     const Operand dyT = carve(cp, N, M);
+    Operand wT{};
+    if (mode == MXQ_SAVE_QUANT) wT = carve(cp, K, N);
     uint8_t *wp = static_cast<uint8_t *>(workspace);
     const Operand dyq = carve(wp, M, N);
     cudaError_t e = mxq::launch_quant_cols(static_cast<const uint16_t *>(dy), M, N, N, dyq.q, dyq.s, dyT.q, dyT.s, st);
@@ -369,10 +429,7 @@ mxq_status mxq_linear_bwd_dw(const void *dy, const void *x, int64_t M, int64_t N
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *cp = static_cast<uint8_t *>(ctx);
     Operand xT{};
-    if (mode == MXQ_SAVE_QUANT) {
-        xT = carve(cp, K, M);
-        (void)carve(cp, K, N);
-    }
+    if (mode == MXQ_SAVE_QUANT) xT = carve(cp, K, M);
     const Operand dyT = carve(cp, N, M);
     if (mode == MXQ_RECOMPUTE) {
         uint8_t *wp = static_cast<uint8_t *>(workspace);
@@ -381,6 +438,127 @@ mxq_status mxq_linear_bwd_dw(const void *dy, const void *x, int64_t M, int64_t N
         if (e != cudaSuccess) return cuda_result(e, "mxq_linear_bwd_dw quant launch");
     }
     return dense_gemm(dyT, xT, N, K, M, dw, K, st);
+}
+
+size_t mxq_linear_weight_cache_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0) return 0;
+    return operand_bytes(N, K) + operand_bytes(K, N);
+}
+size_t mxq_linear_wq_ctx_bytes(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return wq_ctx_bytes(M, N, K, mode);
+}
+
+mxq_status mxq_linear_quantize_weight(const void *w, int64_t N, int64_t K, void *wcache, size_t cache_bytes,
+                                      mxq_stream_t stream) {
+    if (!w || !wcache) return fail(MXQ_ERR_INVALID_ARG, "null tensor pointer");
+    if (!al16(w) || !al16(wcache)) return fail(MXQ_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (N <= 0 || K <= 0 || N % 32 || K % 32)
+        return fail(MXQ_ERR_INVALID_ARG, "N, K must be positive multiples of 32 (got %lld, %lld)", (long long)N,
+                    (long long)K);
+    if (N > (1ll << 31) || K > (1ll << 31)) return fail(MXQ_ERR_UNSUPPORTED, "dimension above 2^31");
+    if (cache_bytes < mxq_linear_weight_cache_bytes(N, K))
+        return fail(MXQ_ERR_INVALID_ARG, "weight cache too small: need %zu bytes, got %zu",
+                    mxq_linear_weight_cache_bytes(N, K), cache_bytes);
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    uint8_t *cp = static_cast<uint8_t *>(wcache);
+    const Operand wq = carve(cp, N, K), wT = carve(cp, K, N);
+    return cuda_result(mxq::launch_quant_cols(static_cast<const uint16_t *>(w), N, K, K, wq.q, wq.s, wT.q, wT.s,
+                                              reinterpret_cast<cudaStream_t>(stream)),
+                       "mxq_linear_quantize_weight launch");
+}
+
+mxq_status mxq_linear_fwd_wq(const void *x, const void *wcache, int64_t M, int64_t N, int64_t K, mxq_mode mode,
+                             void *ctx, void *y, void *workspace, size_t ws_bytes, mxq_stream_t stream) {
+    mxq_status s = check_linear(x, wcache, M, N, K, mode, ctx, y, workspace, ws_bytes, operand_bytes(M, K));
+    if (s != MXQ_OK) return s;
+    if ((s = check_arch()) != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    const Operand xq = carve(wp, M, K);
+    uint8_t *cc = static_cast<uint8_t *>(const_cast<void *>(wcache));
+    const Operand wq = carve(cc, N, K);
+    cudaError_t e;
+    if (mode == MXQ_SAVE_QUANT) {
+        uint8_t *cp = static_cast<uint8_t *>(ctx);
+        const Operand xT = carve(cp, K, M);
+        e = mxq::launch_quant_cols(static_cast<const uint16_t *>(x), M, K, K, xq.q, xq.s, xT.q, xT.s, st);
+    } else {
+        e = mxq::launch_quant_rows(x, false, 0, M, K, K, xq.q, xq.s, st);
+    }
+    if (e != cudaSuccess) return cuda_result(e, "mxq_linear_fwd_wq quant launch");
+    return dense_gemm(xq, wq, M, N, K, y, N, st);
+}
+
+mxq_status mxq_linear_bwd_dx_wq(const void *dy, const void *wcache, int64_t M, int64_t N, int64_t K, mxq_mode mode,
+                                void *ctx, void *dx, void *workspace, size_t ws_bytes, mxq_stream_t stream) {
+    mxq_status s = check_linear(dy, wcache, M, N, K, mode, ctx, dx, workspace, ws_bytes, operand_bytes(M, N));
+    if (s != MXQ_OK) return s;
+    if ((s = check_arch()) != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *cp = static_cast<uint8_t *>(ctx);
+    if (mode == MXQ_SAVE_QUANT) (void)carve(cp, K, M);
+    const Operand dyT = carve(cp, N, M);
+    uint8_t *cc = static_cast<uint8_t *>(const_cast<void *>(wcache));
+    (void)carve(cc, N, K);
+    const Operand wT = carve(cc, K, N);
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    const Operand dyq = carve(wp, M, N);
+    cudaError_t e = mxq::launch_quant_cols(static_cast<const uint16_t *>(dy), M, N, N, dyq.q, dyq.s, dyT.q, dyT.s, st);
+    if (e != cudaSuccess) return cuda_result(e, "mxq_linear_bwd_dx_wq quant launch");
+    return dense_gemm(dyq, wT, M, K, N, dx, K, st);
+}
+
+size_t mxq_qat_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int quantize_input) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    // W4A4: both operands as E4M3 codes + scales; W4A16: Q(W) in bf16
+    return quantize_input ? operand_bytes(M, K) + operand_bytes(N, K)
+                          : round256(2 * static_cast<size_t>(N) * static_cast<size_t>(K));
+}
+
+mxq_status mxq_qat_linear_fwd(const void *x, const void *w, const void *bias, int64_t M, int64_t N, int64_t K,
+                              int quantize_input, float scale_factor, void *y, void *workspace, size_t ws_bytes,
+                              mxq_stream_t stream) {
+    if (!x || !w || !y) return fail(MXQ_ERR_INVALID_ARG, "null tensor pointer");
+    if (!al16(x) || !al16(w) || !al16(y) || (bias && !al16(bias)) || (workspace && !al16(workspace)))
+        return fail(MXQ_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (!(scale_factor > 0.0f) || !(scale_factor <= 3.402823466e38f))
+        return fail(MXQ_ERR_INVALID_ARG, "scale_factor must be finite and > 0");
+    if (M <= 0 || N <= 0 || K <= 0 || M % 32 || N % 32 || K % 32)
+        return fail(MXQ_ERR_INVALID_ARG, "M, N, K must be positive multiples of 32 (got %lld, %lld, %lld)",
+                    (long long)M, (long long)N, (long long)K);
+    if (M > (1ll << 31) || N > (1ll << 31) || K > (1ll << 31))
+        return fail(MXQ_ERR_UNSUPPORTED, "dimension above 2^31");
+    const size_t need = mxq_qat_linear_workspace_bytes(M, N, K, quantize_input);
+    if (!workspace || ws_bytes < need)
+        return fail(MXQ_ERR_INVALID_ARG, "workspace too small: need %zu bytes, got %zu", need,
+                    workspace ? ws_bytes : 0);
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    if (!quantize_input) {
+        // W4A16: Q(W) in bf16 (exact), then the bf16 tensor-core product with x
+        uint16_t *qw = reinterpret_cast<uint16_t *>(wp);
+        cudaError_t e = mxq::launch_qdq_mxfp4_bf16(static_cast<const uint16_t *>(w), qw, N, K, scale_factor, st);
+        if (e != cudaSuccess) return cuda_result(e, "mxq_qat_linear_fwd quant launch");
+        mxq::GemmProblem g{};
+        g.mode = mxq::kDense;
+        g.kind = mxq::kBF16;
+        g.a = static_cast<const uint8_t *>(x); g.a_rows = M; g.a_k = K;
+        g.b = reinterpret_cast<const uint8_t *>(qw); g.b_rows = N; g.b_k = K;
+        g.c = y; g.M = M; g.N = N; g.ldc = N; g.K = K;
+        g.bias = bias;
+        return cuda_result(mxq::launch_gemm(g, st), "mxq_qat_linear_fwd gemm launch");
+    }
+    const Operand xq = carve(wp, M, K), wq = carve(wp, N, K);
+    // MXFP4 quant-dequant of both operands, held exactly as E4M3 codes under
+    // the MXFP4 E8M0 scales, then the block-scaled product plus bias
+    cudaError_t e = mxq::launch_quant_rows(x, false, 2, M, K, K, xq.q, xq.s, st, scale_factor);
+    if (e == cudaSuccess) e = mxq::launch_quant_rows(w, false, 2, N, K, K, wq.q, wq.s, st, scale_factor);
+    if (e != cudaSuccess) return cuda_result(e, "mxq_qat_linear_fwd quant launch");
+    return dense_gemm(xq, wq, M, N, K, y, N, st, bias);
 }
 
 }  // extern "C"

@@ -25,8 +25,10 @@
 //              the stage (in both CTAs of a pair);
 //   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane
 //              sub-partition each) into registers as bf16 (RNE), release of the
-//              accumulator to the MMA warp, then 16-byte global stores that
-//              overlap the next tile's mainloop.
+//              accumulator to the MMA warp, then stores that overlap the next
+//              tile's mainloop: 32 x 32 blocks staged in shared memory and
+//              written by TMA (cp.async.bulk.tensor), or, for a warp whose 32
+//              rows straddle an expert boundary, masked 16-byte row stores.
 // CG = 2 pairs two SMs on one 256 x 256 tile: each CTA loads 128 rows of A and
 // 128 of the 256 rows of B (32 KB per stage, 6 stages), so per SM the operand
 // traffic and the shared memory per stage are two thirds of CG = 1's, and the
@@ -91,7 +93,8 @@ struct Params {
     int64_t b_row_per_expert, b_k_per_expert, c_expert_stride;
     int m_tiles, n_tiles;  // tile counts (m in units of 128 * CG rows)
     int n_fastest;         // kDense tile order: 1 = n fastest (A is the larger operand)
-    int tma_store;         // epilogue stores whole 32 x 32 blocks with TMA (no row masking needed)
+    int tma_store;         // an output tensor map exists: unmasked 32-row boxes are stored with TMA
+    const __nv_bfloat16 *bias;  // kDense: bf16 [N] added to every row in fp32, or null
     int64_t total_tiles;   // tile index space (an upper bound for grouped rows)
 };
 
@@ -102,12 +105,43 @@ struct TileInfo {
     int64_t row_lo, row_hi, out_row0, col0, col_hi, c_off;
 };
 
-// Instruction descriptor, kind::mxf8f6f4: E4M3 x E4M3, both K-major, N = 256,
-// M = 128 * CG, E8M0 scales, scale-factor byte `j` of the A and B scale columns.
-template <int CG>
+// Instruction descriptors, both operands K-major, N = 256, M = 128 * CG.
+// kMXF8 (kind::mxf8f6f4): E4M3 x E4M3, E8M0 scales, scale-factor byte `j` of
+// the A and B scale columns.  kBF16 (kind::f16): bf16 x bf16, fp32 accumulator.
+template <int CG, int KIND>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t j) {
-    return (j << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
-           (static_cast<uint32_t>(Cfg<CG>::TILE_M >> 4) << 24) | (j << 29);
+    if constexpr (KIND == kBF16) {
+        return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+               (static_cast<uint32_t>(Cfg<CG>::TILE_M >> 4) << 24);
+    } else {
+        return (j << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+               (static_cast<uint32_t>(Cfg<CG>::TILE_M >> 4) << 24) | (j << 29);
+    }
+}
+
+// acc[i] += bias[col + i] (fp32) for the columns below col_hi; every lane
+// reads the same bias words (a broadcast).
+__device__ __forceinline__ void add_bias32(uint32_t (&acc)[32], const __nv_bfloat16 *bias, int64_t col,
+                                           int64_t col_hi) {
+    const uint16_t *b = reinterpret_cast<const uint16_t *>(bias) + col;
+    if (col + 32 <= col_hi) {
+#pragma unroll
+        for (int v = 0; v < 4; v++) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4 *>(b) + v);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                acc[8 * v + 2 * j] = __float_as_uint(__uint_as_float(acc[8 * v + 2 * j]) + __uint_as_float(ws[j] << 16));
+                acc[8 * v + 2 * j + 1] =
+                    __float_as_uint(__uint_as_float(acc[8 * v + 2 * j + 1]) + __uint_as_float(ws[j] & 0xFFFF0000u));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; i++)
+            if (col + i < col_hi)
+                acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __uint_as_float(static_cast<uint32_t>(__ldg(b + i)) << 16));
+    }
 }
 
 // Work decomposition: which tile this CTA computes (run by all lanes of a warp).
@@ -295,13 +329,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // non-blocking test of the NEXT stage's barrier issued first and its result
 // read last, so the barrier check's latency overlaps the MMA issue instead of
 // adding to it.  Returns whether the next stage's data has landed.
-template <int CG>
+template <int CG, int KIND>
 __device__ __forceinline__ bool mma4_commit_peek(uint32_t d_tmem, const uint64_t (&ad)[4], const uint64_t (&bd)[4],
                                                  const uint32_t (&id)[4], uint32_t sfa, uint32_t sfb,
                                                  uint32_t accumulate, uint32_t bar_empty_s, uint32_t bar_full_next,
                                                  uint32_t parity_next) {
     uint32_t ready;
-    if constexpr (CG == 2) {
+    if constexpr (KIND == kBF16) {
+        static_assert(CG == 1, "bf16 tiles are single-CTA");
+        asm volatile(
+            "{\n\t.reg .pred pn, pa, p1;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n\t"
+            "setp.ne.b32 pa, %3, 0;\n\t"
+            "setp.eq.u32 p1, 0, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%4], %5, %6, %7, pa;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%4], %8, %9, %7, p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%4], %10, %11, %7, p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%4], %12, %13, %7, p1;\n\t"
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%14];\n\t"
+            "selp.u32 %0, 1, 0, pn;\n\t}"
+            : "=r"(ready)
+            : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "l"(ad[0]), "l"(bd[0]), "r"(id[0]),
+              "l"(ad[1]), "l"(bd[1]), "l"(ad[2]), "l"(bd[2]), "l"(ad[3]), "l"(bd[3]), "r"(bar_empty_s)
+            : "memory");
+        (void)sfa;
+        (void)sfb;
+    } else if constexpr (CG == 2) {
         asm volatile(
             "{\n\t.reg .pred pn, pa, p1;\n\t"
             "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n\t"
@@ -339,9 +392,9 @@ __device__ __forceinline__ bool mma4_commit_peek(uint32_t d_tmem, const uint64_t
     return ready != 0;
 }
 
-template <int CG>
+template <int CG, int KIND, bool BIAS>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_gemm_mxf8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                 const __grid_constant__ CUtensorMap tmC, const Params p) {
     using C = Cfg<CG>;
@@ -432,7 +485,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t sfa_s = sbase + C::OFF_SFA + s * C::SFA_BYTES;
                     const uint32_t sfb_s = sbase + C::OFF_SFB + s * C::SFB_BYTES;
                     const int ka = static_cast<int>(ti.a_k0 + kb * BK), kb_ = static_cast<int>(ti.b_k0 + kb * BK);
-                    if constexpr (CG == 1) {
+                    if constexpr (KIND == kBF16) {
+                        const uint32_t fb = bar_full + 8 * s;
+                        mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+                        tma_load_2d(sa_s, &tmA, fb, ka, static_cast<int>(ti.a_row0));
+                        tma_load_2d(sb_s, &tmB, fb, kb_, static_cast<int>(ti.b_row0));
+                        (void)sfa_s;
+                        (void)sfb_s;
+                    } else if constexpr (CG == 1) {
                         const uint32_t fb = bar_full + 8 * s;
                         mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + C::SFA_BYTES + 512u * ti.b_atoms);
                         tma_load_2d(sa_s, &tmA, fb, ka, static_cast<int>(ti.a_row0));
@@ -492,7 +552,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint64_t dA = smem_desc(sbase + C::OFF_SFA + s * C::SFA_BYTES, 0, 128, 0);
                         const uint64_t dB0 = smem_desc(sbase + C::OFF_SFB + s * C::SFB_BYTES, 0, 128, 0);
                         const uint64_t dB1 = smem_desc(sbase + C::OFF_SFB + s * C::SFB_BYTES + 512, 0, 128, 0);
-                        if constexpr (CG == 2) {
+                        if constexpr (KIND == kBF16) {
+                            (void)dA;  // no scales
+                            (void)dB0;
+                            (void)dB1;
+                        } else if constexpr (CG == 2) {
                             tc_cp_32x128b_warpx4_pair(sfa_t, dA);
                             tc_cp_32x128b_warpx4_pair(sfb_t, dB0);
                             tc_cp_32x128b_warpx4_pair(sfb_t + 4, dB1);
@@ -510,10 +574,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                             for (int j = 0; j < 4; j++) {
                                 ad[j] = smem_desc(sbase + C::OFF_A + s * C::A_BYTES + 32 * j, 0, 1024, 2);
                                 bd[j] = smem_desc(sbase + C::OFF_B + s * C::B_BYTES + 32 * j, 0, 1024, 2);
-                                id[j] = make_idesc<CG>(j);
+                                id[j] = make_idesc<CG, KIND>(j);
                             }
                             const uint32_t s1 = (g + 1) % STAGES, ph1 = ((g + 1) / STAGES) & 1;
-                            ready = mma4_commit_peek<CG>(tmem, ad, bd, id, sfa_t, sfb_t, kb != 0 ? 1u : 0u,
+                            ready = mma4_commit_peek<CG, KIND>(tmem, ad, bd, id, sfa_t, sfb_t, kb != 0 ? 1u : 0u,
                                                          bar_empty + 8 * s, bar_full + 8 * s1, ph1);
                             continue;
                         }
@@ -521,10 +585,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const uint64_t ad = smem_desc(sbase + C::OFF_A + s * C::A_BYTES + 32 * j, 0, 1024, 2);
                             const uint64_t bd = smem_desc(sbase + C::OFF_B + s * C::B_BYTES + 32 * j, 0, 1024, 2);
                             const uint32_t acc = (kb | j) != 0 ? 1u : 0u;
-                            if constexpr (CG == 2)
-                                tc_mma_mxf8_pair(tmem, ad, bd, make_idesc<CG>(j), sfa_t, sfb_t, acc);
+                            if constexpr (KIND == kBF16)
+                                tc_mma_bf16(tmem, ad, bd, make_idesc<CG, KIND>(j), acc);
+                            else if constexpr (CG == 2)
+                                tc_mma_mxf8_pair(tmem, ad, bd, make_idesc<CG, KIND>(j), sfa_t, sfb_t, acc);
                             else
-                                tc_mma_mxf8(tmem, ad, bd, make_idesc<CG>(j), sfa_t, sfb_t, acc);
+                                tc_mma_mxf8(tmem, ad, bd, make_idesc<CG, KIND>(j), sfa_t, sfb_t, acc);
                         }
                         if constexpr (CG == 2) tc_commit_pair_mc(bar_empty + 8 * s, 3);
                         else tc_commit(bar_empty + 8 * s);
@@ -584,6 +650,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int q = 0; q < 2; q++) {
                     const int ch = 2 * h + q;
                     if (ti.col0 + 32 * ch < ti.col_hi) {
+                        if constexpr (BIAS) add_bias32(r[q], p.bias, ti.col0 + 32 * ch, ti.col_hi);
 #pragma unroll
                         for (int i = 0; i < 16; i++)
                             pk[16 * ch + i] =
@@ -598,11 +665,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 else mbar_arrive(bar_acce);
             }
             acc_it++;
-            if (p.tma_store) {
+            // TMA stores take whole 32-row boxes: this warp's rows must all belong
+            // to the tile's output (always for dense problems, where the tensor
+            // map clips rows past M; grouped tiles mask rows of other experts).
+            const int64_t wrow0 = ti.out_row0 + 32 * sub;
+            if (p.tma_store && (p.mode == kDense || (wrow0 >= ti.row_lo && wrow0 + 32 <= ti.row_hi))) {
                 // Stage each 32 x 32 block in a 64-byte-swizzled slot (conflict-free
-                // 16-byte writes) and store it with TMA; rows and columns outside the
-                // output are clipped by the tensor map.
-                const int64_t trow = ti.c_off / p.ldc + ti.out_row0 + 32 * sub;
+                // 16-byte writes) and store it with TMA; columns past N are clipped
+                // by the tensor map.
+                const int64_t trow = ti.c_off / p.ldc + wrow0;
 #pragma unroll
                 for (int ch = 0; ch < BN / 32; ch++) {
                     const int64_t col = ti.col0 + 32 * ch;
@@ -734,18 +805,19 @@ int cta_group_for(const GemmProblem &) {
     return forced == 2 ? 2 : 1;
 }
 
-template <int CG>
+template <int CG, int KIND, bool BIAS>
 cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     using C = Cfg<CG>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(k_gemm_mxf8<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        attr_err = cudaFuncSetAttribute(k_gemm<CG, KIND, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
     CUtensorMap tmA, tmB, tmSA, tmSB, tmC;
-    if (!make_tmap(&tmA, g.a, g.a_rows, g.a_k, C::BM) || !make_tmap(&tmB, g.b, g.b_rows, g.b_k, C::B_ROWS))
+    const int64_t esz = KIND == kBF16 ? 2 : 1;  // operand bytes per element (tensor maps run over bytes)
+    if (!make_tmap(&tmA, g.a, g.a_rows, esz * g.a_k, C::BM) || !make_tmap(&tmB, g.b, g.b_rows, esz * g.b_k, C::B_ROWS))
         return cudaErrorInvalidValue;
     if (CG == 2) {
         if (!make_scale_tmap(&tmSA, g.sa, scale_bytes_of(g.a_rows, g.a_k)) ||
@@ -756,12 +828,12 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         tmSB = tmB;
     }
     p.m_tiles = static_cast<int>((g.M + C::TILE_M - 1) / C::TILE_M);
-    // TMA stores need whole tiles to belong to one output: always for dense
-    // problems, for the grouped weight gradient when each expert's rows fill
-    // whole 128-row tiles; the grouped forward / input gradient mask rows.
+    // output tensor map for the epilogue's TMA stores (all experts' outputs
+    // stacked for the grouped weight gradient); without one (ldc not a
+    // multiple of 8, or rows past the 32-bit TMA coordinate range) every
+    // store is a plain global store
     const int64_t c_rows = g.mode == kGroupedK ? static_cast<int64_t>(g.E) * g.M : g.M;
-    p.tma_store = (g.mode == kDense || (g.mode == kGroupedK && g.M % C::TILE_M == 0)) && c_rows < (1ll << 31) &&
-                  make_out_tmap(&tmC, g.c, c_rows, g.N, g.ldc) ? 1 : 0;
+    p.tma_store = c_rows < (1ll << 31) && make_out_tmap(&tmC, g.c, c_rows, g.N, g.ldc) ? 1 : 0;
     if (!p.tma_store) tmC = tmA;  // unused
     if (g.mode == kDense) p.total_tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     else if (g.mode == kGroupedRows) p.total_tiles = ((g.T + C::TILE_M - 1) / C::TILE_M + g.E) * p.n_tiles;
@@ -792,7 +864,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         if (CG == 2) {
             cfg.gridDim = dim3(2);
             int clusters = 0;
-            e = cudaOccupancyMaxActiveClusters(&clusters, k_gemm_mxf8<CG>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&clusters, k_gemm<CG, KIND, BIAS>, &cfg);
             if (e != cudaSuccess) return e;
             resident[dev] = clusters > 0 ? clusters : 1;
         } else {
@@ -802,7 +874,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     }
     const int64_t units = p.total_tiles < resident[dev] ? p.total_tiles : resident[dev];
     cfg.gridDim = dim3(static_cast<unsigned>(units * CG));
-    return cudaLaunchKernelEx(&cfg, k_gemm_mxf8<CG>, tmA, tmB, tmSA, tmSB, tmC, p);
+    return cudaLaunchKernelEx(&cfg, k_gemm<CG, KIND, BIAS>, tmA, tmB, tmSA, tmSB, tmC, p);
 }
 
 }  // namespace
@@ -822,14 +894,23 @@ cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
     p.sb_kt = (g.b_k / 32 + 3) / 4;
     p.b_row_atoms = (g.b_rows + 127) / 128;
     p.c = static_cast<__nv_bfloat16 *>(g.c);
-    p.M = g.M; p.N = g.N; p.ldc = g.ldc; p.K = g.K;
+    p.M = g.M; p.N = g.N; p.ldc = g.ldc;
+    p.K = g.kind == kBF16 ? 2 * g.K : g.K;  // the mainloop counts contraction bytes
     p.offsets = g.offsets; p.E = g.E;
     p.b_row_per_expert = g.b_row_per_expert;
     p.b_k_per_expert = g.b_k_per_expert;
     p.c_expert_stride = g.c_expert_stride;
+    p.bias = g.mode == kDense ? static_cast<const __nv_bfloat16 *>(g.bias) : nullptr;
     p.n_tiles = static_cast<int>((g.N + BN - 1) / BN);
     p.n_fastest = g.mode == kDense && g.a_rows > g.b_rows ? 1 : 0;
-    return cta_group_for(g) == 2 ? launch_cg<2>(g, p, st) : launch_cg<1>(g, p, st);
+    // bias (dense only) is a separate instance: a per-chunk test in the
+    // epilogue measurably slows the launches that have none
+    if (g.kind == kBF16) {
+        if (g.mode != kDense) return cudaErrorInvalidValue;
+        return p.bias ? launch_cg<1, kBF16, true>(g, p, st) : launch_cg<1, kBF16, false>(g, p, st);
+    }
+    if (p.bias) return launch_cg<1, kMXF8, true>(g, p, st);
+    return cta_group_for(g) == 2 ? launch_cg<2, kMXF8, false>(g, p, st) : launch_cg<1, kMXF8, false>(g, p, st);
 }
 
 }  // namespace mxq

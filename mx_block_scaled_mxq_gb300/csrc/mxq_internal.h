@@ -8,21 +8,32 @@
 namespace mxq {
 
 // ---- quantization (mxq_quant.cu) ----
-// fmt 0: MXFP8 (bf16 in), fmt 1: MXFP4 packed (bf16 or fp32 in).  cols % 32 == 0.
+// cols % 32 == 0.  fmt 0: MXFP8 E4M3 codes (bf16 in); 1: packed MXFP4 nibbles; 2: MXFP4 values as E4M3
+// codes (bf16 in).  fmt 1 takes bf16 or fp32 in.  sf: the MXFP4 scale factor.
 cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, int64_t C, int64_t ldx,
-                              uint8_t *q, uint8_t *s, cudaStream_t st);
+                              uint8_t *q, uint8_t *s, cudaStream_t st, float sf = 6.0f);
 // Column MXFP8 quant of bf16 x; q_row/s_row non-null adds the row quant (dual).
 cudaError_t launch_quant_cols(const uint16_t *x, int64_t R, int64_t C, int64_t ldx, uint8_t *q_row,
                               uint8_t *s_row, uint8_t *qT, uint8_t *sT, cudaStream_t st);
 cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, const int64_t *d_off, int E,
                                       int64_t t_pad, uint8_t *qT, uint8_t *sT, cudaStream_t st);
-cudaError_t launch_qdq_mxfp4(const float *x, float *y, int64_t rows, int64_t cols, float sf, cudaStream_t st);
+cudaError_t launch_qdq_mxfp4(const float *x, float *y, uint32_t *mask, int64_t rows, int64_t cols, float sf,
+                             cudaStream_t st);
+// MXFP4 quant-dequant bf16 -> bf16, blocks of 32 along rows; cols % 32 == 0, 16-byte aligned.
+cudaError_t launch_qdq_mxfp4_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols, float sf,
+                                  cudaStream_t st);
+cudaError_t launch_ste_backward(const float *gy, const uint32_t *mask, float *gx, int64_t rows, int64_t cols,
+                                cudaStream_t st);
 
 // ---- GEMM (mxq_gemm.cu) ----
 enum GemmMode { kDense = 0, kGroupedRows = 1, kGroupedK = 2 };
+// Operand kind: kMXF8 = E4M3 codes with E8M0 block scales (all modes);
+// kBF16 = plain bf16 operands, no scales (kDense only).
+enum GemmKind { kMXF8 = 0, kBF16 = 1 };
 
 struct GemmProblem {
     GemmMode mode;
+    int kind;  // GemmKind; sizes below are in elements for both kinds
     // A: [a_rows x a_k] E4M3 codes, K-major; scales swz(a_rows, a_k/32)
     const uint8_t *a, *sa;
     int64_t a_rows, a_k;
@@ -40,6 +51,7 @@ struct GemmProblem {
     int64_t b_k_per_expert;   // kGroupedRows: B contraction offset of expert e = e * this
     int64_t c_expert_stride;  // kGroupedK: elements between experts' outputs
     int64_t T;                // kGroupedRows: token rows (= off[E])
+    const void *bias;         // kDense: optional bf16 [N] added in fp32 before rounding (16-byte aligned)
 };
 cudaError_t launch_gemm(const GemmProblem &p, cudaStream_t st);
 // Reads the device error word set by bounded waits that gave up, then clears it.

@@ -141,13 +141,21 @@ __device__ __forceinline__ float qdq_one(float x, const E2M1Thr &T) {
 
 // ============================================================================
 // Row quant: 128 x 128 tile per CTA, blocks along cols (cols % 32 == 0).
-//   FMT 0: bf16 -> E4M3 codes [R x C]      FMT 1: bf16/fp32 -> E2M1 [R x C/2]
+//   FMT 0: bf16 -> E4M3 codes [R x C] (MXFP8)
+//   FMT 1: bf16/fp32 -> packed E2M1 nibbles [R x C/2] (MXFP4)
+//   FMT 2: bf16 -> MXFP4 values written as E4M3 codes [R x C]: every E2M1
+//          value is an E4M3 value, so with the same E8M0 scale the MXFP8
+//          block-scaled MMA multiplies exactly the MXFP4 quant-dequant.
+// MXFP4 formats take the scale factor sf (6 by default).
 // Each thread owns 8 chunks of 8 elements; 4 lanes form one 32-block.
 // ============================================================================
+// E4M3 code of E2M1 codebook index i (0, .5, 1, 1.5, 2, 3, 4, 6), byte i.
+constexpr unsigned long long kE2M1AsE4M3 = 0x4C4844403C383000ull;
+
 template <typename InT, int FMT>
 __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__ x, int64_t R, int64_t C,
                                                          int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
-                                                         uint8_t *__restrict__ s, int64_t kb_tiles) {
+                                                         uint8_t *__restrict__ s, int64_t kb_tiles, float sf) {
     __shared__ __align__(16) uint8_t satom[512];
     const int tid = threadIdx.x, lane = tid & 31;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile, c0 = static_cast<int64_t>(blockIdx.x) * kTile;
@@ -204,18 +212,37 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
             a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
             a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
             const bool nonfinite = a >= 0x7F800000u;
-            const int e = nonfinite ? 0 : mx4_exp(__uint_as_float(a), 6.0f);
+            const int e = nonfinite ? 0 : mx4_exp(__uint_as_float(a), sf);
             sbyte = nonfinite ? 0xFF : static_cast<uint8_t>(e + 127);
             const E2M1Thr T = e2m1_thresholds(e);
-            uint32_t packed = 0;
+            if (FMT == 1) {
+                uint32_t packed = 0;
 #pragma unroll
-            for (int k = 0; k < 8; k++) {
-                const uint32_t idx = nonfinite ? 7u : e2m1_index(fabsf(v[k]), T);
-                const uint32_t nib = ((__float_as_uint(v[k]) >> 28) & 8u) | idx;
-                packed |= nib << (4 * k);
-            }
-            if (valid) {
-                asm volatile("st.global.u32 [%0], %1;" ::"l"(q + gr * ldq + gc / 2), "r"(packed) : "memory");
+                for (int k = 0; k < 8; k++) {
+                    const uint32_t idx = nonfinite ? 7u : e2m1_index(fabsf(v[k]), T);
+                    const uint32_t nib = ((__float_as_uint(v[k]) >> 28) & 8u) | idx;
+                    packed |= nib << (4 * k);
+                }
+                if (valid) {
+                    asm volatile("st.global.u32 [%0], %1;" ::"l"(q + gr * ldq + gc / 2), "r"(packed) : "memory");
+                }
+            } else {
+                // E4M3 byte: sign | code of the E2M1 value; a non-finite block
+                // gets the NaN code 0x7F | sign under scale byte 0xFF
+                uint32_t lo = 0, hi = 0;
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const uint32_t mag = nonfinite ? 0x7Fu
+                                                   : static_cast<uint32_t>(
+                                                         (kE2M1AsE4M3 >> (8 * e2m1_index(fabsf(v[k]), T))) & 0xFFu);
+                    const uint32_t code = ((__float_as_uint(v[k]) >> 24) & 0x80u) | mag;
+                    if (k < 4) lo |= code << (8 * k);
+                    else hi |= code << (8 * (k - 4));
+                }
+                if (valid) {
+                    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(q + gr * ldq + gc), "r"(lo), "r"(hi)
+                                 : "memory");
+                }
             }
         }
         if (!valid) sbyte = 0;  // padding rows / blocks of the scale tile
@@ -402,19 +429,23 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
 }
 
 // ============================================================================
-// MXFP4 quant-dequant.
+// MXFP4 quant-dequant, optionally with the saturation mask of the clipped
+// straight-through estimator (|x| > 6 * block scale; one 32-bit word per
+// block, bit i = element i of the block; 0 for a block with a non-finite
+// element, whose scale is not finite).
 //  Vector path (cols % 32 == 0, 16-byte aligned): 8 floats per thread, 4
 //  lanes per block.  General path: one warp per block of 32 (ragged rows).
 // Warp-uniform grid-stride loops so that every shuffle has all 32 lanes.
 // ============================================================================
-__global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restrict__ x, float *y, int64_t nchunks,
-                                                            float sf) {
+template <bool MASK>
+__global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restrict__ x, float *y,
+                                                            uint32_t *__restrict__ mask, int64_t nchunks, float sf) {
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t wstride = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
     for (int64_t wb = warp0 * 32; wb < nchunks; wb += wstride * 32) {
         const int64_t g = wb + lane;
-        const bool valid = g < nchunks;
+        const bool valid = g < nchunks;  // uniform over the 4 lanes of a block (nchunks % 4 == 0)
         float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         if (valid) {
             const uint4 a = ldg_nc_v4(x + 8 * g), b = ldg_nc_v4(x + 8 * g + 4);
@@ -426,23 +457,39 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restr
         for (int k = 0; k < 8; k++) a = max(a, __float_as_uint(v[k]) & 0x7FFFFFFFu);
         a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
         a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
-        if (!valid) continue;
         float o[8];
+        uint32_t bits = 0;
         if (a >= 0x7F800000u) {
 #pragma unroll
             for (int k = 0; k < 8; k++) o[k] = __uint_as_float(0x7FC00000u);
         } else {
             const E2M1Thr T = e2m1_thresholds(mx4_exp(__uint_as_float(a), sf));
+            const float limit = 6.0f * T.s;  // +inf for e = 127: nothing saturates
 #pragma unroll
-            for (int k = 0; k < 8; k++) o[k] = qdq_one(v[k], T);
+            for (int k = 0; k < 8; k++) {
+                o[k] = qdq_one(v[k], T);
+                if (MASK) bits |= (fabsf(v[k]) > limit ? 1u : 0u) << k;
+            }
         }
+        if (MASK) {
+            // the block's word from its 4 lanes, then lanes 0-7 write the warp's
+            // 8 consecutive words
+            uint32_t w = bits << (8 * (lane & 3));
+            w |= __shfl_xor_sync(0xffffffffu, w, 1);
+            w |= __shfl_xor_sync(0xffffffffu, w, 2);
+            w = __shfl_sync(0xffffffffu, w, (4 * lane) & 31);
+            if (lane < 8 && wb + 4 * lane < nchunks) mask[wb / 4 + lane] = w;
+        }
+        if (!valid) continue;
         stg_v4(y + 8 * g, make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3])));
         stg_v4(y + 8 * g + 4, make_uint4(__float_as_uint(o[4]), __float_as_uint(o[5]), __float_as_uint(o[6]), __float_as_uint(o[7])));
     }
 }
 
-__global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restrict__ x, float *y, int64_t rows,
-                                                            int64_t cols, float sf) {
+template <bool MASK>
+__global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restrict__ x, float *y,
+                                                            uint32_t *__restrict__ mask, int64_t rows, int64_t cols,
+                                                            float sf) {
     const int lane = threadIdx.x & 31;
     const int64_t nb = (cols + 31) / 32;
     const int64_t nblocks = rows * nb;
@@ -456,15 +503,95 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restr
         uint32_t a = __float_as_uint(v) & 0x7FFFFFFFu;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
-        if (!valid) continue;
         float out;
+        bool sat = false;
         if (a >= 0x7F800000u) {
             out = __uint_as_float(0x7FC00000u);
         } else {
             const E2M1Thr T = e2m1_thresholds(mx4_exp(__uint_as_float(a), sf));
             out = qdq_one(v, T);
+            sat = valid && fabsf(v) > 6.0f * T.s;
         }
-        y[r * cols + c] = out;
+        if (MASK) {
+            const uint32_t w = __ballot_sync(0xffffffffu, sat);
+            if (lane == 0) mask[k] = w;
+        }
+        if (valid) y[r * cols + c] = out;
+    }
+}
+
+// MXFP4 quant-dequant of bf16 to bf16 (cols % 32 == 0, 16-byte aligned): 8
+// elements per thread, 4 lanes per block.  Every result (codebook value x
+// 2^e, or NaN for a non-finite block) is exact in bf16, so the fp32 result's
+// upper half is the bf16 result.
+__global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_bf16(const uint16_t *__restrict__ x, uint16_t *y,
+                                                             int64_t nchunks, float sf) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t wstride = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+    for (int64_t wb = warp0 * 32; wb < nchunks; wb += wstride * 32) {
+        const int64_t g = wb + lane;
+        const bool valid = g < nchunks;
+        uint4 in = make_uint4(0, 0, 0, 0);
+        if (valid) in = ldg_nc_v4(x + 8 * g);
+        const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 4; k++) { v[2 * k] = bf16lo(w[k]); v[2 * k + 1] = bf16hi(w[k]); }
+        const uint32_t (&w4)[4] = w;
+        uint32_t a = amax8_bf16(w4) << 16;  // |bf16| bits as fp32 bits
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        if (!valid) continue;
+        uint32_t o[4];
+        if (a >= 0x7F800000u) {
+#pragma unroll
+            for (int k = 0; k < 4; k++) o[k] = 0x7FC07FC0u;
+        } else {
+            const E2M1Thr T = e2m1_thresholds(mx4_exp(__uint_as_float(a), sf));
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+                o[k] = (__float_as_uint(qdq_one(v[2 * k], T)) >> 16) |
+                       (__float_as_uint(qdq_one(v[2 * k + 1], T)) & 0xFFFF0000u);
+        }
+        stg_v4(y + 8 * g, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+}
+
+// Clipped straight-through estimator, backward: gx = gy except +0.0 where the
+// forward's saturation mask is set.  Vector path: 8 floats per thread (cols %
+// 32 == 0, 16-byte aligned); general path: one warp per block.
+__global__ void __launch_bounds__(kThreads) k_ste_backward_vec(const float *__restrict__ gy,
+                                                               const uint32_t *__restrict__ mask, float *gx,
+                                                               int64_t nchunks) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < nchunks; g += stride) {
+        const uint32_t bits = (__ldg(mask + g / 4) >> (8 * (g & 3))) & 0xFFu;
+        uint4 a = ldg_nc_v4(gy + 8 * g), b = ldg_nc_v4(gy + 8 * g + 4);
+        if (bits) {
+            a.x = (bits & 1u) ? 0u : a.x;    a.y = (bits & 2u) ? 0u : a.y;
+            a.z = (bits & 4u) ? 0u : a.z;    a.w = (bits & 8u) ? 0u : a.w;
+            b.x = (bits & 16u) ? 0u : b.x;   b.y = (bits & 32u) ? 0u : b.y;
+            b.z = (bits & 64u) ? 0u : b.z;   b.w = (bits & 128u) ? 0u : b.w;
+        }
+        stg_v4(gx + 8 * g, a);
+        stg_v4(gx + 8 * g + 4, b);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_ste_backward_gen(const float *__restrict__ gy,
+                                                               const uint32_t *__restrict__ mask, float *gx,
+                                                               int64_t rows, int64_t cols) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nb = (cols + 31) / 32;
+    const int64_t nblocks = rows * nb;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t wstride = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+    for (int64_t k = warp0; k < nblocks; k += wstride) {
+        const int64_t r = k / nb, c = 32 * (k % nb) + lane;
+        if (c >= cols) continue;
+        const bool sat = (__ldg(mask + k) >> lane) & 1u;
+        gx[r * cols + c] = sat ? 0.0f : gy[r * cols + c];
     }
 }
 
@@ -479,15 +606,19 @@ int grid_for(int64_t work_items, int per_cta) {
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, int64_t C, int64_t ldx, uint8_t *q,
-                              uint8_t *s, cudaStream_t st) {
+                              uint8_t *s, cudaStream_t st, float sf) {
     const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((R + kTile - 1) / kTile));
     const int64_t kb_tiles = ((C / 32) + 3) / 4;
+    const uint16_t *xb = static_cast<const uint16_t *>(x);
     if (fmt == 0) {
-        k_quant_rows<uint16_t, 0><<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(x), R, C, ldx, q, C, s, kb_tiles);
+        k_quant_rows<uint16_t, 0><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf);
+    } else if (fmt == 2) {
+        k_quant_rows<uint16_t, 2><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf);
     } else if (fp32_in) {
-        k_quant_rows<float, 1><<<grid, kThreads, 0, st>>>(static_cast<const float *>(x), R, C, ldx, q, C / 2, s, kb_tiles);
+        k_quant_rows<float, 1><<<grid, kThreads, 0, st>>>(static_cast<const float *>(x), R, C, ldx, q, C / 2, s,
+                                                          kb_tiles, sf);
     } else {
-        k_quant_rows<uint16_t, 1><<<grid, kThreads, 0, st>>>(static_cast<const uint16_t *>(x), R, C, ldx, q, C / 2, s, kb_tiles);
+        k_quant_rows<uint16_t, 1><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C / 2, s, kb_tiles, sf);
     }
     return cudaGetLastError();
 }
@@ -515,14 +646,39 @@ cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, c
     return cudaGetLastError();
 }
 
-cudaError_t launch_qdq_mxfp4(const float *x, float *y, int64_t rows, int64_t cols, float sf, cudaStream_t st) {
+cudaError_t launch_qdq_mxfp4(const float *x, float *y, uint32_t *mask, int64_t rows, int64_t cols, float sf,
+                             cudaStream_t st) {
     const bool vec = (cols % 32 == 0) && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) == 0;
     if (vec) {
         const int64_t nchunks = rows * cols / 8;
-        k_qdq_mxfp4_vec<<<grid_for(nchunks, kThreads * 2), kThreads, 0, st>>>(x, y, nchunks, sf);
+        const int grid = grid_for(nchunks, kThreads * 2);
+        if (mask) k_qdq_mxfp4_vec<true><<<grid, kThreads, 0, st>>>(x, y, mask, nchunks, sf);
+        else k_qdq_mxfp4_vec<false><<<grid, kThreads, 0, st>>>(x, y, nullptr, nchunks, sf);
     } else {
         const int64_t nblocks = rows * ((cols + 31) / 32);
-        k_qdq_mxfp4_gen<<<grid_for(nblocks, kThreads / 32), kThreads, 0, st>>>(x, y, rows, cols, sf);
+        const int grid = grid_for(nblocks, kThreads / 32);
+        if (mask) k_qdq_mxfp4_gen<true><<<grid, kThreads, 0, st>>>(x, y, mask, rows, cols, sf);
+        else k_qdq_mxfp4_gen<false><<<grid, kThreads, 0, st>>>(x, y, nullptr, rows, cols, sf);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qdq_mxfp4_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols, float sf,
+                                  cudaStream_t st) {
+    const int64_t nchunks = rows * cols / 8;
+    k_qdq_mxfp4_bf16<<<grid_for(nchunks, kThreads * 2), kThreads, 0, st>>>(x, y, nchunks, sf);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ste_backward(const float *gy, const uint32_t *mask, float *gx, int64_t rows, int64_t cols,
+                                cudaStream_t st) {
+    const bool vec = (cols % 32 == 0) && ((reinterpret_cast<uintptr_t>(gy) | reinterpret_cast<uintptr_t>(gx)) & 15) == 0;
+    if (vec) {
+        const int64_t nchunks = rows * cols / 8;
+        k_ste_backward_vec<<<grid_for(nchunks, kThreads * 2), kThreads, 0, st>>>(gy, mask, gx, nchunks);
+    } else {
+        const int64_t nblocks = rows * ((cols + 31) / 32);
+        k_ste_backward_gen<<<grid_for(nblocks, kThreads / 32), kThreads, 0, st>>>(gy, mask, gx, rows, cols);
     }
     return cudaGetLastError();
 }

@@ -43,6 +43,11 @@ def test_size_queries(lib):
     assert m.mxq_linear_saved_bytes(M, N, K, m.RECOMPUTE) == 0
     assert m.mxq_linear_ctx_bytes(M, N, K, m.RECOMPUTE) == N * M + N * (M // 32)
     assert m.mxq_linear_workspace_bytes(M, N, K, m.RECOMPUTE) >= m.mxq_linear_workspace_bytes(M, N, K, m.SAVE_QUANT)
+    # weight cache: row(W) + colT(W); the cached path's ctx has no colT(W)
+    assert m.mxq_linear_weight_cache_bytes(N, K) == 2 * (N * K + K * (N // 32))
+    colTW = N * K + N * (K // 32)
+    assert m.mxq_linear_wq_ctx_bytes(M, N, K, m.SAVE_QUANT) == m.mxq_linear_ctx_bytes(M, N, K, m.SAVE_QUANT) - colTW
+    assert m.mxq_linear_wq_ctx_bytes(M, N, K, m.RECOMPUTE) == m.mxq_linear_ctx_bytes(M, N, K, m.RECOMPUTE)
 
 
 def _status(fn, *args):
@@ -68,6 +73,29 @@ def test_host_validation_rejects_before_launch(lib):
     assert _status(m.mxq_qdq_mxfp4, FAKE, FAKE, 4, 64, 32, 0.0, 0) == INV
     assert _status(m.mxq_qdq_mxfp4, FAKE, FAKE, 4, 64, 32, -1.0, 0) == INV
     assert _status(m.mxq_qdq_mxfp4, FAKE, FAKE, 4, 64, 32, float("nan"), 0) == INV
+    # clipped STE: same checks as the QDQ plus a non-null, aligned mask
+    assert _status(m.mxq_mxfp4_ste_forward, FAKE, FAKE, FAKE, 4, 64, 16, 6.0, 0) == UNS
+    assert _status(m.mxq_mxfp4_ste_forward, FAKE, FAKE, None, 4, 64, 32, 6.0, 0) == INV
+    assert _status(m.mxq_mxfp4_ste_forward, FAKE, FAKE, FAKE + 2, 4, 64, 32, 6.0, 0) == INV
+    assert _status(m.mxq_mxfp4_ste_forward, FAKE, FAKE, FAKE, 4, 64, 32, 0.0, 0) == INV
+    assert _status(m.mxq_mxfp4_ste_backward, FAKE, None, 4, 64, FAKE, 0) == INV
+    assert _status(m.mxq_mxfp4_ste_backward, None, FAKE, 4, 64, FAKE, 0) == INV
+    assert _status(m.mxq_mxfp4_ste_backward, FAKE, FAKE, -1, 64, FAKE, 0) == INV
+    assert _status(m.mxq_mxfp4_ste_backward, None, None, 0, 64, None, 0) == 0
+    # QAT linear forward: dims multiple of 32, sf > 0, workspace, aligned bias
+    assert _status(m.mxq_qat_linear_fwd, FAKE, FAKE, None, 64, 64, 48, 1, 6.0, FAKE, FAKE, 1 << 30, 0) == INV
+    assert _status(m.mxq_qat_linear_fwd, FAKE, FAKE, None, 64, 64, 64, 1, 0.0, FAKE, FAKE, 1 << 30, 0) == INV
+    assert _status(m.mxq_qat_linear_fwd, FAKE, FAKE, FAKE + 2, 64, 64, 64, 1, 6.0, FAKE, FAKE, 1 << 30, 0) == INV
+    assert _status(m.mxq_qat_linear_fwd, FAKE, FAKE, None, 64, 64, 64, 1, 6.0, FAKE, FAKE, 16, 0) == INV
+    assert m.mxq_qat_linear_workspace_bytes(64, 64, 64, 1) == 2 * (64 * 64 + 512)
+    assert m.mxq_qat_linear_workspace_bytes(64, 64, 64, 0) == 2 * 64 * 64
+    # bf16 quant-dequant: cols % 32, aligned pointers
+    assert _status(m.mxq_qdq_mxfp4_bf16, FAKE, FAKE, 4, 48, 32, 6.0, 0) == UNS
+    assert _status(m.mxq_qdq_mxfp4_bf16, FAKE + 8, FAKE, 4, 64, 32, 6.0, 0) == INV
+    # weight cache: size and dims checked before launch
+    assert _status(m.mxq_linear_quantize_weight, FAKE, 64, 64, FAKE, 16, 0) == INV
+    assert _status(m.mxq_linear_quantize_weight, FAKE, 64, 48, FAKE, 1 << 30, 0) == INV
+    assert _status(m.mxq_linear_fwd_wq, FAKE, FAKE, 64, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 16, 0) == INV
     # quantize: MXFP8 needs bf16, E2M1 is last-axis only, block axis multiple of 32
     assert _status(m.mxq_quantize, FAKE, m.F32, 64, 64, 64, -1, m.E4M3, 0, FAKE, FAKE, None, None, 0) == UNS
     assert _status(m.mxq_quantize, FAKE, m.BF16, 64, 64, 64, -2, m.E2M1, 0, None, None, FAKE, FAKE, 0) == UNS

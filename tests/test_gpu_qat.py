@@ -1,0 +1,119 @@
+"""GPU parity of the MXFP4 QAT linear forward ("AMCT FakeQuant" article,
+section 4.3): y = F.linear(Q(x), Q(W), b) against the binary64 oracle.
+
+Tolerance as for the MXFP8 GEMMs (max-rel 1e-2, Frobenius 2e-3 against the
+binary64 product of the quant-dequantized operands plus bias); where every
+partial sum is exact in fp32 the bf16 result must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import mxq_inputs
+import oracle
+from test_gpu_gemm import check_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _bf16(a) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _rne_bits(ref: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy()
+
+
+def _on_grid(R, K, seed, emin=-2, emax=2):
+    """Blocks of codebook values x 2^e, each holding +-6 * 2^e: fixed points of
+    the MXFP4 quant-dequant along K."""
+    rng = np.random.default_rng(seed)
+    book = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    v = rng.choice(book, size=(R, K)) * rng.choice([-1.0, 1.0], size=(R, K))
+    v[:, ::32] = 6.0 * rng.choice([-1.0, 1.0], size=(R, K // 32))
+    e = rng.integers(emin, emax + 1, size=(R, K // 32))
+    return v * np.repeat(np.exp2(e), 32, axis=1)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (96, 352, 96), (256, 512, 256)])
+def test_exact_sums_bit_exact(mxq, M, N, K):
+    """Operands on the MXFP4 grid with exponents in [-2, 2] and a bias on a
+    2^-2 grid: every partial sum is exact in fp32, so y = bf16(exact)."""
+    x, w = _on_grid(M, K, 1), _on_grid(N, K, 2)
+    b = np.random.default_rng(3).integers(-64, 64, size=N) * 0.25
+    y = mxq.qat_linear_fwd(_bf16(x).to(DEV), _bf16(w).to(DEV), _bf16(b).to(DEV))
+    ref = oracle.qat_linear_ref(_bf16(x), _bf16(w), _bf16(b))
+    assert np.array_equal(ref, x @ w.T + b[None, :])
+    assert np.array_equal(y.cpu().view(torch.int16).numpy(), _rne_bits(ref))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (1024, 768, 1024), (224, 352, 160)])
+@pytest.mark.parametrize("sf", [6.0, 7.5])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_random_within_tolerance(mxq, M, N, K, sf, with_bias):
+    x, w, _ = mxq_inputs.linear_inputs(M, N, K, seed=M + N)
+    b = _bf16(0.05 * np.random.default_rng(N).standard_normal(N)) if with_bias else None
+    y = mxq.qat_linear_fwd(x.to(DEV), w.to(DEV), None if b is None else b.to(DEV), scale_factor=sf)
+    torch.cuda.synchronize()
+    assert mxq.mxq_poll_device_error() == 0
+    check_close(y, oracle.qat_linear_ref(x, w, b, scale_factor=sf))
+
+
+def test_full_size_sampled_rows(mxq):
+    """8192 x 14336 x 4096 (the dense layer's shape), 64 sampled rows."""
+    M, N, K = 8192, 14336, 4096
+    x, w, _ = mxq_inputs.linear_inputs(M, N, K, seed=0)
+    b = _bf16(0.05 * np.random.default_rng(1).standard_normal(N))
+    y = mxq.qat_linear_fwd(x.to(DEV), w.to(DEV), b.to(DEV))
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.random.default_rng(2).choice(M, 60, replace=False), [0, 127, 128, M - 1]]))
+    ref = oracle.qat_linear_ref(x[torch.from_numpy(rows)], w, b)
+    check_close(y[torch.from_numpy(rows).to(DEV)], ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (96, 352, 512)])
+def test_w4a16_exact_sums_bit_exact(mxq, M, N, K):
+    """x on a 2^-4 grid (|x| <= 8), W on the MXFP4 grid: every partial sum of
+    x Q(W)^T is exact in fp32, so y = bf16(exact)."""
+    rng = np.random.default_rng(M + K)
+    x = rng.integers(-128, 129, size=(M, K)) / 16.0
+    w = _on_grid(N, K, 5)
+    y = mxq.qat_linear_fwd(_bf16(x).to(DEV), _bf16(w).to(DEV), quantize_input=False)
+    ref = oracle.qat_linear_ref(_bf16(x), _bf16(w), quantize_input=False)
+    assert np.array_equal(ref, x @ w.T)
+    assert np.array_equal(y.cpu().view(torch.int16).numpy(), _rne_bits(ref))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (224, 352, 160), (1024, 768, 1024)])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_w4a16_random_within_tolerance(mxq, M, N, K, with_bias):
+    x, w, _ = mxq_inputs.linear_inputs(M, N, K, seed=3 * M + N)
+    b = _bf16(0.05 * np.random.default_rng(K).standard_normal(N)) if with_bias else None
+    y = mxq.qat_linear_fwd(x.to(DEV), w.to(DEV), None if b is None else b.to(DEV), quantize_input=False)
+    torch.cuda.synchronize()
+    assert mxq.mxq_poll_device_error() == 0
+    check_close(y, oracle.qat_linear_ref(x, w, b, quantize_input=False))
+
+
+def test_w4a16_full_size_sampled_rows(mxq):
+    M, N, K = 8192, 14336, 4096
+    x, w, _ = mxq_inputs.linear_inputs(M, N, K, seed=0)
+    y = mxq.qat_linear_fwd(x.to(DEV), w.to(DEV), quantize_input=False)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.random.default_rng(4).choice(M, 60, replace=False), [0, M - 1]]))
+    check_close(y[torch.from_numpy(rows).to(DEV)],
+                oracle.qat_linear_ref(x[torch.from_numpy(rows)], w, quantize_input=False))
+
+
+@pytest.mark.parametrize("shape", [(64, 256), (4096, 4096), (3, 96)])
+@pytest.mark.parametrize("sf", [6.0, 7.5])
+def test_bf16_qdq_bit_exact(mxq, shape, sf):
+    """bf16 -> bf16 quant-dequant equals the fp32 oracle on the widened values,
+    narrowed back to bf16 (exact)."""
+    a = mxq_inputs.mxfp4_large(shape[0], shape[1], seed=shape[0])
+    xb = _bf16(a)
+    y = mxq.qdq_mxfp4(xb.to(DEV), sf).cpu()
+    ref = oracle.mxfp4_qdq(xb.to(torch.float32).numpy(), np.float32(sf))
+    assert np.array_equal(torch.from_numpy(ref).to(torch.bfloat16).to(torch.float32).numpy().view(np.uint32),
+                          ref.view(np.uint32))  # exact in bf16
+    assert np.array_equal(y.view(torch.int16).numpy(), torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy())
