@@ -879,6 +879,37 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
 
 }  // namespace
 
+bool encode_tmap_2d(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle,
+                    CUtensorMapL2promotion promo) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(m, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+             promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t device_error_word(unsigned int **out) {
+    static unsigned int *addr[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_error);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<unsigned int *>(p);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
 cudaError_t read_and_clear_device_error(unsigned int *word) {
     cudaError_t e = cudaMemcpyFromSymbol(word, g_device_error, sizeof(unsigned int));
     if (e != cudaSuccess || *word == 0) return e;

@@ -1,6 +1,7 @@
 // mxq_internal.h -- kernel launchers shared between the libmxq translation units.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "mxq.h"
@@ -54,6 +55,13 @@ struct GemmProblem {
     const void *bias;         // kDense: optional bf16 [N] added in fp32 before rounding (16-byte aligned)
 };
 cudaError_t launch_gemm(const GemmProblem &p, cudaStream_t st);
+// 2-D tiled tensor map over [outer x inner] elements with the given row
+// stride in bytes (false if the driver entry point or the encode fails).
+bool encode_tmap_2d(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle,
+                    CUtensorMapL2promotion promo);
+// Device address of the error word that bounded waits set (current device).
+cudaError_t device_error_word(unsigned int **out);
 // Reads the device error word set by bounded waits that gave up, then clears it.
 cudaError_t read_and_clear_device_error(unsigned int *word);
 

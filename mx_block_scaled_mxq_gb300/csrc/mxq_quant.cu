@@ -429,6 +429,223 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
 }
 
 // ============================================================================
+// Persistent column quant (optionally dual / grouped) with TMA staging.
+// Same output as k_quant_cols; each CTA walks tiles blockIdx.x, +gridDim.x, ...
+// and keeps a two-deep ring of 128 x 128 bf16 tiles in shared memory: warp 0
+// issues the next tile's cp.async.bulk.tensor load before the CTA works on the
+// current one, so HBM reads overlap the quantization.  Grid = CTAs resident on
+// all SMs (3 per SM).  Waits are bounded: a timeout sets the device error word
+// and the CTA stops after its copies have landed.
+// ============================================================================
+constexpr uint32_t kTileBytes = kTile * kTile * 2;
+
+// First source row and the number of data rows of padded tile `rt` of a
+// per-group column quant (warp-wide; lane 0's result is returned to all).
+__device__ void grouped_tile_source(const ColParams &P, int64_t rt, int lane, int64_t &src0, int &nvalid) {
+    const int64_t t0 = rt * kTile;
+    int64_t run = 0, f_src0 = 0;
+    int f_nvalid = 0;
+    for (int base = 0; base < P.E; base += 32) {
+        const int e = base + lane;
+        int64_t n = 0;
+        if (e < P.E) n = P.offsets[e + 1] - P.offsets[e];
+        const int64_t padn = (n + 127) / 128 * 128;
+        int64_t incl = padn;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const int64_t start = run + incl - padn;
+        const bool mine = e < P.E && padn > 0 && t0 >= start && t0 < start + padn;
+        const unsigned bal = __ballot_sync(0xffffffffu, mine);
+        if (mine) {
+            f_src0 = P.offsets[e] + (t0 - start);
+            const int64_t left = n - (t0 - start);
+            f_nvalid = static_cast<int>(left < kTile ? left : kTile);
+        }
+        if (bal) {
+            const int src = __ffs(bal) - 1;
+            src0 = __shfl_sync(0xffffffffu, f_src0, src);
+            nvalid = __shfl_sync(0xffffffffu, f_nvalid, src);
+            return;
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    src0 = 0;
+    nvalid = 0;  // a padding tile past the last group: all zeros
+}
+
+template <bool ROWS, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_constant__ CUtensorMap tmX, ColParams P,
+                                                             int64_t n_tiles, int64_t ct_tiles, unsigned int *err) {
+    extern __shared__ __align__(128) uint8_t ring[];  // 2 x kTileBytes
+    __shared__ __align__(16) uint8_t srow_atom[512];
+    __shared__ __align__(16) uint8_t scol_atom[512];
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int64_t sh_src0[2];
+    __shared__ int sh_nvalid[2];
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t ring_s = smem_u32(ring), bar0 = smem_u32(&bars[0]);
+    volatile int *abort_v = &abort_flag;
+    if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // warp 0: resolve tile t into slot `buf` and start its load
+    auto issue = [&](int64_t t, int buf) {
+        const int64_t rt = t / ct_tiles, ct = t % ct_tiles;
+        int64_t src0 = rt * kTile;
+        int nvalid;
+        if (GROUPED) {
+            grouped_tile_source(P, rt, lane, src0, nvalid);
+        } else {
+            const int64_t left = P.R - src0;
+            nvalid = static_cast<int>(left < kTile ? left : kTile);
+        }
+        if (lane == 0) {
+            sh_src0[buf] = src0;
+            sh_nvalid[buf] = nvalid;
+            fence_proxy_async_smem();  // the slot's earlier generic reads come first
+            mbar_arrive_expect_tx(bar0 + 8 * buf, kTileBytes);
+            tma_load_2d(ring_s + buf * kTileBytes, &tmX, bar0 + 8 * buf, static_cast<int>(ct * kTile),
+                        static_cast<int>(src0));
+        }
+    };
+
+    int64_t t = blockIdx.x;
+    if (warp == 0 && t < n_tiles) issue(t, 0);
+    uint32_t k = 0;
+    int pending = t < n_tiles ? 0 : -1;  // slot with a load in flight (for the abort path)
+    for (; t < n_tiles; t += gridDim.x, k++) {
+        const int buf = k & 1;
+        const int64_t tn = t + gridDim.x;
+        if (warp == 0 && tn < n_tiles) issue(tn, buf ^ 1);
+        pending = tn < n_tiles ? (buf ^ 1) : -1;
+        const bool ok = mbar_wait(bar0 + 8 * buf, (k >> 1) & 1, abort_v, err);
+        if (!__syncthreads_and(ok)) break;
+
+        const uint8_t *tile = ring + buf * kTileBytes;
+        const int64_t rt = t / ct_tiles, ct = t % ct_tiles;
+        const int64_t c0 = ct * kTile;
+        const int64_t src0 = sh_src0[buf];
+        const int nvalid = sh_nvalid[buf];
+
+        if (ROWS) {
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int id = tid + kThreads * i;
+                const int row = id >> 4, ch = id & 15;
+                const int64_t gc = c0 + ch * 8;
+                const bool valid = row < nvalid && gc < P.C;
+                const uint4 v = *reinterpret_cast<const uint4 *>(tile + row * (kTile * 2) + ch * 16);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t a = amax8_bf16(w);
+                a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+                a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+                const int X = mx8_exp_from_bf16(a);
+                if (valid) {
+                    const uint2 codes = e4m3_codes8(w, X);
+                    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(P.q_row + (src0 + row) * P.C + gc),
+                                 "r"(codes.x), "r"(codes.y)
+                                 : "memory");
+                }
+                if ((lane & 3) == 0) srow_atom[16 * (row & 31) + 4 * (row >> 5) + (ch >> 2)] = valid ? mx8_scale_byte(X) : 0;
+            }
+        }
+
+        // ---- column pass: thread (p, b) = (column pair, 32-row block) ----
+        {
+            const int p = tid & 63, b = tid >> 6;
+            uint32_t col[32];
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+                const uint32_t wv = *reinterpret_cast<const uint32_t *>(tile + (32 * b + i) * (kTile * 2) + 4 * p);
+                col[i] = (!GROUPED || 32 * b + i < nvalid) ? wv : 0u;  // rows of the next group read as zero
+            }
+            uint32_t m2 = 0;
+#pragma unroll
+            for (int i = 0; i < 32; i++) m2 = __vmaxu2(m2, col[i] & 0x7FFF7FFFu);
+            const int Xlo = mx8_exp_from_bf16(m2 & 0xFFFFu), Xhi = mx8_exp_from_bf16(m2 >> 16);
+            const int cl = 2 * p, ch2 = 2 * p + 1;
+            scol_atom[16 * (cl & 31) + 4 * (cl >> 5) + b] = mx8_scale_byte(Xlo);
+            scol_atom[16 * (ch2 & 31) + 4 * (ch2 >> 5) + b] = mx8_scale_byte(Xhi);
+
+            const int64_t gcol = c0 + cl;
+            if (gcol < P.C) {
+                uint32_t lo[8], hi[8];
+                const float ilo = pow2_neg(Xlo > 127 ? 0 : Xlo), ihi = pow2_neg(Xhi > 127 ? 0 : Xhi);
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    const uint32_t a0 = col[4 * q], a1 = col[4 * q + 1], a2 = col[4 * q + 2], a3 = col[4 * q + 3];
+                    lo[q] = e4m3x4(bf16lo(a0) * ilo, bf16lo(a1) * ilo, bf16lo(a2) * ilo, bf16lo(a3) * ilo);
+                    hi[q] = e4m3x4(bf16hi(a0) * ihi, bf16hi(a1) * ihi, bf16hi(a2) * ihi, bf16hi(a3) * ihi);
+                }
+                if (Xlo > 127 || Xhi > 127) {  // non-finite blocks: NaN codes with the sign kept
+#pragma unroll
+                    for (int q = 0; q < 8; q++) {
+                        uint32_t sl = 0, sh = 0;
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            sl |= (0x7Fu | ((col[4 * q + j] >> 8) & 0x80u)) << (8 * j);
+                            sh |= (0x7Fu | ((col[4 * q + j] >> 24) & 0x80u)) << (8 * j);
+                        }
+                        if (Xlo > 127) lo[q] = sl;
+                        if (Xhi > 127) hi[q] = sh;
+                    }
+                }
+                const int64_t pos = rt * kTile + 32 * b;  // first output column (token) of the block
+                uint8_t *dlo = P.qT + gcol * P.ldqT + pos;
+                uint8_t *dhi = dlo + P.ldqT;
+                const int64_t limit = GROUPED ? P.ldqT : P.R;  // grouped tiles write padding zeros too
+                if (pos + 32 <= limit && (P.ldqT & 15) == 0) {
+                    stg_v4(dlo, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+                    stg_v4(dlo + 16, make_uint4(lo[4], lo[5], lo[6], lo[7]));
+                    stg_v4(dhi, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+                    stg_v4(dhi + 16, make_uint4(hi[4], hi[5], hi[6], hi[7]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j++) {
+                        if (pos + j < limit) {
+                            dlo[j] = static_cast<uint8_t>(lo[j >> 2] >> (8 * (j & 3)));
+                            dhi[j] = static_cast<uint8_t>(hi[j >> 2] >> (8 * (j & 3)));
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        if (ROWS && tid < 32) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(srow_atom + 16 * tid);
+            stg_v4(P.s_row + (rt * P.kb_row_tiles + ct) * 512 + 16 * tid, v);
+        } else if (tid >= 32 && tid < 64) {
+            const int l = tid - 32;
+            const uint4 v = *reinterpret_cast<const uint4 *>(scol_atom + 16 * l);
+            stg_v4(P.sT + (ct * P.kb_col_tiles + rt) * 512 + 16 * l, v);
+        }
+        __syncthreads();  // the slot and the atoms are free again
+    }
+    // stopped early: let the loads still in flight (this tile's and the
+    // prefetched one) land before shared memory goes away; bounded as well
+    if (tid == 0 && t < n_tiles) {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t j = 0; j < 2; j++) {
+            const uint32_t kk = k + j;
+            if (j == 1 && pending < 0) break;
+            while (!mbar_try_wait(bar0 + 8 * (kk & 1), (kk >> 1) & 1)) {
+                if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+            }
+        }
+    }
+}
+
+// ============================================================================
 // MXFP4 quant-dequant, optionally with the saturation mask of the clipped
 // straight-through estimator (|x| > 6 * block scale; one 32-bit word per
 // block, bit i = element i of the block; 0 for a block with a non-finite
@@ -623,13 +840,63 @@ cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, i
     return cudaGetLastError();
 }
 
+namespace {
+
+// Persistent TMA-staged launch of the column quant; returns false (no launch)
+// when the input cannot be described by a tensor map (unaligned base or row
+// stride, or coordinates past 2^31), so the caller falls back.
+template <bool ROWS, bool GROUPED>
+bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cudaError_t *res) {
+    if ((reinterpret_cast<uintptr_t>(P.x) & 15) || (P.ldx % 8) || P.C >= (1ll << 31) || P.R >= (1ll << 31) ||
+        P.R == 0)
+        return false;
+    CUtensorMap tm;
+    if (!encode_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, P.x, static_cast<uint64_t>(P.C),
+                        static_cast<uint64_t>(P.R), static_cast<uint64_t>(P.ldx) * 2, kTile, kTile,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return false;
+    unsigned int *err = nullptr;
+    cudaError_t e = device_error_word(&err);
+    if (e != cudaSuccess) { *res = e; return true; }
+    const int smem = 2 * static_cast<int>(kTileBytes);
+    static int per_sm[64] = {0}, sms[64] = {0};
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) { *res = e; return true; }
+    if (dev < 0 || dev >= 64) { *res = cudaErrorInvalidDevice; return true; }
+    if (per_sm[dev] == 0) {
+        if ((e = cudaFuncSetAttribute(k_quant_cols_tma<ROWS, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      smem)) != cudaSuccess ||
+            (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev], k_quant_cols_tma<ROWS, GROUPED>, kThreads,
+                                                               smem)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+            per_sm[dev] = 0;
+            *res = e;
+            return true;
+        }
+        if (per_sm[dev] < 1) per_sm[dev] = 1;
+    }
+    const int64_t ct_tiles = (P.C + kTile - 1) / kTile;
+    const int64_t n_tiles = row_tiles * ct_tiles;
+    const int64_t grid = n_tiles < static_cast<int64_t>(per_sm[dev]) * sms[dev] ? n_tiles
+                                                                                 : static_cast<int64_t>(per_sm[dev]) * sms[dev];
+    k_quant_cols_tma<ROWS, GROUPED><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tm, P, n_tiles, ct_tiles, err);
+    *res = cudaGetLastError();
+    return true;
+}
+
+}  // namespace
+
 cudaError_t launch_quant_cols(const uint16_t *x, int64_t R, int64_t C, int64_t ldx, uint8_t *q_row, uint8_t *s_row,
                               uint8_t *qT, uint8_t *sT, cudaStream_t st) {
     ColParams P{};
     P.x = x; P.R = R; P.C = C; P.ldx = ldx;
     P.q_row = q_row; P.s_row = s_row; P.kb_row_tiles = ((C / 32) + 3) / 4;
     P.qT = qT; P.sT = sT; P.ldqT = R; P.kb_col_tiles = (((R + 31) / 32) + 3) / 4;
-    const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((R + kTile - 1) / kTile));
+    const int64_t row_tiles = (R + kTile - 1) / kTile;
+    cudaError_t res = cudaSuccess;
+    if (q_row ? launch_cols_tma<true, false>(P, row_tiles, st, &res) : launch_cols_tma<false, false>(P, row_tiles, st, &res))
+        return res;
+    const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>(row_tiles));
     if (q_row) k_quant_cols<true, false><<<grid, kThreads, 0, st>>>(P);
     else k_quant_cols<false, false><<<grid, kThreads, 0, st>>>(P);
     return cudaGetLastError();
@@ -641,6 +908,8 @@ cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, c
     P.x = x; P.R = T; P.C = C; P.ldx = C;
     P.qT = qT; P.sT = sT; P.ldqT = t_pad; P.kb_col_tiles = (t_pad / 32 + 3) / 4;
     P.offsets = d_off; P.E = E;
+    cudaError_t res = cudaSuccess;
+    if (launch_cols_tma<false, true>(P, t_pad / kTile, st, &res)) return res;
     const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>(t_pad / kTile));
     k_quant_cols<false, true><<<grid, kThreads, 0, st>>>(P);
     return cudaGetLastError();
