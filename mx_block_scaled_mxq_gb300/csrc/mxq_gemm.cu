@@ -392,6 +392,62 @@ __device__ __forceinline__ bool mma4_commit_peek(uint32_t d_tmem, const uint64_t
     return ready != 0;
 }
 
+// One whole k-block of the single-CTA block-scaled path in one asm block:
+// the non-blocking test of the NEXT stage's full barrier is issued first, then
+// the three scale-tile copies (A, B rows 0-127, B rows 128-255) into TMEM, the
+// four K = 32 MMAs and the commit that frees the stage; the test's result is
+// read last, so its latency overlaps all of this stage's tcgen05 issue.
+// Descriptors are assembled from per-stage 32-bit low words (start address
+// >> 4) and constant high words; +32 bytes of K is +2 in the low word.
+// Returns whether the next stage's data has landed.
+__device__ __forceinline__ bool kblock_mxf8_cg1(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t sfa_t,
+                                                uint32_t sfb_t, uint32_t sa_lo, uint32_t sb_lo, uint32_t accumulate,
+                                                uint32_t bar_empty_s, uint32_t bar_full_next, uint32_t parity_next) {
+    constexpr uint32_t kAbHi = (1024u >> 4) | (1u << 14) | (2u << 29);  // SBO 1024, version 1, 128-byte swizzle
+    constexpr uint32_t kSfHi = (128u >> 4) | (1u << 14);                 // SBO 128, version 1, no swizzle
+    constexpr uint32_t kId0 = (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(128 >> 4) << 24);
+    uint32_t ready;
+    asm volatile(
+        "{\n\t.reg .pred pn, pa, p1;\n\t.reg .b64 da, db, ds;\n\t.reg .b32 ta, tb, tt;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n\t"
+        "mov.b64 ds, {%9, %11};\n\t"
+        "tcgen05.cp.cta_group::1.32x128b.warpx4 [%7], ds;\n\t"
+        "mov.b64 ds, {%10, %11};\n\t"
+        "tcgen05.cp.cta_group::1.32x128b.warpx4 [%8], ds;\n\t"
+        "add.u32 tt, %10, 32;\n\t"
+        "mov.b64 ds, {tt, %11};\n\t"
+        "add.u32 tt, %8, 4;\n\t"
+        "tcgen05.cp.cta_group::1.32x128b.warpx4 [tt], ds;\n\t"
+        "setp.ne.b32 pa, %3, 0;\n\t"
+        "setp.eq.u32 p1, 0, 0;\n\t"
+        "mov.b64 da, {%5, %12};\n\t"
+        "mov.b64 db, {%6, %12};\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %13, [%7], [%8], pa;\n\t"
+        "add.u32 ta, %5, 2;\n\t"
+        "add.u32 tb, %6, 2;\n\t"
+        "mov.b64 da, {ta, %12};\n\t"
+        "mov.b64 db, {tb, %12};\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %14, [%7], [%8], p1;\n\t"
+        "add.u32 ta, %5, 4;\n\t"
+        "add.u32 tb, %6, 4;\n\t"
+        "mov.b64 da, {ta, %12};\n\t"
+        "mov.b64 db, {tb, %12};\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %15, [%7], [%8], p1;\n\t"
+        "add.u32 ta, %5, 6;\n\t"
+        "add.u32 tb, %6, 6;\n\t"
+        "mov.b64 da, {ta, %12};\n\t"
+        "mov.b64 db, {tb, %12};\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %16, [%7], [%8], p1;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%17];\n\t"
+        "selp.u32 %0, 1, 0, pn;\n\t}"
+        : "=r"(ready)
+        : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(sfa_t),
+          "r"(sfb_t), "r"(sa_lo), "r"(sb_lo), "n"(kSfHi), "n"(kAbHi), "n"(kId0), "n"(kId0 | (1u << 4) | (1u << 29)),
+          "n"(kId0 | (2u << 4) | (2u << 29)), "n"(kId0 | (3u << 4) | (3u << 29)), "r"(bar_empty_s)
+        : "memory");
+    return ready != 0;
+}
+
 template <int CG, int KIND, bool BIAS>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -534,6 +590,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (CG == 1 || leader) {
             uint32_t g = 0, acc_it = 0;
             bool issued_any = false;
+            // descriptor low words (start address >> 4) of stage 0's operand and scale tiles
+            const uint32_t a_lo0 = (sbase + C::OFF_A) >> 4, b_lo0 = (sbase + C::OFF_B) >> 4;
+            const uint32_t sa_lo0 = (sbase + C::OFF_SFA) >> 4, sb_lo0 = (sbase + C::OFF_SFB) >> 4;
             for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
                 const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
                 if (!ti.valid) break;
@@ -544,7 +603,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (acc_it > 0 && !mbar_wait(bar_acce, (acc_it - 1) & 1, abort_flag, &g_device_error)) stop = 1;
                     tc_fence_after();
                     bool ready = false;  // stage g known to have landed (from the previous stage's peek)
-                    for (int kb = 0; kb < ti.nkb && !stop; kb++, g++) {
+                    int kb0 = 0;         // first k-block left to the general loop below
+                    if constexpr (CG == 1 && KIND == kMXF8) {
+                        // every k-block but a short last one: one asm block each
+                        const int nfull = ti.k_last == 4 ? ti.nkb : ti.nkb - 1;
+                        for (; kb0 < nfull; kb0++, g++) {
+                            const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
+                            if (!ready && !mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_device_error)) {
+                                stop = 1;
+                                break;
+                            }
+                            tc_fence_after();
+                            issued_any = true;
+                            const uint32_t s1 = (g + 1) % STAGES, ph1 = ((g + 1) / STAGES) & 1;
+                            const uint32_t sf_t = tmem + SF_COL0 + s * SF_STRIDE;
+                            ready = kblock_mxf8_cg1(tmem, a_lo0 + s * (C::A_BYTES >> 4), b_lo0 + s * (C::B_BYTES >> 4),
+                                                    sf_t, sf_t + 4, sa_lo0 + s * (C::SFA_BYTES >> 4),
+                                                    sb_lo0 + s * (C::SFB_BYTES >> 4), kb0 != 0 ? 1u : 0u,
+                                                    bar_empty + 8 * s, bar_full + 8 * s1, ph1);
+                        }
+                    }
+                    for (int kb = kb0; kb < ti.nkb && !stop; kb++, g++) {
                         const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
                         if (!ready && !mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_device_error)) { stop = 1; break; }
                         tc_fence_after();
