@@ -42,34 +42,38 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// The waiting thread may be suspended until the phase completes, for at most
+// kSuspendNs: a parked warp does not take issue slots from the warps that
+// are working (the MMA issuer and the TMA producer share SM sub-partitions
+// with the epilogue warps, which wait for most of each tile).
+constexpr uint32_t kSuspendNs = 10000000u;  // 10 ms
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
 
 // Wait until the phase with the given parity has completed.  Gives up (and
-// ORs kErrTimeout into *err) after kWaitTimeoutNs, or as soon as *abort is set
-// by another warp of the block.  Returns true when the phase completed.
+// ORs kErrTimeout into *err) after kWaitTimeoutNs, or once *abort is set by
+// another warp of the block (checked after every suspension).  Returns true
+// when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           unsigned int *err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-                *abort = 1;
-                atomicOr(err, kErrTimeout);
-                return false;
-            }
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            *abort = 1;
+            atomicOr(err, kErrTimeout);
+            return false;
         }
     }
 }

@@ -57,6 +57,11 @@ namespace {
 constexpr int BN = 256, BK = 128, THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512, SF_COL0 = 256, SF_STRIDE = 16;
 constexpr int kMaxTableE = 256;  // experts whose group tables are kept in shared memory
+// Epilogue stores: true = 32 x 32 blocks staged in shared memory and written
+// by TMA stores; false = coalesced 16-byte global stores after an in-register
+// transpose.  On GB300 the two are within 1% of each other (dense forward
+// 329 vs 327 us; MoE weight gradient 0.98 vs 0.99 ms).
+constexpr bool kEpilogueTma = true;
 
 template <int CG>
 struct Cfg {
@@ -94,6 +99,7 @@ struct Params {
     int m_tiles, n_tiles;  // tile counts (m in units of 128 * CG rows)
     int n_fastest;         // kDense tile order: 1 = n fastest (A is the larger operand)
     int tma_store;         // an output tensor map exists: unmasked 32-row boxes are stored with TMA
+    int vec_store;         // rows of C are 16-byte aligned (coalesced 16-byte stores)
     const __nv_bfloat16 *bias;  // kDense: bf16 [N] added to every row in fp32, or null
     int64_t total_tiles;   // tile index space (an upper bound for grouped rows)
 };
@@ -748,6 +754,59 @@ __global__ void __launch_bounds__(THREADS, 1)
             // to the tile's output (always for dense problems, where the tensor
             // map clips rows past M; grouped tiles mask rows of other experts).
             const int64_t wrow0 = ti.out_row0 + 32 * sub;
+            if (!kEpilogueTma && p.vec_store) {
+                // Per 32 x 32 block: a 4 x 4 transpose of 16-byte chunks inside each
+                // group of 4 lanes (two xor-shuffle rounds, in place) leaves lane
+                // 4g + c with chunk c of rows 4g .. 4g + 3, so each store
+                // instruction writes 8 rows x 64 contiguous bytes.  Rows outside the
+                // tile's output are masked per lane; a block cut by the last column
+                // goes row by row.
+                const int c4 = lane & 3;
+                const int64_t r0 = wrow0 + 4 * (lane >> 2);
+                uint8_t *wp = reinterpret_cast<uint8_t *>(p.c + ti.c_off + r0 * p.ldc + ti.col0 + 8 * c4);
+                const int64_t rstride = p.ldc * 2;
+                unsigned rmask = 0;
+#pragma unroll
+                for (int k = 0; k < 4; k++) rmask |= (r0 + k >= ti.row_lo && r0 + k < ti.row_hi ? 1u : 0u) << k;
+#pragma unroll
+                for (int ch = 0; ch < BN / 32; ch++) {
+                    const int64_t col = ti.col0 + 32 * ch;
+                    if (col >= ti.col_hi) break;  // warp-uniform
+                    uint32_t *m = pk + 16 * ch;    // chunk j, word w at m[4 * j + w]
+                    if (col + 32 <= ti.col_hi) {
+#pragma unroll
+                        for (int j = 0; j < 4; j += 2)
+#pragma unroll
+                            for (int w = 0; w < 4; w++) {
+                                const uint32_t snd = (lane & 1) ? m[4 * j + w] : m[4 * j + 4 + w];
+                                const uint32_t rcv = __shfl_xor_sync(0xffffffffu, snd, 1);
+                                if (lane & 1) m[4 * j + w] = rcv;
+                                else m[4 * j + 4 + w] = rcv;
+                            }
+#pragma unroll
+                        for (int j = 0; j < 2; j++)
+#pragma unroll
+                            for (int w = 0; w < 4; w++) {
+                                const uint32_t snd = (lane & 2) ? m[4 * j + w] : m[4 * j + 8 + w];
+                                const uint32_t rcv = __shfl_xor_sync(0xffffffffu, snd, 2);
+                                if (lane & 2) m[4 * j + w] = rcv;
+                                else m[4 * j + 8 + w] = rcv;
+                            }
+#pragma unroll
+                        for (int k = 0; k < 4; k++)
+                            if (rmask & (1u << k))
+                                *reinterpret_cast<uint4 *>(wp + k * rstride + 64 * ch) =
+                                    make_uint4(m[4 * k], m[4 * k + 1], m[4 * k + 2], m[4 * k + 3]);
+                    } else if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 32; i++)
+                            if (col + i < ti.col_hi)
+                                reinterpret_cast<uint16_t *>(crow)[col + i] =
+                                    static_cast<uint16_t>(m[i >> 1] >> (16 * (i & 1)));
+                    }
+                }
+                continue;
+            }
             if (p.tma_store && (p.mode == kDense || (wrow0 >= ti.row_lo && wrow0 + 32 <= ti.row_hi))) {
                 // Stage each 32 x 32 block in a 64-byte-swizzled slot (conflict-free
                 // 16-byte writes) and store it with TMA; columns past N are clipped
@@ -913,6 +972,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     // store is a plain global store
     const int64_t c_rows = g.mode == kGroupedK ? static_cast<int64_t>(g.E) * g.M : g.M;
     p.tma_store = c_rows < (1ll << 31) && make_out_tmap(&tmC, g.c, c_rows, g.N, g.ldc) ? 1 : 0;
+    p.vec_store = (g.ldc % 8 == 0 && (reinterpret_cast<uintptr_t>(g.c) & 15) == 0) ? 1 : 0;
     if (!p.tma_store) tmC = tmA;  // unused
     if (g.mode == kDense) p.total_tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     else if (g.mode == kGroupedRows) p.total_tiles = ((g.T + C::TILE_M - 1) / C::TILE_M + g.E) * p.n_tiles;
