@@ -75,7 +75,10 @@ struct Cfg {
     static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-    static constexpr uint32_t NUM_BARS = 2 * STAGES + 3;
+    // full / empty per stage; accumulator full / empty / drain; single-CTA
+    // tiles add the second accumulator bank's full / empty and both banks'
+    // "head drained" barriers
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + (CG == 1 ? 7 : 3);
     static constexpr uint32_t OFF_MISC = OFF_BAR + 128;
     static constexpr uint32_t OFF_GRP = OFF_MISC + 256;  // group tables (grouped modes, E <= kMaxTableE)
     // epilogue store staging: 4 warps x 2 slots x (32 rows x 64 bytes), 1024-aligned
@@ -470,6 +473,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bar_full = sbase + C::OFF_BAR, bar_empty = bar_full + 8 * STAGES;
     const uint32_t bar_accf = bar_full + 16 * STAGES, bar_acce = bar_accf + 8, bar_drain = bar_accf + 16;
+    // Two accumulator banks (single-CTA block-scaled tiles): tile t accumulates in
+    // TMEM columns [256 b, 256 b + 256), b = t % 2, and keeps its scale slots in
+    // the first 64 columns of the other bank.  The MMA warp starts tile t once
+    // tile t - 2 has been drained from bank b and the epilogue has read the first
+    // 64 columns of tile t - 1 (which also means tile t - 1's MMAs are done), so
+    // the next tile's MMAs overlap most of the previous tile's drain.
+    constexpr bool DB = CG == 1 && KIND == kMXF8;
+    const uint32_t bar_accf1 = bar_accf + 24, bar_acce1 = bar_accf + 32;
+    const uint32_t bar_headf0 = bar_accf + 40, bar_headf1 = bar_accf + 48;
     uint32_t rank = 0;
     if constexpr (CG == 2) rank = cluster_ctarank();
     const bool leader = rank == 0;
@@ -501,6 +513,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bar_accf, 1);
             mbar_init(bar_acce, 4 * CG);  // one arrival per epilogue warp (of both CTAs)
             mbar_init(bar_drain, 1);
+            if constexpr (DB) {
+                mbar_init(bar_accf1, 1);
+                mbar_init(bar_acce1, 4);
+                mbar_init(bar_headf0, 4);
+                mbar_init(bar_headf1, 4);
+            }
             fence_mbar_init();
         }
         __syncwarp();
@@ -604,9 +622,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!ti.valid) break;
                 if (ti.nkb == 0) continue;  // empty group: the epilogue writes zeros
                 int stop = 0;
+                // accumulator bank and scale-slot base of this tile
+                const uint32_t bank = DB ? (acc_it & 1) : 0;
+                const uint32_t d_tmem = tmem + 256 * bank;
+                const uint32_t sf_base = DB ? tmem + 256 * (1 - bank) : tmem + SF_COL0;
                 if (lane == 0) {
-                    // the epilogue must have drained the previous accumulator
-                    if (acc_it > 0 && !mbar_wait(bar_acce, (acc_it - 1) & 1, abort_flag, &g_device_error)) stop = 1;
+                    if constexpr (DB) {
+                        // bank drained of tile t - 2; head of tile t - 1 drained
+                        if (acc_it >= 2 && !mbar_wait(bank ? bar_acce1 : bar_acce, ((acc_it - 2) >> 1) & 1, abort_flag,
+                                                      &g_device_error))
+                            stop = 1;
+                        if (!stop && acc_it >= 1 &&
+                            !mbar_wait(bank ? bar_headf0 : bar_headf1, ((acc_it - 1) >> 1) & 1, abort_flag,
+                                       &g_device_error))
+                            stop = 1;
+                    } else {
+                        // the epilogue must have drained the previous accumulator
+                        if (acc_it > 0 && !mbar_wait(bar_acce, (acc_it - 1) & 1, abort_flag, &g_device_error)) stop = 1;
+                    }
                     tc_fence_after();
                     bool ready = false;  // stage g known to have landed (from the previous stage's peek)
                     int kb0 = 0;         // first k-block left to the general loop below
@@ -622,8 +655,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             tc_fence_after();
                             issued_any = true;
                             const uint32_t s1 = (g + 1) % STAGES, ph1 = ((g + 1) / STAGES) & 1;
-                            const uint32_t sf_t = tmem + SF_COL0 + s * SF_STRIDE;
-                            ready = kblock_mxf8_cg1(tmem, a_lo0 + s * (C::A_BYTES >> 4), b_lo0 + s * (C::B_BYTES >> 4),
+                            const uint32_t sf_t = sf_base + s * SF_STRIDE;
+                            ready = kblock_mxf8_cg1(d_tmem, a_lo0 + s * (C::A_BYTES >> 4), b_lo0 + s * (C::B_BYTES >> 4),
                                                     sf_t, sf_t + 4, sa_lo0 + s * (C::SFA_BYTES >> 4),
                                                     sb_lo0 + s * (C::SFB_BYTES >> 4), kb0 != 0 ? 1u : 0u,
                                                     bar_empty + 8 * s, bar_full + 8 * s1, ph1);
@@ -633,7 +666,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint32_t s = g % STAGES, ph = (g / STAGES) & 1;
                         if (!ready && !mbar_wait(bar_full + 8 * s, ph, abort_flag, &g_device_error)) { stop = 1; break; }
                         tc_fence_after();
-                        const uint32_t sfa_t = tmem + SF_COL0 + s * SF_STRIDE, sfb_t = sfa_t + 4;
+                        const uint32_t sfa_t = sf_base + s * SF_STRIDE, sfb_t = sfa_t + 4;
                         const uint64_t dA = smem_desc(sbase + C::OFF_SFA + s * C::SFA_BYTES, 0, 128, 0);
                         const uint64_t dB0 = smem_desc(sbase + C::OFF_SFB + s * C::SFB_BYTES, 0, 128, 0);
                         const uint64_t dB1 = smem_desc(sbase + C::OFF_SFB + s * C::SFB_BYTES + 512, 0, 128, 0);
@@ -662,7 +695,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 id[j] = make_idesc<CG, KIND>(j);
                             }
                             const uint32_t s1 = (g + 1) % STAGES, ph1 = ((g + 1) / STAGES) & 1;
-                            ready = mma4_commit_peek<CG, KIND>(tmem, ad, bd, id, sfa_t, sfb_t, kb != 0 ? 1u : 0u,
+                            ready = mma4_commit_peek<CG, KIND>(d_tmem, ad, bd, id, sfa_t, sfb_t, kb != 0 ? 1u : 0u,
                                                          bar_empty + 8 * s, bar_full + 8 * s1, ph1);
                             continue;
                         }
@@ -671,11 +704,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const uint64_t bd = smem_desc(sbase + C::OFF_B + s * C::B_BYTES + 32 * j, 0, 1024, 2);
                             const uint32_t acc = (kb | j) != 0 ? 1u : 0u;
                             if constexpr (KIND == kBF16)
-                                tc_mma_bf16(tmem, ad, bd, make_idesc<CG, KIND>(j), acc);
+                                tc_mma_bf16(d_tmem, ad, bd, make_idesc<CG, KIND>(j), acc);
                             else if constexpr (CG == 2)
-                                tc_mma_mxf8_pair(tmem, ad, bd, make_idesc<CG, KIND>(j), sfa_t, sfb_t, acc);
+                                tc_mma_mxf8_pair(d_tmem, ad, bd, make_idesc<CG, KIND>(j), sfa_t, sfb_t, acc);
                             else
-                                tc_mma_mxf8(tmem, ad, bd, make_idesc<CG, KIND>(j), sfa_t, sfb_t, acc);
+                                tc_mma_mxf8(d_tmem, ad, bd, make_idesc<CG, KIND>(j), sfa_t, sfb_t, acc);
                         }
                         if constexpr (CG == 2) tc_commit_pair_mc(bar_empty + 8 * s, 3);
                         else tc_commit(bar_empty + 8 * s);
@@ -683,7 +716,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     if (!stop) {
                         if constexpr (CG == 2) tc_commit_pair_mc(bar_accf, 3);
-                        else tc_commit(bar_accf);
+                        else tc_commit(DB && bank ? bar_accf1 : bar_accf);
                     }
                 }
                 acc_it++;
@@ -717,8 +750,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 continue;
             }
-            if (!mbar_wait(bar_accf, acc_it & 1, abort_flag, &g_device_error)) break;
+            const uint32_t bank = DB ? (acc_it & 1) : 0;
+            if (!mbar_wait(DB && bank ? bar_accf1 : bar_accf, DB ? ((acc_it >> 1) & 1) : (acc_it & 1), abort_flag,
+                           &g_device_error))
+                break;
             tc_fence_after();
+            const uint32_t acc_t = tmem + 256 * bank;
             // four quarters of 2 x 32 columns: two TMEM loads in flight per wait
             uint32_t pk[BN / 2];
 #pragma unroll
@@ -728,9 +765,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int q = 0; q < 2; q++) {
                     const int ch = 2 * h + q;
                     if (ti.col0 + 32 * ch < ti.col_hi)  // warp-uniform
-                        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * sub) << 16) + 32 * ch, r[q]);
+                        tmem_ld_32x32b_x32(acc_t + (static_cast<uint32_t>(32 * sub) << 16) + 32 * ch, r[q]);
                 }
                 tc_wait_ld();
+                if (DB && h == 0) {  // columns 0-63 read: the next tile may put its scales there
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bank ? bar_headf1 : bar_headf0);
+                }
 #pragma unroll
                 for (int q = 0; q < 2; q++) {
                     const int ch = 2 * h + q;
@@ -747,7 +789,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (lane == 0) {
                 if constexpr (CG == 2) mbar_arrive_cluster(lead_acce);
-                else mbar_arrive(bar_acce);
+                else mbar_arrive(DB && bank ? bar_acce1 : bar_acce);
             }
             acc_it++;
             // TMA stores take whole 32-row boxes: this warp's rows must all belong
