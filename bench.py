@@ -52,8 +52,8 @@ GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f
 # full-size launches (profiles/k_gemm__bench_launches_dram.md), keyed by a
 # hash of the kernel source; when the source has changed since, traffic is null.
 GEMM_DRAM_TRAFFIC = {
-    "5fedab98aa70dec5": {"linear_dw_gemm": 261166592, "moe_fwd_gemm": 1521294848,
-                         "moe_dx_gemm": 1531592192, "moe_dw_gemm": 2234944768},
+    "a5f3721a1133bca0": {"linear_dw_gemm": 259453440, "moe_fwd_gemm": 1496931584,
+                         "moe_dx_gemm": 1530479872, "moe_dw_gemm": 2234756608},
 }
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
