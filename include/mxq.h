@@ -336,6 +336,15 @@ const char *mxq_last_error_string(void);
  * otherwise.  word may be NULL. */
 mxq_status mxq_poll_device_error(uint32_t *word);
 
+/* Failure-detection self-test (no counterpart on the pages): launches one
+ * kernel whose thread waits, with the same bounded-wait code every kernel of
+ * this library uses, on an mbarrier that nothing arrives on.  After
+ * timeout_ms (1..10000) the wait gives up, sets bit 0 of the device error
+ * word and writes 1 to *d_gave_up (DEVICE int); the kernel then returns
+ * normally, so the context stays usable.  mxq_poll_device_error reports and
+ * clears the bit.  While the bit is set, GEMM launches skip their work. */
+mxq_status mxq_selftest_wait_timeout(uint32_t timeout_ms, int *d_gave_up, mxq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,7 @@ __all__ = [
     "mxq_mxfp4_ste_forward", "mxq_mxfp4_ste_backward", "mxfp4_ste_forward", "mxfp4_ste_backward",
     "mxq_qat_linear_workspace_bytes", "mxq_qat_linear_fwd", "qat_linear_fwd", "mxq_qdq_mxfp4_bf16",
     "mxq_linear_weight_cache_bytes", "mxq_linear_wq_ctx_bytes", "mxq_linear_quantize_weight", "mxq_linear_fwd_wq",
-    "mxq_linear_bwd_dx_wq",
+    "mxq_linear_bwd_dx_wq", "mxq_selftest_wait_timeout",
 ]
 
 BF16, F32 = 0, 1
@@ -78,6 +78,7 @@ _SIGNATURES = {
     "mxq_linear_bwd_dx_wq": (_I32, [_P, _P, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
     "mxq_last_error_string": (ctypes.c_char_p, []),
     "mxq_poll_device_error": (_I32, [ctypes.POINTER(ctypes.c_uint32)]),
+    "mxq_selftest_wait_timeout": (_I32, [ctypes.c_uint32, _P, _P]),
 }
 
 
@@ -230,6 +231,10 @@ def mxq_linear_fwd_noalloc(x, w, M, N, K, y, stream=None):
 
 def mxq_last_error_string() -> str:
     return load().mxq_last_error_string().decode(errors="replace")
+
+
+def mxq_selftest_wait_timeout(timeout_ms, d_gave_up, stream=None):
+    _check(load().mxq_selftest_wait_timeout(timeout_ms, _p(d_gave_up), _s(stream)), "mxq_selftest_wait_timeout")
 
 
 def mxq_poll_device_error():

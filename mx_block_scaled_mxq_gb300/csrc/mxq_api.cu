@@ -153,6 +153,17 @@ int64_t mxq_grouped_padded_rows(int64_t T, int E) {
     return 128 * (ceil_div(T, 128) + E);
 }
 
+mxq_status mxq_selftest_wait_timeout(uint32_t timeout_ms, int *d_gave_up, mxq_stream_t stream) {
+    if (!d_gave_up || (reinterpret_cast<uintptr_t>(d_gave_up) & 3))
+        return fail(MXQ_ERR_INVALID_ARG, "d_gave_up must be a non-null int pointer");
+    if (timeout_ms == 0 || timeout_ms > 10000) return fail(MXQ_ERR_INVALID_ARG, "timeout_ms must be in [1, 10000]");
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    return cuda_result(mxq::launch_selftest_wait(static_cast<uint64_t>(timeout_ms) * 1000000ull, d_gave_up,
+                                                 reinterpret_cast<cudaStream_t>(stream)),
+                       "mxq_selftest_wait_timeout launch");
+}
+
 mxq_status mxq_poll_device_error(uint32_t *word) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail(MXQ_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));

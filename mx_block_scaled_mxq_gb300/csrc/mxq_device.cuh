@@ -63,19 +63,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // ORs kErrTimeout into *err) after kWaitTimeoutNs, or once *abort is set by
 // another warp of the block (checked after every suspension).  Returns true
 // when the phase completed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          unsigned int *err) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int *abort,
+                                              unsigned int *err, uint64_t timeout_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if (global_timer_ns() - t0 > timeout_ns) {
             *abort = 1;
             atomicOr(err, kErrTimeout);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned int *err) {
+    return mbar_wait_for(bar, parity, abort, err, kWaitTimeoutNs);
 }
 
 // ---------------------------------------------------------------- TMA / bulk copies

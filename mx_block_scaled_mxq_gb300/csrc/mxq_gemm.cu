@@ -1091,6 +1091,28 @@ cudaError_t device_error_word(unsigned int **out) {
     return cudaSuccess;
 }
 
+namespace {
+// Failure-detection self-test: one thread waits on an mbarrier that nothing
+// arrives on, with a bounded wait of `timeout_ns`; the wait gives up, sets
+// the timeout bit of the device error word and the kernel returns normally.
+__global__ void k_selftest_wait(uint64_t timeout_ns, int *gave_up) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    const bool done = mbar_wait_for(b, 0, &abort_flag, &g_device_error, timeout_ns);
+    *gave_up = done ? 0 : 1;
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, int *d_gave_up, cudaStream_t st) {
+    k_selftest_wait<<<1, 32, 0, st>>>(timeout_ns, d_gave_up);
+    return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_device_error(unsigned int *word) {
     cudaError_t e = cudaMemcpyFromSymbol(word, g_device_error, sizeof(unsigned int));
     if (e != cudaSuccess || *word == 0) return e;

@@ -62,6 +62,9 @@ bool encode_tmap_2d(CUtensorMap *m, CUtensorMapDataType type, const void *base, 
                     CUtensorMapL2promotion promo);
 // Device address of the error word that bounded waits set (current device).
 cudaError_t device_error_word(unsigned int **out);
+// Self-test of the bounded waits: a kernel whose wait nothing completes gives
+// up after timeout_ns, sets the error word and writes 1 to *d_gave_up.
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, int *d_gave_up, cudaStream_t st);
 // Reads the device error word set by bounded waits that gave up, then clears it.
 cudaError_t read_and_clear_device_error(unsigned int *word);
 

@@ -96,6 +96,10 @@ def test_host_validation_rejects_before_launch(lib):
     assert _status(m.mxq_linear_quantize_weight, FAKE, 64, 64, FAKE, 16, 0) == INV
     assert _status(m.mxq_linear_quantize_weight, FAKE, 64, 48, FAKE, 1 << 30, 0) == INV
     assert _status(m.mxq_linear_fwd_wq, FAKE, FAKE, 64, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 16, 0) == INV
+    # failure-detection self-test: bounded timeout, device flag required
+    assert _status(m.mxq_selftest_wait_timeout, 0, FAKE, 0) == INV
+    assert _status(m.mxq_selftest_wait_timeout, 20000, FAKE, 0) == INV
+    assert _status(m.mxq_selftest_wait_timeout, 50, None, 0) == INV
     # quantize: MXFP8 needs bf16, E2M1 is last-axis only, block axis multiple of 32
     assert _status(m.mxq_quantize, FAKE, m.F32, 64, 64, 64, -1, m.E4M3, 0, FAKE, FAKE, None, None, 0) == UNS
     assert _status(m.mxq_quantize, FAKE, m.BF16, 64, 64, 64, -2, m.E2M1, 0, None, None, FAKE, FAKE, 0) == UNS
