@@ -459,7 +459,7 @@ def main():
     ap.add_argument("--mode", choices=["save", "recompute"], default="save")
     ap.add_argument("--cpu-steps", type=int, default=5, help="oracle sample steps for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=30)
     args = ap.parse_args()
     world, rank, local = dist_init()
 
@@ -553,7 +553,7 @@ def component_timings(wl, world):
     R4, C4 = FP4["R"], FP4["C"]
     m4 = torch.empty((R4, C4 // 32), dtype=torch.int32, device=wl.dev)
     g4 = torch.empty_like(wl.a4)
-    qat_ws_bytes = m.mxq_qat_linear_workspace_bytes(M, N, K, 1)
+    qat_ws_bytes = max(m.mxq_qat_linear_workspace_bytes(M, N, K, 1), m.mxq_qat_linear_workspace_bytes(M, N, K, 0))
     qat_ws = torch.empty(qat_ws_bytes, dtype=torch.uint8, device=wl.dev)
     wc_bytes = m.mxq_linear_weight_cache_bytes(N, K)
     wcache = torch.empty(wc_bytes, dtype=torch.uint8, device=wl.dev)
@@ -583,6 +583,8 @@ def component_timings(wl, world):
         "linear_wq": layer_wq,
         "qat_linear_fwd_w4a4": lambda: m.mxq_qat_linear_fwd(wl.x, wl.w, None, M, N, K, 1, 6.0, wl.y, qat_ws,
                                                             qat_ws_bytes),
+        "qat_linear_fwd_w4a16": lambda: m.mxq_qat_linear_fwd(wl.x, wl.w, None, M, N, K, 0, 6.0, wl.y, qat_ws,
+                                                             qat_ws_bytes),
     }
     out = {}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=wl.dev)
@@ -602,6 +604,7 @@ def component_timings(wl, world):
     out["mxfp4_ste_fwd_gbs"] = round(R4 * C4 * 8.125 / (out["mxfp4_ste_fwd_ms"] / 1e3) / 1e9, 1)
     out["mxfp4_ste_bwd_gbs"] = round(R4 * C4 * 8.125 / (out["mxfp4_ste_bwd_ms"] / 1e3) / 1e9, 1)
     out["qat_linear_fwd_w4a4_tflops"] = round(2 * M * N * K / (out["qat_linear_fwd_w4a4_ms"] / 1e3) / 1e12, 1)
+    out["qat_linear_fwd_w4a16_tflops"] = round(2 * M * N * K / (out["qat_linear_fwd_w4a16_ms"] / 1e3) / 1e12, 1)
     out["moe_fwd_tflops"] = round(2 * T * Nm * Km / (out["moe_fwd_ms"] / 1e3) / 1e12, 1)
     # the other linear mode on the same buffers
     other = m.RECOMPUTE if wl.mode == m.SAVE_QUANT else m.SAVE_QUANT
