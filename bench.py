@@ -52,8 +52,8 @@ GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f
 # full-size launches (profiles/k_gemm__bench_launches_dram.md), keyed by a
 # hash of the kernel source; when the source has changed since, traffic is null.
 GEMM_DRAM_TRAFFIC = {
-    "a5f3721a1133bca0": {"linear_dw_gemm": 259453440, "moe_fwd_gemm": 1496931584,
-                         "moe_dx_gemm": 1530479872, "moe_dw_gemm": 2234756608},
+    "ccce64a8ef498586": {"linear_dw_gemm": 260368384, "moe_fwd_gemm": 1499354368,
+                         "moe_dx_gemm": 1531265280, "moe_dw_gemm": 2234426368},
 }
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
@@ -460,9 +460,14 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=5, help="oracle sample steps for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--quant-sweep", action="store_true",
+                    help="instead of the step: dual-axis MXFP8 quant bandwidth over sizes (one JSON line each)")
     args = ap.parse_args()
     world, rank, local = dist_init()
 
+    if args.quant_sweep:
+        quant_sweep()
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
@@ -539,6 +544,37 @@ def main():
         line["cpu_baseline"]["value"] = float(f"{line['cpu_baseline']['value']:.4g}")
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def quant_sweep():
+    """Dual-axis MXFP8 quant of bf16 [R x C], C in {2048, 7168, 14336},
+    R = ceil128(2^p / C) for p = 20, 22, ..., 30; algorithmic bytes 2 in +
+    2 (1 + 1/32) out per element; L2 flushed before each timed launch."""
+    import mxq_inputs
+    import mx_block_scaled_mxq_gb300 as m
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    m.load()
+    peaks, peak_kind = read_peaks()
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for C in (2048, 7168, 14336):
+        for p in range(20, 31, 2):
+            R = ((1 << p) // C + 127) // 128 * 128
+            x = mxq_inputs.sweep_bf16_device(R, C, seed=p * 100 + C, device=dev)
+            q, s, qT, sT = (torch.empty(R * C, dtype=torch.uint8, device=dev),
+                            torch.empty(m.mxq_scale_bytes(R, C // 32), dtype=torch.uint8, device=dev),
+                            torch.empty(R * C, dtype=torch.uint8, device=dev),
+                            torch.empty(m.mxq_scale_bytes(C, R // 32), dtype=torch.uint8, device=dev))
+            fn = lambda: m.mxq_quantize(x, m.BF16, R, C, C, -1, m.E4M3, 1, q, s, qT, sT)  # noqa: E731
+            fn()
+            ms = time_flushed(fn, 5, flush)
+            gbs = R * C * 4.0625 / (ms / 1e3) / 1e9
+            print(json.dumps({"sweep": "mxfp8_dual_quant", "rows": R, "cols": C, "elements": R * C,
+                              "ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 3),
+                              "peak": f"{hbm} GB/s ({peak_kind} HBM copy)"}), flush=True)
+            del x, q, s, qT, sT
+    assert m.mxq_poll_device_error() == 0
 
 
 def component_timings(wl, world):

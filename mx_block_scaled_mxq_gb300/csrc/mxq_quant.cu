@@ -852,8 +852,10 @@ cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, i
 namespace {
 
 // Persistent TMA-staged launch of the column quant; returns false (no launch)
-// when the input cannot be described by a tensor map (unaligned base or row
-// stride, or coordinates past 2^31), so the caller falls back.
+// when the input cannot be described by a tensor map -- no rows at all (a
+// per-group quant whose groups are all empty writes only padding), or an
+// unaligned base or row stride, which the C entry points reject before they
+// get here -- so the caller runs the one-tile-per-CTA kernel.
 template <bool ROWS, bool GROUPED>
 bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cudaError_t *res) {
     if ((reinterpret_cast<uintptr_t>(P.x) & 15) || (P.ldx % 8) || P.C >= (1ll << 31) || P.R >= (1ll << 31) ||

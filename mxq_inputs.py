@@ -106,3 +106,20 @@ def mxfp4_large(rows: int = 4096, cols: int = 4096, seed: int = 0) -> np.ndarray
 def sweep_bf16(R: int, C: int, seed: int = 0) -> torch.Tensor:
     """bf16 0.1*StudentT(3) with 1% outliers x1000 (dual-quant bandwidth sweep)."""
     return _bf16(heavy_tail((R, C), 1000.0, seed))
+
+
+def sweep_bf16_device(R: int, C: int, seed: int, device) -> torch.Tensor:
+    """The sweep_bf16 distribution drawn on the device (seeded torch generator)
+    for the sweep's largest sizes (up to 2^30 elements): 0.1 * Z / sqrt(V/3)
+    with Z ~ N(0,1) and V a sum of 3 squared normals (StudentT(3)), entries
+    multiplied by 1000 with probability 0.01, rounded to bf16."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    z = torch.randn((R, C), generator=g, device=device)
+    v = torch.zeros((R, C), device=device)
+    for _ in range(3):
+        v.add_(torch.randn((R, C), generator=g, device=device).square_())
+    t = z.mul_(0.1).div_(v.div_(3.0).sqrt_())
+    del v
+    out = torch.where(torch.rand((R, C), generator=g, device=device) < 0.01, t * 1000.0, t)
+    return out.to(torch.bfloat16)

@@ -154,3 +154,31 @@ def test_full_size_moe_sampled(mxq):
         check_close(dw[e], oracle.gemm_ref(a, sa, b, sb))
     for e in np.nonzero(n == 0)[0]:
         assert not torch.any(dw[int(e)].float() != 0)
+
+
+def test_grouped_many_experts_decode_without_tables(mxq):
+    """300 experts: more than the kernel keeps in its shared-memory group tables,
+    so tiles are decoded from the device offsets (and the per-group column
+    quant scans 300 groups)."""
+    E, T, K, N = 300, 1200, 64, 128
+    sizes = mxq_inputs.dirichlet_group_sizes(E, T, alpha=0.5, seed=3)
+    assert (sizes == 0).any() and (sizes > 0).sum() > 100
+    off, x, w, dy = mxq_inputs.moe_inputs(E, T, K, N, seed=5, sizes=sizes)
+    moe = MoE(mxq, off, x, w, dy)
+    y, dx, dw = moe.fwd(), moe.dx(), moe.dw()
+    torch.cuda.synchronize()
+    assert mxq.mxq_poll_device_error() == 0
+    qx, sx = oracle.mxfp8_quant_rows(x)
+    qw, sw, qwT, swT = _oracle_w(w)
+    qdy, sdy = oracle.mxfp8_quant_rows(dy)
+    check_close(y, oracle.grouped_fwd_ref(qx, sx, qw, sw, off))
+    check_close(dx, oracle.grouped_fwd_ref(qdy, sdy, qwT, swT, off))
+    qdyT, sdyT = oracle.mxfp8_quant_cols_grouped(dy, off)
+    qxT, sxT = oracle.mxfp8_quant_cols_grouped(x, off)
+    ref_dw = oracle.grouped_dw_ref(qdyT, sdyT, qxT, sxT, off)
+    got_dw = dw.float().cpu().numpy()
+    for e in range(E):
+        if sizes[e] == 0:
+            assert not np.any(got_dw[e])
+        else:
+            check_close(dw[e], ref_dw[e])

@@ -149,3 +149,37 @@ def test_full_size_linear_operands_dual_quant(mxq):
         assert np.array_equal(qT.cpu().numpy(), oqT)
         assert np.array_equal(sT.cpu().numpy(), oracle.swizzle_scales(osT))
         del q, s, qT, sT
+
+
+@pytest.mark.parametrize("R,C,pad,shift", [(256, 64, 8, 0), (130, 96, 16, 8), (64, 128, 8, 24)])
+def test_dual_quant_strided_views(mxq, R, C, pad, shift):
+    """A row stride larger than the row (ldx = C + pad + shift elements) and a
+    base 16-byte aligned but not tile aligned (shift elements in): the staged
+    tiles follow the stride, so codes and scales are those of the contiguous
+    tensor."""
+    x = _inputs(R, C, "heavy", seed=R + C + pad)
+    wide = torch.zeros((R, C + pad + shift), dtype=torch.bfloat16)
+    wide[:, shift:shift + C] = x
+    view = wide.to(DEV)[:, shift:shift + C]
+    assert view.stride(0) == C + pad + shift
+    q, s, qT, sT = mxq.quantize_mxfp8(view, dual=True)
+    oq, os_ = oracle.mxfp8_quant_rows(x)
+    oqT, osT = oracle.mxfp8_quant_cols(x)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
+    assert np.array_equal(qT.cpu().numpy(), oqT)
+    assert np.array_equal(sT.cpu().numpy(), oracle.swizzle_scales(osT))
+
+
+def test_grouped_col_quant_with_no_rows_writes_zero_padding(mxq):
+    """Every group empty (T = 0): each byte of the t_pad-wide outputs is padding
+    and must be written as 0 (the codes and the E8M0 scale bytes)."""
+    E, C = 3, 64
+    t_pad = mxq.mxq_grouped_padded_rows(0, E)
+    assert t_pad == 128 * E
+    d_off = torch.zeros(E + 1, dtype=torch.int64, device=DEV)
+    qT = torch.full((C, t_pad), 0xFF, dtype=torch.uint8, device=DEV)
+    sT = torch.full((mxq.mxq_scale_bytes(C, t_pad // 32),), 0xFF, dtype=torch.uint8, device=DEV)
+    mxq.mxq_quantize_grouped_col(None, 0, C, d_off, E, t_pad, qT, sT)
+    torch.cuda.synchronize()
+    assert not qT.any() and not sT.any()
