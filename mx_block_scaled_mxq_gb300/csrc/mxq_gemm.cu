@@ -401,6 +401,41 @@ __device__ __forceinline__ bool mma4_commit_peek(uint32_t d_tmem, const uint64_t
     return ready != 0;
 }
 
+// One whole k-block of the single-CTA bf16 path (kind::f16, no scales) in one
+// asm block: the next stage's barrier test first, then the four K = 16 MMAs
+// and the commit; the test result is read last.
+__device__ __forceinline__ bool kblock_bf16_cg1(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t accumulate,
+                                                uint32_t bar_empty_s, uint32_t bar_full_next, uint32_t parity_next) {
+    constexpr uint32_t kAbHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+    constexpr uint32_t kId = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                             (static_cast<uint32_t>(128 >> 4) << 24);
+    uint32_t ready;
+    asm volatile(
+        "{\n\t.reg .pred pn, pa, p1;\n\t.reg .b64 da, db;\n\t.reg .b32 ta, tb;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n\t"
+        "setp.ne.b32 pa, %3, 0;\n\t"
+        "setp.eq.u32 p1, 0, 0;\n\t"
+        "mov.b64 da, {%5, %8};\n\t"
+        "mov.b64 db, {%6, %8};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%4], da, db, %9, pa;\n\t"
+        "add.u32 ta, %5, 2;\n\t" "add.u32 tb, %6, 2;\n\t"
+        "mov.b64 da, {ta, %8};\n\t" "mov.b64 db, {tb, %8};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%4], da, db, %9, p1;\n\t"
+        "add.u32 ta, %5, 4;\n\t" "add.u32 tb, %6, 4;\n\t"
+        "mov.b64 da, {ta, %8};\n\t" "mov.b64 db, {tb, %8};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%4], da, db, %9, p1;\n\t"
+        "add.u32 ta, %5, 6;\n\t" "add.u32 tb, %6, 6;\n\t"
+        "mov.b64 da, {ta, %8};\n\t" "mov.b64 db, {tb, %8};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%4], da, db, %9, p1;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+        "selp.u32 %0, 1, 0, pn;\n\t}"
+        : "=r"(ready)
+        : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(bar_empty_s),
+          "n"(kAbHi), "n"(kId)
+        : "memory");
+    return ready != 0;
+}
+
 // One whole k-block of the single-CTA block-scaled path in one asm block:
 // the non-blocking test of the NEXT stage's full barrier is issued first, then
 // the three scale-tile copies (A, B rows 0-127, B rows 128-255) into TMEM, the
@@ -479,7 +514,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // tile t - 2 has been drained from bank b and the epilogue has read the first
     // 64 columns of tile t - 1 (which also means tile t - 1's MMAs are done), so
     // the next tile's MMAs overlap most of the previous tile's drain.
-    constexpr bool DB = CG == 1 && KIND == kMXF8;
+    constexpr bool DB = CG == 1;  // bf16 tiles use the banks too (they keep no scales)
     const uint32_t bar_accf1 = bar_accf + 24, bar_acce1 = bar_accf + 32;
     const uint32_t bar_headf0 = bar_accf + 40, bar_headf1 = bar_accf + 48;
     uint32_t rank = 0;
@@ -643,7 +678,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_after();
                     bool ready = false;  // stage g known to have landed (from the previous stage's peek)
                     int kb0 = 0;         // first k-block left to the general loop below
-                    if constexpr (CG == 1 && KIND == kMXF8) {
+                    if constexpr (CG == 1) {
                         // every k-block but a short last one: one asm block each
                         const int nfull = ti.k_last == 4 ? ti.nkb : ti.nkb - 1;
                         for (; kb0 < nfull; kb0++, g++) {
@@ -655,11 +690,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                             tc_fence_after();
                             issued_any = true;
                             const uint32_t s1 = (g + 1) % STAGES, ph1 = ((g + 1) / STAGES) & 1;
-                            const uint32_t sf_t = sf_base + s * SF_STRIDE;
-                            ready = kblock_mxf8_cg1(d_tmem, a_lo0 + s * (C::A_BYTES >> 4), b_lo0 + s * (C::B_BYTES >> 4),
-                                                    sf_t, sf_t + 4, sa_lo0 + s * (C::SFA_BYTES >> 4),
-                                                    sb_lo0 + s * (C::SFB_BYTES >> 4), kb0 != 0 ? 1u : 0u,
-                                                    bar_empty + 8 * s, bar_full + 8 * s1, ph1);
+                            if constexpr (KIND == kBF16) {
+                                ready = kblock_bf16_cg1(d_tmem, a_lo0 + s * (C::A_BYTES >> 4),
+                                                        b_lo0 + s * (C::B_BYTES >> 4), kb0 != 0 ? 1u : 0u,
+                                                        bar_empty + 8 * s, bar_full + 8 * s1, ph1);
+                            } else {
+                                const uint32_t sf_t = sf_base + s * SF_STRIDE;
+                                ready = kblock_mxf8_cg1(d_tmem, a_lo0 + s * (C::A_BYTES >> 4),
+                                                        b_lo0 + s * (C::B_BYTES >> 4), sf_t, sf_t + 4,
+                                                        sa_lo0 + s * (C::SFA_BYTES >> 4),
+                                                        sb_lo0 + s * (C::SFB_BYTES >> 4), kb0 != 0 ? 1u : 0u,
+                                                        bar_empty + 8 * s, bar_full + 8 * s1, ph1);
+                            }
                         }
                     }
                     for (int kb = kb0; kb < ti.nkb && !stop; kb++, g++) {
