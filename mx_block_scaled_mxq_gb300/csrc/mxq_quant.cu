@@ -38,12 +38,6 @@ __device__ __forceinline__ void stg_v4(void *p, uint4 v) {
                  : "memory");
 }
 
-// Two fp32 values -> two E4M3 codes (lo in the low byte), RNE + satfinite.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
 // Four fp32 values -> four E4M3 codes (a in the low byte); the two halves are
 // packed by register pairing.
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
@@ -69,8 +63,16 @@ __device__ __forceinline__ int mx8_exp_from_bf16(uint32_t a) {
     return max(fl - 8, -127);  // fl <= 127 so X <= 119
 }
 __device__ __forceinline__ uint8_t mx8_scale_byte(int X) { return X > 127 ? 0xFF : static_cast<uint8_t>(X + 127); }
-// 2^-X as fp32 (a normal number for X in [-127, 119]).
-__device__ __forceinline__ float pow2_neg(int X) { return __uint_as_float(static_cast<uint32_t>(127 - X) << 23); }
+// 2^-X as a bf16 bit pattern (normal for X in [-127, 119]).
+__device__ __forceinline__ uint32_t pow2_neg_bf16(int X) { return static_cast<uint32_t>(127 - X) << 7; }
+// Two bf16 products in one instruction.  x * 2^-X is exact in bf16 whenever
+// it is at least 2^-126; smaller products round to E4M3 zero either way, so
+// the codes equal those of the exact product.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
 
 // E4M3 codes of 8 bf16 (4 packed words, element 2k in the low half of word k).
 __device__ __forceinline__ uint2 e4m3_codes8(const uint32_t (&w)[4], int X) {
@@ -86,9 +88,11 @@ __device__ __forceinline__ uint2 e4m3_codes8(const uint32_t (&w)[4], int X) {
         out.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
         return out;
     }
-    const float inv = pow2_neg(X);
-    out.x = e4m3x4(bf16lo(w[0]) * inv, bf16hi(w[0]) * inv, bf16lo(w[1]) * inv, bf16hi(w[1]) * inv);
-    out.y = e4m3x4(bf16lo(w[2]) * inv, bf16hi(w[2]) * inv, bf16lo(w[3]) * inv, bf16hi(w[3]) * inv);
+    const uint32_t inv2 = pow2_neg_bf16(X) * 0x00010001u;
+    const uint32_t s0 = mul_bf16x2(w[0], inv2), s1 = mul_bf16x2(w[1], inv2);
+    const uint32_t s2 = mul_bf16x2(w[2], inv2), s3 = mul_bf16x2(w[3], inv2);
+    out.x = e4m3x4(bf16lo(s0), bf16hi(s0), bf16lo(s1), bf16hi(s1));
+    out.y = e4m3x4(bf16lo(s2), bf16hi(s2), bf16lo(s3), bf16hi(s3));
     return out;
 }
 
@@ -386,12 +390,14 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
         const int64_t gcol = c0 + cl;
         if (gcol < P.C) {
             uint32_t lo[8], hi[8];
-            const float ilo = pow2_neg(Xlo > 127 ? 0 : Xlo), ihi = pow2_neg(Xhi > 127 ? 0 : Xhi);
+            // column 2p's scale in the low half, column 2p + 1's in the high half
+            const uint32_t inv2 = pow2_neg_bf16(Xlo > 127 ? 0 : Xlo) | (pow2_neg_bf16(Xhi > 127 ? 0 : Xhi) << 16);
 #pragma unroll
             for (int k = 0; k < 8; k++) {
-                const uint32_t a0 = col[4 * k], a1 = col[4 * k + 1], a2 = col[4 * k + 2], a3 = col[4 * k + 3];
-                lo[k] = e4m3x4(bf16lo(a0) * ilo, bf16lo(a1) * ilo, bf16lo(a2) * ilo, bf16lo(a3) * ilo);
-                hi[k] = e4m3x4(bf16hi(a0) * ihi, bf16hi(a1) * ihi, bf16hi(a2) * ihi, bf16hi(a3) * ihi);
+                const uint32_t a0 = mul_bf16x2(col[4 * k], inv2), a1 = mul_bf16x2(col[4 * k + 1], inv2);
+                const uint32_t a2 = mul_bf16x2(col[4 * k + 2], inv2), a3 = mul_bf16x2(col[4 * k + 3], inv2);
+                lo[k] = e4m3x4(bf16lo(a0), bf16lo(a1), bf16lo(a2), bf16lo(a3));
+                hi[k] = e4m3x4(bf16hi(a0), bf16hi(a1), bf16hi(a2), bf16hi(a3));
             }
             if (Xlo > 127 || Xhi > 127) {  // non-finite blocks: NaN codes with the sign kept
 #pragma unroll
@@ -589,12 +595,14 @@ __global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_con
             const int64_t gcol = c0 + cl;
             if (gcol < P.C) {
                 uint32_t lo[8], hi[8];
-                const float ilo = pow2_neg(Xlo > 127 ? 0 : Xlo), ihi = pow2_neg(Xhi > 127 ? 0 : Xhi);
+                // column 2p's scale in the low half, column 2p + 1's in the high half
+                const uint32_t inv2 = pow2_neg_bf16(Xlo > 127 ? 0 : Xlo) | (pow2_neg_bf16(Xhi > 127 ? 0 : Xhi) << 16);
 #pragma unroll
                 for (int q = 0; q < 8; q++) {
-                    const uint32_t a0 = col[4 * q], a1 = col[4 * q + 1], a2 = col[4 * q + 2], a3 = col[4 * q + 3];
-                    lo[q] = e4m3x4(bf16lo(a0) * ilo, bf16lo(a1) * ilo, bf16lo(a2) * ilo, bf16lo(a3) * ilo);
-                    hi[q] = e4m3x4(bf16hi(a0) * ihi, bf16hi(a1) * ihi, bf16hi(a2) * ihi, bf16hi(a3) * ihi);
+                    const uint32_t a0 = mul_bf16x2(col[4 * q], inv2), a1 = mul_bf16x2(col[4 * q + 1], inv2);
+                    const uint32_t a2 = mul_bf16x2(col[4 * q + 2], inv2), a3 = mul_bf16x2(col[4 * q + 3], inv2);
+                    lo[q] = e4m3x4(bf16lo(a0), bf16lo(a1), bf16lo(a2), bf16lo(a3));
+                    hi[q] = e4m3x4(bf16hi(a0), bf16hi(a1), bf16hi(a2), bf16hi(a3));
                 }
                 if (Xlo > 127 || Xhi > 127) {  // non-finite blocks: NaN codes with the sign kept
 #pragma unroll

@@ -183,3 +183,24 @@ def test_grouped_col_quant_with_no_rows_writes_zero_padding(mxq):
     mxq.mxq_quantize_grouped_col(None, 0, C, d_off, E, t_pad, qT, sT)
     torch.cuda.synchronize()
     assert not qT.any() and not sT.any()
+
+
+def test_every_bf16_pattern_alone_in_a_block(mxq):
+    """Each of the 65,536 bf16 bit patterns (zeros, subnormals, normals, Inf,
+    NaN) as the only nonzero element of its 32-element block, in both the row
+    and the column direction: codes and scales bit for bit."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = np.zeros((65536, 32), dtype=np.uint16)
+    x[:, 7] = bits
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    q, s, _, _ = mxq.quantize_mxfp8(xt.to(DEV))
+    oq, os_ = oracle.mxfp8_quant_rows(x)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
+    # column direction: the transpose, column j holding pattern j alone
+    xc = np.ascontiguousarray(x.T)
+    xc_t = torch.from_numpy(xc.view(np.int16)).view(torch.bfloat16)
+    _, _, qT, sT = mxq.quantize_mxfp8(xc_t.to(DEV), axis=-2)
+    oqT, osT = oracle.mxfp8_quant_cols(xc)
+    assert np.array_equal(qT.cpu().numpy(), oqT)
+    assert np.array_equal(sT.cpu().numpy(), oracle.swizzle_scales(osT))
