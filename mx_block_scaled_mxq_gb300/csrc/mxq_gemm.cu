@@ -35,7 +35,8 @@
 // deeper ring hides more load latency.  Each CTA holds its own rows' A scales
 // and all of B's scales; every load of both CTAs completes on the even CTA's
 // stage barrier.
-// TMEM: columns [0, 256) accumulator; [256 + 16 s, +12) scale slots of stage s
+// TMEM: two accumulator banks of 256 columns; a tile in one bank keeps the
+// scale slots of stage s in columns [16 s, 16 s + 12) of the other bank
 // (A: 4 columns, B: 2 x 4 columns).  Every wait is bounded (mxq_device.cuh).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -55,7 +56,7 @@ __device__ unsigned int g_device_error = 0;
 namespace {
 
 constexpr int BN = 256, BK = 128, THREADS = 192;
-constexpr uint32_t TMEM_COLS = 512, SF_COL0 = 256, SF_STRIDE = 16;
+constexpr uint32_t TMEM_COLS = 512, SF_STRIDE = 16;
 constexpr int kMaxTableE = 256;  // experts whose group tables are kept in shared memory
 // Epilogue stores: true = 32 x 32 blocks staged in shared memory and written
 // by TMA stores; false = coalesced 16-byte global stores after an in-register
@@ -75,17 +76,15 @@ struct Cfg {
     static constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-    // full / empty per stage; accumulator full / empty / drain; single-CTA
-    // tiles add the second accumulator bank's full / empty and both banks'
-    // "head drained" barriers
-    static constexpr uint32_t NUM_BARS = 2 * STAGES + (CG == 1 ? 7 : 3);
-    static constexpr uint32_t OFF_MISC = OFF_BAR + 128;
+    // full / empty per stage; accumulator full / empty / drain, the second
+    // accumulator bank's full / empty and both banks' "head drained" barriers
+    static constexpr uint32_t NUM_BARS = 2 * STAGES + 7;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + 256;
     static constexpr uint32_t OFF_GRP = OFF_MISC + 256;  // group tables (grouped modes, E <= kMaxTableE)
     // epilogue store staging: 4 warps x 2 slots x (32 rows x 64 bytes), 1024-aligned
     static constexpr uint32_t OFF_STORE = (OFF_GRP + 2 * 8 * (kMaxTableE + 1) + 1023) / 1024 * 1024;
     static constexpr uint32_t SMEM_ALLOC = OFF_STORE + 4 * 2 * 2048 + 1024;  // + slack to align the base
-    static_assert(NUM_BARS * 8 <= 128, "barrier area");
-    static_assert(SF_COL0 + STAGES * SF_STRIDE <= TMEM_COLS, "tmem budget");
+    static_assert(NUM_BARS * 8 <= 256, "barrier area");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -499,6 +498,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const __grid_constant__ CUtensorMap tmC, const Params p) {
     using C = Cfg<CG>;
     constexpr int STAGES = C::STAGES;
+    // the epilogue's 64-column quarter after which the scale-slot columns are read
+    constexpr int kHeadQuarter = (STAGES * SF_STRIDE - 1) / 64;
+    static_assert(kHeadQuarter < 4, "scale slots fit in one bank");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -508,13 +510,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bar_full = sbase + C::OFF_BAR, bar_empty = bar_full + 8 * STAGES;
     const uint32_t bar_accf = bar_full + 16 * STAGES, bar_acce = bar_accf + 8, bar_drain = bar_accf + 16;
-    // Two accumulator banks (single-CTA block-scaled tiles): tile t accumulates in
-    // TMEM columns [256 b, 256 b + 256), b = t % 2, and keeps its scale slots in
-    // the first 64 columns of the other bank.  The MMA warp starts tile t once
-    // tile t - 2 has been drained from bank b and the epilogue has read the first
-    // 64 columns of tile t - 1 (which also means tile t - 1's MMAs are done), so
-    // the next tile's MMAs overlap most of the previous tile's drain.
-    constexpr bool DB = CG == 1;  // bf16 tiles use the banks too (they keep no scales)
+    // Two accumulator banks: tile t accumulates in TMEM columns [256 b, 256 b +
+    // 256), b = t % 2, and keeps its scale slots in the first STAGES * 16 columns
+    // of the other bank.  The MMA warp starts tile t once tile t - 2 has been
+    // drained from bank b and the epilogue has read the head of tile t - 1 (the
+    // columns that hold tile t's scale slots; this also means tile t - 1's MMAs
+    // are done), so the next tile's MMAs overlap most of the previous tile's
+    // drain.  For a CTA pair the bank's release and "head read" barriers live in
+    // the even CTA and count the epilogue warps of both CTAs.
     const uint32_t bar_accf1 = bar_accf + 24, bar_acce1 = bar_accf + 32;
     const uint32_t bar_headf0 = bar_accf + 40, bar_headf1 = bar_accf + 48;
     uint32_t rank = 0;
@@ -546,14 +549,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_init(bar_empty + 8 * s, 1);
             }
             mbar_init(bar_accf, 1);
-            mbar_init(bar_acce, 4 * CG);  // one arrival per epilogue warp (of both CTAs)
+            mbar_init(bar_accf1, 1);
+            // one arrival per epilogue warp (of both CTAs of a pair)
+            mbar_init(bar_acce, 4 * CG);
+            mbar_init(bar_acce1, 4 * CG);
+            mbar_init(bar_headf0, 4 * CG);
+            mbar_init(bar_headf1, 4 * CG);
             mbar_init(bar_drain, 1);
-            if constexpr (DB) {
-                mbar_init(bar_accf1, 1);
-                mbar_init(bar_acce1, 4);
-                mbar_init(bar_headf0, 4);
-                mbar_init(bar_headf1, 4);
-            }
             fence_mbar_init();
         }
         __syncwarp();
@@ -577,11 +579,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         gt.off = off;
         gt.pre = pre;
     }
-    // stage barriers and the accumulator-release barrier of the even CTA
-    uint32_t lead_full = bar_full, lead_acce = bar_acce;
+    // stage barriers and the accumulator-release barriers of the even CTA
+    uint32_t lead_full = bar_full, lead_acce = bar_acce, lead_headf0 = bar_headf0;
     if constexpr (CG == 2) {
         lead_full = mapa_shared(bar_full, 0);
         lead_acce = mapa_shared(bar_acce, 0);
+        lead_headf0 = mapa_shared(bar_headf0, 0);
     }
     const bool run = *abort_flag == 0;
 
@@ -658,23 +661,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (ti.nkb == 0) continue;  // empty group: the epilogue writes zeros
                 int stop = 0;
                 // accumulator bank and scale-slot base of this tile
-                const uint32_t bank = DB ? (acc_it & 1) : 0;
+                const uint32_t bank = acc_it & 1;
                 const uint32_t d_tmem = tmem + 256 * bank;
-                const uint32_t sf_base = DB ? tmem + 256 * (1 - bank) : tmem + SF_COL0;
+                const uint32_t sf_base = tmem + 256 * (1 - bank);
                 if (lane == 0) {
-                    if constexpr (DB) {
-                        // bank drained of tile t - 2; head of tile t - 1 drained
-                        if (acc_it >= 2 && !mbar_wait(bank ? bar_acce1 : bar_acce, ((acc_it - 2) >> 1) & 1, abort_flag,
-                                                      &g_device_error))
-                            stop = 1;
-                        if (!stop && acc_it >= 1 &&
-                            !mbar_wait(bank ? bar_headf0 : bar_headf1, ((acc_it - 1) >> 1) & 1, abort_flag,
-                                       &g_device_error))
-                            stop = 1;
-                    } else {
-                        // the epilogue must have drained the previous accumulator
-                        if (acc_it > 0 && !mbar_wait(bar_acce, (acc_it - 1) & 1, abort_flag, &g_device_error)) stop = 1;
-                    }
+                    // bank drained of tile t - 2; head of tile t - 1 drained
+                    if (acc_it >= 2 && !mbar_wait(bank ? bar_acce1 : bar_acce, ((acc_it - 2) >> 1) & 1, abort_flag,
+                                                  &g_device_error))
+                        stop = 1;
+                    if (!stop && acc_it >= 1 &&
+                        !mbar_wait(bank ? bar_headf0 : bar_headf1, ((acc_it - 1) >> 1) & 1, abort_flag, &g_device_error))
+                        stop = 1;
                     tc_fence_after();
                     bool ready = false;  // stage g known to have landed (from the previous stage's peek)
                     int kb0 = 0;         // first k-block left to the general loop below
@@ -757,8 +754,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ready = false;
                     }
                     if (!stop) {
-                        if constexpr (CG == 2) tc_commit_pair_mc(bar_accf, 3);
-                        else tc_commit(DB && bank ? bar_accf1 : bar_accf);
+                        if constexpr (CG == 2) tc_commit_pair_mc(bank ? bar_accf1 : bar_accf, 3);
+                        else tc_commit(bank ? bar_accf1 : bar_accf);
                     }
                 }
                 acc_it++;
@@ -792,10 +789,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 continue;
             }
-            const uint32_t bank = DB ? (acc_it & 1) : 0;
-            if (!mbar_wait(DB && bank ? bar_accf1 : bar_accf, DB ? ((acc_it >> 1) & 1) : (acc_it & 1), abort_flag,
-                           &g_device_error))
-                break;
+            const uint32_t bank = acc_it & 1;
+            if (!mbar_wait(bank ? bar_accf1 : bar_accf, (acc_it >> 1) & 1, abort_flag, &g_device_error)) break;
             tc_fence_after();
             const uint32_t acc_t = tmem + 256 * bank;
             // four quarters of 2 x 32 columns: two TMEM loads in flight per wait
@@ -810,10 +805,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tmem_ld_32x32b_x32(acc_t + (static_cast<uint32_t>(32 * sub) << 16) + 32 * ch, r[q]);
                 }
                 tc_wait_ld();
-                if (DB && h == 0) {  // columns 0-63 read: the next tile may put its scales there
+                if (h == kHeadQuarter) {  // head read: the next tile may put its scales there
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bank ? bar_headf1 : bar_headf0);
+                    if (lane == 0) {
+                        if constexpr (CG == 2) mbar_arrive_cluster(lead_headf0 + 8 * bank);
+                        else mbar_arrive(bar_headf0 + 8 * bank);
+                    }
                 }
 #pragma unroll
                 for (int q = 0; q < 2; q++) {
@@ -830,8 +828,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if constexpr (CG == 2) mbar_arrive_cluster(lead_acce);
-                else mbar_arrive(DB && bank ? bar_acce1 : bar_acce);
+                if constexpr (CG == 2) mbar_arrive_cluster(bank ? lead_acce + 24 : lead_acce);
+                else mbar_arrive(bank ? bar_acce1 : bar_acce);
             }
             acc_it++;
             // TMA stores take whole 32-row boxes: this warp's rows must all belong
