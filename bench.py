@@ -52,8 +52,8 @@ GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f
 # full-size launches (profiles/k_gemm__bench_launches_dram.md), keyed by a
 # hash of the kernel source; when the source has changed since, traffic is null.
 GEMM_DRAM_TRAFFIC = {
-    "ccce64a8ef498586": {"linear_dw_gemm": 260368384, "moe_fwd_gemm": 1499354368,
-                         "moe_dx_gemm": 1531265280, "moe_dw_gemm": 2234426368},
+    "3beaad66eca8b7ca": {"linear_dw_gemm": 259180032, "moe_fwd_gemm": 1493929472,
+                         "moe_dx_gemm": 1531132672, "moe_dw_gemm": 2234405376},
 }
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
