@@ -186,7 +186,7 @@ class Workload:
     # kernel launches per step (counted from the entry points called below)
     def launches(self) -> int:
         lin = 6 if self.mode == self.m.SAVE_QUANT else 8
-        return lin + 8 + 2
+        return lin + 6 + 2
 
     def step(self, ev=None):
         """One pass; `ev` (a list) receives (name, start, end, flop) event pairs
@@ -214,11 +214,12 @@ class Workload:
             timed("linear_dw_gemm", 2 * M * N * K, dw_call)   # saved-quant dW launches the GEMM only
         else:
             dw_call()
-        m.mxq_quantize(self.xm, m.BF16, T, Km, Km, -1, m.E4M3, 0, self.xmq, self.xms, None, None)
+        # X and dY: row quant (fwd / dX operands) and per-group column quant (dW
+        # operands) from one read each; W: row quant and column quant along N
+        m.mxq_quantize_grouped_dual(self.xm, T, Km, self.off, E, self.t_pad, self.xmq, self.xms, self.xmqT, self.xmsT)
         m.mxq_quantize(self.wm, m.BF16, E * Nm, Km, Km, -1, m.E4M3, 1, self.wmq, self.wms, self.wmqT, self.wmsT)
-        m.mxq_quantize(self.dym, m.BF16, T, Nm, Nm, -1, m.E4M3, 0, self.dymq, self.dyms, None, None)
-        m.mxq_quantize_grouped_col(self.dym, T, Nm, self.off, E, self.t_pad, self.dymqT, self.dymsT)
-        m.mxq_quantize_grouped_col(self.xm, T, Km, self.off, E, self.t_pad, self.xmqT, self.xmsT)
+        m.mxq_quantize_grouped_dual(self.dym, T, Nm, self.off, E, self.t_pad, self.dymq, self.dyms, self.dymqT,
+                                    self.dymsT)
         gf = 2 * T * Nm * Km
         timed("moe_fwd_gemm", gf, lambda: m.mxq_grouped_gemm(m.GG_FWD, self.xmq, self.xms, self.wmq, self.wms,
                                                              self.off, E, T, Nm, Km, 0, self.ym))
@@ -610,6 +611,8 @@ def component_timings(wl, world):
         "dual_quant_dY": lambda: m.mxq_quantize(wl.dy, m.BF16, M, N, N, -1, m.E4M3, 1, dq, ds, dqT, dsT),
         "moe_grouped_col_quant_X": lambda: m.mxq_quantize_grouped_col(wl.xm, T, Km, wl.off, E, wl.t_pad, wl.xmqT,
                                                                       wl.xmsT),
+        "moe_grouped_dual_quant_X": lambda: m.mxq_quantize_grouped_dual(wl.xm, T, Km, wl.off, E, wl.t_pad, wl.xmq,
+                                                                        wl.xms, wl.xmqT, wl.xmsT),
         "moe_fwd": lambda: m.mxq_grouped_gemm(m.GG_FWD, wl.xmq, wl.xms, wl.wmq, wl.wms, wl.off, E, T, Nm, Km, 0, wl.ym),
         "mxfp4_qdq": lambda: m.mxq_qdq_mxfp4(wl.a4, wl.y4, R4, C4, 32, 6.0),
         "mxfp4_ste_fwd": lambda: m.mxq_mxfp4_ste_forward(wl.a4, wl.y4, m4, R4, C4, 32, 6.0),
@@ -635,6 +638,8 @@ def component_timings(wl, world):
     tp = wl.t_pad
     gcol_bytes = T * Km * 2 + Km * tp * (1 + 1 / 32)
     out["moe_grouped_col_quant_X_gbs"] = round(gcol_bytes / (out["moe_grouped_col_quant_X_ms"] / 1e3) / 1e9, 1)
+    gdual_bytes = gcol_bytes + T * Km * (1 + 1 / 32)
+    out["moe_grouped_dual_quant_X_gbs"] = round(gdual_bytes / (out["moe_grouped_dual_quant_X_ms"] / 1e3) / 1e9, 1)
     out["mxfp4_qdq_gbs"] = round(R4 * C4 * 8 / (out["mxfp4_qdq_ms"] / 1e3) / 1e9, 1)
     # clipped STE: 4 B in + 4 B out + 1/8 B of mask per element, both directions
     out["mxfp4_ste_fwd_gbs"] = round(R4 * C4 * 8.125 / (out["mxfp4_ste_fwd_ms"] / 1e3) / 1e9, 1)

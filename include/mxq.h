@@ -127,6 +127,23 @@ mxq_status mxq_quantize_grouped_col(const void *x_bf16, int64_t rows, int64_t co
                                     const int64_t *d_offsets, int E, int64_t t_pad,
                                     void *q_colT, void *s_colT, mxq_stream_t stream);
 
+/* Grouped dual-axis MXFP8 quant: the per-group column quant above and the
+ * plain row quant of the same x from one read of x, as the MoE layer needs
+ * them ([TT] MoE MXFP8 mode: the forward and input-gradient matmuls take the
+ * row quant of X and dY along the feature dim, the weight-gradient matmul
+ * their per-group column quant; [FB] for producing both axes in one pass).
+ *  q_row [rows x cols] u8 and s_row swz(rows, cols/32) are exactly what
+ *  mxq_quantize(x, MXQ_BF16, rows, cols, cols, -1, MXQ_E4M3, 0, ...) writes,
+ *  padding bytes included; q_colT/s_colT exactly what
+ *  mxq_quantize_grouped_col writes.  x is dense (leading dim cols).
+ *  q_row and s_row are both given (cols % 32 == 0) or both NULL (then this is
+ *  mxq_quantize_grouped_col).  Other arguments and errors as for
+ *  mxq_quantize_grouped_col. */
+mxq_status mxq_quantize_grouped_dual(const void *x_bf16, int64_t rows, int64_t cols,
+                                     const int64_t *d_offsets, int E, int64_t t_pad,
+                                     void *q_row, void *s_row, void *q_colT, void *s_colT,
+                                     mxq_stream_t stream);
+
 /* MXFP4 quant-dequant ([AMCT] sections 2, 3.2-3.3): fp32 x viewed as
  * [rows x cols] with cols the tensor's last dim; blocks of 32 along each row,
  * the last block of a row zero-padded (never spanning two rows);

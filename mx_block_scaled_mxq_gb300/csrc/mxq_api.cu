@@ -213,11 +213,14 @@ mxq_status mxq_quantize(const void *x, mxq_dtype dtype, int64_t rows, int64_t co
     return cuda_result(e, "mxq_quantize launch");
 }
 
-mxq_status mxq_quantize_grouped_col(const void *x_bf16, int64_t rows, int64_t cols, const int64_t *d_offsets, int E,
-                                    int64_t t_pad, void *q_colT, void *s_colT, mxq_stream_t stream) {
+mxq_status mxq_quantize_grouped_dual(const void *x_bf16, int64_t rows, int64_t cols, const int64_t *d_offsets,
+                                     int E, int64_t t_pad, void *q_row, void *s_row, void *q_colT, void *s_colT,
+                                     mxq_stream_t stream) {
     if (rows < 0 || cols < 0) return fail(MXQ_ERR_INVALID_ARG, "negative size");
     if (E < 1 || E > 4096) return fail(MXQ_ERR_INVALID_ARG, "E must be in [1, 4096]");
     if (cols % 8) return fail(MXQ_ERR_INVALID_ARG, "cols must be a multiple of 8");
+    const bool want_row = q_row != nullptr || s_row != nullptr;
+    if (want_row && cols % 32) return fail(MXQ_ERR_INVALID_ARG, "cols must be a multiple of 32 for the row quant");
     if (t_pad < 0 || t_pad % 128 || t_pad < mxq_grouped_padded_rows(rows, E))
         return fail(MXQ_ERR_INVALID_ARG, "t_pad must be a multiple of 128 and >= mxq_grouped_padded_rows(rows, E) = %lld",
                     (long long)mxq_grouped_padded_rows(rows, E));
@@ -227,13 +230,22 @@ mxq_status mxq_quantize_grouped_col(const void *x_bf16, int64_t rows, int64_t co
         return fail(MXQ_ERR_INVALID_ARG, "d_offsets must be a non-null 8-byte aligned device pointer");
     if ((rows > 0 && (!x_bf16 || !al16(x_bf16))) || !q_colT || !s_colT || !al16(q_colT) || !al16(s_colT))
         return fail(MXQ_ERR_INVALID_ARG, "tensor pointers must be non-null and 16-byte aligned");
+    if (want_row && (!q_row || !s_row || !al16(q_row) || !al16(s_row)))
+        return fail(MXQ_ERR_INVALID_ARG, "q_row/s_row must both be non-null and 16-byte aligned");
     mxq_status s = check_arch();
     if (s != MXQ_OK) return s;
     return cuda_result(mxq::launch_quant_cols_grouped(static_cast<const uint16_t *>(x_bf16), rows, cols, d_offsets, E,
-                                                      t_pad, static_cast<uint8_t *>(q_colT),
+                                                      t_pad, static_cast<uint8_t *>(q_row),
+                                                      static_cast<uint8_t *>(s_row), static_cast<uint8_t *>(q_colT),
                                                       static_cast<uint8_t *>(s_colT),
                                                       reinterpret_cast<cudaStream_t>(stream)),
-                       "mxq_quantize_grouped_col launch");
+                       "mxq_quantize_grouped_dual launch");
+}
+
+mxq_status mxq_quantize_grouped_col(const void *x_bf16, int64_t rows, int64_t cols, const int64_t *d_offsets, int E,
+                                    int64_t t_pad, void *q_colT, void *s_colT, mxq_stream_t stream) {
+    return mxq_quantize_grouped_dual(x_bf16, rows, cols, d_offsets, E, t_pad, nullptr, nullptr, q_colT, s_colT,
+                                     stream);
 }
 
 mxq_status mxq_qdq_mxfp4(const float *x, float *y, int64_t rows, int64_t cols, int block_size, float scale_factor,

@@ -16,8 +16,11 @@ cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, i
 // Column MXFP8 quant of bf16 x; q_row/s_row non-null adds the row quant (dual).
 cudaError_t launch_quant_cols(const uint16_t *x, int64_t R, int64_t C, int64_t ldx, uint8_t *q_row,
                               uint8_t *s_row, uint8_t *qT, uint8_t *sT, cudaStream_t st);
+// Per-group column MXFP8 quant of bf16 x [T x C]; q_row/s_row non-null adds the
+// plain row quant of x from the same read (cols % 32 == 0).
 cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, const int64_t *d_off, int E,
-                                      int64_t t_pad, uint8_t *qT, uint8_t *sT, cudaStream_t st);
+                                      int64_t t_pad, uint8_t *q_row, uint8_t *s_row, uint8_t *qT, uint8_t *sT,
+                                      cudaStream_t st);
 cudaError_t launch_qdq_mxfp4(const float *x, float *y, uint32_t *mask, int64_t rows, int64_t cols, float sf,
                              cudaStream_t st);
 // MXFP4 quant-dequant bf16 -> bf16, blocks of 32 along rows; cols % 32 == 0, 16-byte aligned.

@@ -454,6 +454,29 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
 // ============================================================================
 constexpr uint32_t kTileBytes = kTile * kTile * 2;
 
+// Groups whose offsets and padded starts a CTA keeps in shared memory.
+constexpr int kQuantTableE = 256;
+
+// The same from the CTA's shared tables: off[e] = group offsets, pre[e] =
+// padded start P_e of group e (pre[E] = the padded total).
+__device__ __forceinline__ void grouped_tile_source_tab(const int64_t *off, const int64_t *pre, int E, int64_t rt,
+                                                        int64_t &src0, int &nvalid) {
+    const int64_t t0 = rt * kTile;
+    if (t0 >= pre[E]) {  // a padding tile past the last group: all zeros
+        src0 = 0;
+        nvalid = 0;
+        return;
+    }
+    int lo = 0, hi = E;  // pre[lo] <= t0 < pre[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= t0) lo = mid; else hi = mid;
+    }
+    src0 = off[lo] + (t0 - pre[lo]);
+    const int64_t left = off[lo + 1] - src0;
+    nvalid = static_cast<int>(left < kTile ? left : kTile);
+}
+
 // First source row and the number of data rows of padded tile `rt` of a
 // per-group column quant (warp-wide; lane 0's result is returned to all).
 __device__ void grouped_tile_source(const ColParams &P, int64_t rt, int lane, int64_t &src0, int &nvalid) {
@@ -501,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_con
     __shared__ int64_t sh_src0[2];
     __shared__ int sh_nvalid[2];
     __shared__ int abort_flag;
+    __shared__ int64_t g_tab[GROUPED ? 2 * (kQuantTableE + 1) : 1];  // group offsets, padded starts
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t ring_s = smem_u32(ring), bar0 = smem_u32(&bars[0]);
@@ -511,6 +535,29 @@ __global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_con
         mbar_init(bar0 + 8, 1);
         fence_mbar_init();
     }
+    const bool tables = GROUPED && P.E <= kQuantTableE;
+    int64_t *g_off = g_tab, *g_pre = g_tab + (kQuantTableE + 1);
+    if (tables && warp == 0) {
+        // one scan of the offsets per CTA instead of one per tile
+        int64_t run = 0;
+        for (int base = 0; base <= P.E; base += 32) {
+            const int e = base + lane;
+            int64_t o0 = 0, padn = 0;
+            if (e <= P.E) o0 = P.offsets[e];
+            if (e < P.E) padn = (P.offsets[e + 1] - o0 + 127) / 128 * 128;
+            int64_t incl = padn;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            if (e <= P.E) {
+                g_off[e] = o0;
+                g_pre[e] = run + incl - padn;
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
     __syncthreads();
 
     // warp 0: resolve tile t into slot `buf` and start its load
@@ -518,7 +565,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_con
         const int64_t rt = t / ct_tiles, ct = t % ct_tiles;
         int64_t src0 = rt * kTile;
         int nvalid;
-        if (GROUPED) {
+        if (GROUPED && tables) {
+            grouped_tile_source_tab(g_off, g_pre, P.E, rt, src0, nvalid);
+        } else if (GROUPED) {
             grouped_tile_source(P, rt, lane, src0, nvalid);
         } else {
             const int64_t left = P.R - src0;
@@ -533,6 +582,17 @@ __global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_con
                         static_cast<int>(src0));
         }
     };
+
+    if (ROWS && GROUPED && blockIdx.x == 0) {
+        // row scales of the padding rows [R, ceil128(R)) of the last scale tile:
+        // no tile owns them
+        const int64_t npad = (P.R + 127) / 128 * 128 - P.R;
+        for (int64_t i = tid; i < npad * P.kb_row_tiles; i += kThreads) {
+            const int64_t r = P.R + i / P.kb_row_tiles, kt = i % P.kb_row_tiles;
+            *reinterpret_cast<uint32_t *>(P.s_row + ((r >> 7) * P.kb_row_tiles + kt) * 512 + 16 * (r & 31) +
+                                          4 * ((r >> 5) & 3)) = 0u;
+        }
+    }
 
     int64_t t = blockIdx.x;
     if (warp == 0 && t < n_tiles) issue(t, 0);
@@ -571,7 +631,12 @@ __global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_con
                                  "r"(codes.x), "r"(codes.y)
                                  : "memory");
                 }
-                if ((lane & 3) == 0) srow_atom[16 * (row & 31) + 4 * (row >> 5) + (ch >> 2)] = valid ? mx8_scale_byte(X) : 0;
+                if ((lane & 3) == 0) {
+                    if (GROUPED)  // row-major staging: row r's four blocks form word r
+                        srow_atom[4 * row + (ch >> 2)] = gc < P.C ? mx8_scale_byte(X) : 0;
+                    else
+                        srow_atom[16 * (row & 31) + 4 * (row >> 5) + (ch >> 2)] = valid ? mx8_scale_byte(X) : 0;
+                }
             }
         }
 
@@ -638,7 +703,15 @@ __global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_con
             }
         }
         __syncthreads();
-        if (ROWS && tid < 32) {
+        if (ROWS && GROUPED && tid >= kThreads - kTile && tid - (kThreads - kTile) < nvalid) {
+            // A group's rows start anywhere inside a 128-row scale tile: each
+            // row's word goes to its own place, and only this tile's rows.
+            const int row = tid - (kThreads - kTile);
+            const int64_t r = src0 + row;
+            *reinterpret_cast<uint32_t *>(P.s_row + ((r >> 7) * P.kb_row_tiles + ct) * 512 + 16 * (r & 31) +
+                                          4 * ((r >> 5) & 3)) = *reinterpret_cast<const uint32_t *>(srow_atom + 4 * row);
+        }
+        if (ROWS && !GROUPED && tid < 32) {
             const uint4 v = *reinterpret_cast<const uint4 *>(srow_atom + 16 * tid);
             stg_v4(P.s_row + (rt * P.kb_row_tiles + ct) * 512 + 16 * tid, v);
         } else if (tid >= 32 && tid < 64) {
@@ -922,13 +995,21 @@ cudaError_t launch_quant_cols(const uint16_t *x, int64_t R, int64_t C, int64_t l
 }
 
 cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, const int64_t *d_off, int E,
-                                      int64_t t_pad, uint8_t *qT, uint8_t *sT, cudaStream_t st) {
+                                      int64_t t_pad, uint8_t *q_row, uint8_t *s_row, uint8_t *qT, uint8_t *sT,
+                                      cudaStream_t st) {
     ColParams P{};
     P.x = x; P.R = T; P.C = C; P.ldx = C;
+    P.q_row = q_row; P.s_row = s_row; P.kb_row_tiles = ((C / 32) + 3) / 4;
     P.qT = qT; P.sT = sT; P.ldqT = t_pad; P.kb_col_tiles = (t_pad / 32 + 3) / 4;
     P.offsets = d_off; P.E = E;
     cudaError_t res = cudaSuccess;
-    if (launch_cols_tma<false, true>(P, t_pad / kTile, st, &res)) return res;
+    if (q_row && T > 0) {
+        if (launch_cols_tma<true, true>(P, t_pad / kTile, st, &res)) return res;
+        // no tensor map for x: the row quant on its own, then the column quant
+        if ((res = launch_quant_rows(x, false, 0, T, C, C, q_row, s_row, st)) != cudaSuccess) return res;
+    } else if (launch_cols_tma<false, true>(P, t_pad / kTile, st, &res)) {
+        return res;
+    }
     const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>(t_pad / kTile));
     k_quant_cols<false, true><<<grid, kThreads, 0, st>>>(P);
     return cudaGetLastError();

@@ -112,6 +112,11 @@ def test_host_validation_rejects_before_launch(lib):
     # grouped: E range, t_pad capacity, N multiple of 128 for FWD/DX
     assert _status(m.mxq_quantize_grouped_col, FAKE, 100, 64, FAKE, 0, 1024, FAKE, FAKE, 0) == INV
     assert _status(m.mxq_quantize_grouped_col, FAKE, 1000, 64, FAKE, 4, 1024, FAKE, FAKE, 0) == INV
+    # grouped dual: row outputs both or neither, and cols % 32 == 0 for them
+    assert _status(m.mxq_quantize_grouped_dual, FAKE, 100, 64, FAKE, 2, 512, FAKE, None, FAKE, FAKE, 0) == INV
+    assert _status(m.mxq_quantize_grouped_dual, FAKE, 100, 72, FAKE, 2, 512, FAKE, FAKE, FAKE, FAKE, 0) == INV
+    assert _status(m.mxq_quantize_grouped_dual, FAKE, 100, 64, FAKE, 2, 128, FAKE, FAKE, FAKE, FAKE, 0) == INV
+    assert "t_pad" in m.mxq_last_error_string()
     assert _status(m.mxq_grouped_gemm, m.GG_FWD, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 192, 64, 0, FAKE, 0) == INV
     assert _status(m.mxq_grouped_gemm, m.GG_DW, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 128, 64, 100, FAKE, 0) == INV
     # linear: dimensions multiple of 32, workspace large enough

@@ -171,6 +171,62 @@ def test_dual_quant_strided_views(mxq, R, C, pad, shift):
     assert np.array_equal(sT.cpu().numpy(), oracle.swizzle_scales(osT))
 
 
+def _grouped_dual(mxq, x, off):
+    T, C = x.shape
+    E = len(off) - 1
+    t_pad = mxq.mxq_grouped_padded_rows(T, E)
+    poison = lambda *shape: torch.full(shape, 0xAB, dtype=torch.uint8, device=DEV)  # noqa: E731
+    q, s = poison(max(T, 1), C), poison(mxq.mxq_scale_bytes(T, C // 32))
+    qT, sT = poison(C, t_pad), poison(mxq.mxq_scale_bytes(C, t_pad // 32))
+    mxq.mxq_quantize_grouped_dual(x.to(DEV), T, C, torch.from_numpy(off).to(DEV), E, t_pad, q, s, qT, sT)
+    return q.cpu().numpy()[:T], s.cpu().numpy(), qT.cpu().numpy(), sT.cpu().numpy(), t_pad
+
+
+@pytest.mark.parametrize("sizes", [[0, 5, 128, 33, 0, 200, 1], [300], [0, 0, 64], [1] * 40, [129, 127, 0, 3]])
+@pytest.mark.parametrize("C", [160, 256])
+def test_grouped_dual_quant_bit_exact(mxq, sizes, C):
+    """Row quant and per-group column quant from one read: both equal the
+    oracle's separate quants byte for byte, padding included (outputs are
+    poisoned first; rows past T in the last row-scale tile must read 0)."""
+    off = mxq_inputs.offsets_from_sizes(sizes)
+    x = _inputs(int(off[-1]), C, "heavy", seed=len(sizes) + C)
+    q, s, qT, sT, t_pad = _grouped_dual(mxq, x, off)
+    oq, os_ = oracle.mxfp8_quant_rows(x)
+    assert np.array_equal(q, oq)
+    assert np.array_equal(s, oracle.swizzle_scales(os_))
+    oqT, osT = oracle.mxfp8_quant_cols_grouped(x, off, t_pad)
+    assert np.array_equal(qT, oqT)
+    assert np.array_equal(sT, oracle.swizzle_scales(osT))
+
+
+def test_grouped_dual_quant_full_size_moe_dy(mxq):
+    """The MoE layer's dY, 32768 x 4096 bf16 in 32 Dirichlet(0.5) groups: every
+    byte of the four outputs against the oracle."""
+    E, T, C = 32, 32768, 4096
+    off = mxq_inputs.offsets_from_sizes(mxq_inputs.dirichlet_group_sizes(E, T, seed=0))
+    x = mxq_inputs.normal_bf16((T, C), 1e-3, seed=5)
+    q, s, qT, sT, t_pad = _grouped_dual(mxq, x, off)
+    oq, os_ = oracle.mxfp8_quant_rows(x)
+    assert np.array_equal(q, oq)
+    assert np.array_equal(s, oracle.swizzle_scales(os_))
+    oqT, osT = oracle.mxfp8_quant_cols_grouped(x, off, t_pad)
+    assert np.array_equal(qT, oqT)
+    assert np.array_equal(sT, oracle.swizzle_scales(osT))
+
+
+def test_grouped_dual_quant_without_row_outputs_is_the_column_quant(mxq):
+    off = mxq_inputs.offsets_from_sizes([7, 0, 250, 64])
+    x = _inputs(int(off[-1]), 96, "heavy", seed=3)
+    T, C, E = x.shape[0], x.shape[1], len(off) - 1
+    t_pad = mxq.mxq_grouped_padded_rows(T, E)
+    qT = torch.full((C, t_pad), 0xAB, dtype=torch.uint8, device=DEV)
+    sT = torch.full((mxq.mxq_scale_bytes(C, t_pad // 32),), 0xAB, dtype=torch.uint8, device=DEV)
+    mxq.mxq_quantize_grouped_dual(x.to(DEV), T, C, torch.from_numpy(off).to(DEV), E, t_pad, None, None, qT, sT)
+    oqT, osT = oracle.mxfp8_quant_cols_grouped(x, off, t_pad)
+    assert np.array_equal(qT.cpu().numpy(), oqT)
+    assert np.array_equal(sT.cpu().numpy(), oracle.swizzle_scales(osT))
+
+
 def test_grouped_col_quant_with_no_rows_writes_zero_padding(mxq):
     """Every group empty (T = 0): each byte of the t_pad-wide outputs is padding
     and must be written as 0 (the codes and the E8M0 scale bytes)."""
