@@ -453,6 +453,11 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
 // and the CTA stops after its copies have landed.
 // ============================================================================
 constexpr uint32_t kTileBytes = kTile * kTile * 2;
+// Tiles a CTA keeps in its ring: one being quantized, kRing - 1 loading.
+// Two slots at three CTAs per SM beat three slots at two CTAs per SM by 7%
+// (dual quant of 131072 x 7168: 730 vs 787 us): the kernel needs the warps
+// more than the deeper prefetch.
+constexpr int kRing = 2, kRingCtasPerSm = kRing == 2 ? 3 : 2;
 
 // Groups whose offsets and padded starts a CTA keeps in shared memory.
 constexpr int kQuantTableE = 256;
@@ -515,14 +520,17 @@ __device__ void grouped_tile_source(const ColParams &P, int64_t rt, int lane, in
 }
 
 template <bool ROWS, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_constant__ CUtensorMap tmX, ColParams P,
-                                                             int64_t n_tiles, int64_t ct_tiles, unsigned int *err) {
-    extern __shared__ __align__(128) uint8_t ring[];  // 2 x kTileBytes
-    __shared__ __align__(16) uint8_t srow_atom[512];
-    __shared__ __align__(16) uint8_t scol_atom[512];
-    __shared__ __align__(8) uint64_t bars[2];
-    __shared__ int64_t sh_src0[2];
-    __shared__ int sh_nvalid[2];
+__global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
+    k_quant_cols_tma(const __grid_constant__ CUtensorMap tmX, ColParams P, int64_t n_tiles, int64_t ct_tiles,
+                     unsigned int *err) {
+    extern __shared__ __align__(128) uint8_t ring[];  // kRing x kTileBytes
+    // scale tiles staged per tile, two deep: tile k + 1's passes fill one while
+    // tile k's are still being stored from the other
+    __shared__ __align__(16) uint8_t srow_atoms[2][512];
+    __shared__ __align__(16) uint8_t scol_atoms[2][512];
+    __shared__ __align__(8) uint64_t bars[kRing];
+    __shared__ int64_t sh_src0[kRing];
+    __shared__ int sh_nvalid[kRing];
     __shared__ int abort_flag;
     __shared__ int64_t g_tab[GROUPED ? 2 * (kQuantTableE + 1) : 1];  // group offsets, padded starts
 
@@ -531,8 +539,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_con
     volatile int *abort_v = &abort_flag;
     if (tid == 0) {
         abort_flag = 0;
-        mbar_init(bar0, 1);
-        mbar_init(bar0 + 8, 1);
+        for (int j = 0; j < kRing; j++) mbar_init(bar0 + 8 * j, 1);
         fence_mbar_init();
     }
     const bool tables = GROUPED && P.E <= kQuantTableE;
@@ -595,16 +602,20 @@ __global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_con
     }
 
     int64_t t = blockIdx.x;
-    if (warp == 0 && t < n_tiles) issue(t, 0);
+    if (warp == 0) {
+        for (int j = 0; j < kRing - 1; j++)
+            if (t + j * static_cast<int64_t>(gridDim.x) < n_tiles) issue(t + j * static_cast<int64_t>(gridDim.x), j);
+    }
     uint32_t k = 0;
-    int pending = t < n_tiles ? 0 : -1;  // slot with a load in flight (for the abort path)
     for (; t < n_tiles; t += gridDim.x, k++) {
-        const int buf = k & 1;
-        const int64_t tn = t + gridDim.x;
-        if (warp == 0 && tn < n_tiles) issue(tn, buf ^ 1);
-        pending = tn < n_tiles ? (buf ^ 1) : -1;
-        const bool ok = mbar_wait(bar0 + 8 * buf, (k >> 1) & 1, abort_v, err);
+        const int buf = static_cast<int>(k % kRing);
+        const bool ok = mbar_wait(bar0 + 8 * buf, (k / kRing) & 1, abort_v, err);
         if (!__syncthreads_and(ok)) break;
+        // every thread is past tile k - 1, so its slot is free: the load kRing - 1
+        // tiles ahead goes there
+        const int64_t tn = t + (kRing - 1) * static_cast<int64_t>(gridDim.x);
+        if (warp == 0 && tn < n_tiles) issue(tn, static_cast<int>((k + kRing - 1) % kRing));
+        uint8_t *srow_atom = srow_atoms[k & 1], *scol_atom = scol_atoms[k & 1];
 
         const uint8_t *tile = ring + buf * kTileBytes;
         const int64_t rt = t / ct_tiles, ct = t % ct_tiles;
@@ -719,16 +730,15 @@ __global__ void __launch_bounds__(kThreads, 3) k_quant_cols_tma(const __grid_con
             const uint4 v = *reinterpret_cast<const uint4 *>(scol_atom + 16 * l);
             stg_v4(P.sT + (ct * P.kb_col_tiles + rt) * 512 + 16 * l, v);
         }
-        __syncthreads();  // the slot and the atoms are free again
     }
     // stopped early: let the loads still in flight (this tile's and the
-    // prefetched one) land before shared memory goes away; bounded as well
+    // prefetched ones) land before shared memory goes away; bounded as well
     if (tid == 0 && t < n_tiles) {
         const uint64_t t0 = global_timer_ns();
-        for (uint32_t j = 0; j < 2; j++) {
+        for (uint32_t j = 0; j < static_cast<uint32_t>(kRing) - 1; j++) {
             const uint32_t kk = k + j;
-            if (j == 1 && pending < 0) break;
-            while (!mbar_try_wait(bar0 + 8 * (kk & 1), (kk >> 1) & 1)) {
+            if (t + j * static_cast<int64_t>(gridDim.x) >= n_tiles) break;
+            while (!mbar_try_wait(bar0 + 8 * (kk % kRing), (kk / kRing) & 1)) {
                 if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
             }
         }
@@ -950,7 +960,7 @@ bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cud
     unsigned int *err = nullptr;
     cudaError_t e = device_error_word(&err);
     if (e != cudaSuccess) { *res = e; return true; }
-    const int smem = 2 * static_cast<int>(kTileBytes);
+    const int smem = kRing * static_cast<int>(kTileBytes);
     static int per_sm[64] = {0}, sms[64] = {0};
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) { *res = e; return true; }
