@@ -601,119 +601,124 @@ __global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
         }
     }
 
+    // One barrier per tile.  A thread may start tile k once its slot's mbarrier
+    // completes (the arrive that armed it also publishes sh_src0/sh_nvalid);
+    // after the barrier that ends tile k every thread is done with its slot,
+    // and the load kRing tiles ahead goes there.
     int64_t t = blockIdx.x;
     if (warp == 0) {
-        for (int j = 0; j < kRing - 1; j++)
+        for (int j = 0; j < kRing; j++)
             if (t + j * static_cast<int64_t>(gridDim.x) < n_tiles) issue(t + j * static_cast<int64_t>(gridDim.x), j);
     }
     uint32_t k = 0;
     for (; t < n_tiles; t += gridDim.x, k++) {
         const int buf = static_cast<int>(k % kRing);
-        const bool ok = mbar_wait(bar0 + 8 * buf, (k / kRing) & 1, abort_v, err);
-        if (!__syncthreads_and(ok)) break;
-        // every thread is past tile k - 1, so its slot is free: the load kRing - 1
-        // tiles ahead goes there
-        const int64_t tn = t + (kRing - 1) * static_cast<int64_t>(gridDim.x);
-        if (warp == 0 && tn < n_tiles) issue(tn, static_cast<int>((k + kRing - 1) % kRing));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * buf, (k / kRing) & 1, abort_v, err));
         uint8_t *srow_atom = srow_atoms[k & 1], *scol_atom = scol_atoms[k & 1];
 
         const uint8_t *tile = ring + buf * kTileBytes;
         const int64_t rt = t / ct_tiles, ct = t % ct_tiles;
         const int64_t c0 = ct * kTile;
-        const int64_t src0 = sh_src0[buf];
+        const int64_t src0 = sh_src0[buf];  // read before the barrier that frees the slot
         const int nvalid = sh_nvalid[buf];
+        if (ok) {
 
-        if (ROWS) {
+            if (ROWS) {
 #pragma unroll
-            for (int i = 0; i < 8; i++) {
-                const int id = tid + kThreads * i;
-                const int row = id >> 4, ch = id & 15;
-                const int64_t gc = c0 + ch * 8;
-                const bool valid = row < nvalid && gc < P.C;
-                const uint4 v = *reinterpret_cast<const uint4 *>(tile + row * (kTile * 2) + ch * 16);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                uint32_t a = amax8_bf16(w);
-                a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
-                a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
-                const int X = mx8_exp_from_bf16(a);
-                if (valid) {
-                    const uint2 codes = e4m3_codes8(w, X);
-                    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(P.q_row + (src0 + row) * P.C + gc),
-                                 "r"(codes.x), "r"(codes.y)
-                                 : "memory");
-                }
-                if ((lane & 3) == 0) {
-                    if (GROUPED)  // row-major staging: row r's four blocks form word r
-                        srow_atom[4 * row + (ch >> 2)] = gc < P.C ? mx8_scale_byte(X) : 0;
-                    else
-                        srow_atom[16 * (row & 31) + 4 * (row >> 5) + (ch >> 2)] = valid ? mx8_scale_byte(X) : 0;
+                for (int i = 0; i < 8; i++) {
+                    const int id = tid + kThreads * i;
+                    const int row = id >> 4, ch = id & 15;
+                    const int64_t gc = c0 + ch * 8;
+                    const bool valid = row < nvalid && gc < P.C;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(tile + row * (kTile * 2) + ch * 16);
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t a = amax8_bf16(w);
+                    a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+                    a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+                    const int X = mx8_exp_from_bf16(a);
+                    if (valid) {
+                        const uint2 codes = e4m3_codes8(w, X);
+                        asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(P.q_row + (src0 + row) * P.C + gc),
+                                     "r"(codes.x), "r"(codes.y)
+                                     : "memory");
+                    }
+                    if ((lane & 3) == 0) {
+                        if (GROUPED)  // row-major staging: row r's four blocks form word r
+                            srow_atom[4 * row + (ch >> 2)] = gc < P.C ? mx8_scale_byte(X) : 0;
+                        else
+                            srow_atom[16 * (row & 31) + 4 * (row >> 5) + (ch >> 2)] = valid ? mx8_scale_byte(X) : 0;
+                    }
                 }
             }
-        }
 
-        // ---- column pass: thread (p, b) = (column pair, 32-row block) ----
-        {
-            const int p = tid & 63, b = tid >> 6;
-            uint32_t col[32];
+            // ---- column pass: thread (p, b) = (column pair, 32-row block) ----
+            {
+                const int p = tid & 63, b = tid >> 6;
+                uint32_t col[32];
 #pragma unroll
-            for (int i = 0; i < 32; i++) {
-                const uint32_t wv = *reinterpret_cast<const uint32_t *>(tile + (32 * b + i) * (kTile * 2) + 4 * p);
-                col[i] = (!GROUPED || 32 * b + i < nvalid) ? wv : 0u;  // rows of the next group read as zero
-            }
-            uint32_t m2 = 0;
-#pragma unroll
-            for (int i = 0; i < 32; i++) m2 = __vmaxu2(m2, col[i] & 0x7FFF7FFFu);
-            const int Xlo = mx8_exp_from_bf16(m2 & 0xFFFFu), Xhi = mx8_exp_from_bf16(m2 >> 16);
-            const int cl = 2 * p, ch2 = 2 * p + 1;
-            scol_atom[16 * (cl & 31) + 4 * (cl >> 5) + b] = mx8_scale_byte(Xlo);
-            scol_atom[16 * (ch2 & 31) + 4 * (ch2 >> 5) + b] = mx8_scale_byte(Xhi);
-
-            const int64_t gcol = c0 + cl;
-            if (gcol < P.C) {
-                uint32_t lo[8], hi[8];
-                // column 2p's scale in the low half, column 2p + 1's in the high half
-                const uint32_t inv2 = pow2_neg_bf16(Xlo > 127 ? 0 : Xlo) | (pow2_neg_bf16(Xhi > 127 ? 0 : Xhi) << 16);
-#pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    const uint32_t a0 = mul_bf16x2(col[4 * q], inv2), a1 = mul_bf16x2(col[4 * q + 1], inv2);
-                    const uint32_t a2 = mul_bf16x2(col[4 * q + 2], inv2), a3 = mul_bf16x2(col[4 * q + 3], inv2);
-                    lo[q] = e4m3x4(bf16lo(a0), bf16lo(a1), bf16lo(a2), bf16lo(a3));
-                    hi[q] = e4m3x4(bf16hi(a0), bf16hi(a1), bf16hi(a2), bf16hi(a3));
+                for (int i = 0; i < 32; i++) {
+                    const uint32_t wv = *reinterpret_cast<const uint32_t *>(tile + (32 * b + i) * (kTile * 2) + 4 * p);
+                    col[i] = (!GROUPED || 32 * b + i < nvalid) ? wv : 0u;  // rows of the next group read as zero
                 }
-                if (Xlo > 127 || Xhi > 127) {  // non-finite blocks: NaN codes with the sign kept
+                uint32_t m2 = 0;
+#pragma unroll
+                for (int i = 0; i < 32; i++) m2 = __vmaxu2(m2, col[i] & 0x7FFF7FFFu);
+                const int Xlo = mx8_exp_from_bf16(m2 & 0xFFFFu), Xhi = mx8_exp_from_bf16(m2 >> 16);
+                const int cl = 2 * p, ch2 = 2 * p + 1;
+                scol_atom[16 * (cl & 31) + 4 * (cl >> 5) + b] = mx8_scale_byte(Xlo);
+                scol_atom[16 * (ch2 & 31) + 4 * (ch2 >> 5) + b] = mx8_scale_byte(Xhi);
+
+                const int64_t gcol = c0 + cl;
+                if (gcol < P.C) {
+                    uint32_t lo[8], hi[8];
+                    // column 2p's scale in the low half, column 2p + 1's in the high half
+                    const uint32_t inv2 = pow2_neg_bf16(Xlo > 127 ? 0 : Xlo) | (pow2_neg_bf16(Xhi > 127 ? 0 : Xhi) << 16);
 #pragma unroll
                     for (int q = 0; q < 8; q++) {
-                        uint32_t sl = 0, sh = 0;
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            sl |= (0x7Fu | ((col[4 * q + j] >> 8) & 0x80u)) << (8 * j);
-                            sh |= (0x7Fu | ((col[4 * q + j] >> 24) & 0x80u)) << (8 * j);
-                        }
-                        if (Xlo > 127) lo[q] = sl;
-                        if (Xhi > 127) hi[q] = sh;
+                        const uint32_t a0 = mul_bf16x2(col[4 * q], inv2), a1 = mul_bf16x2(col[4 * q + 1], inv2);
+                        const uint32_t a2 = mul_bf16x2(col[4 * q + 2], inv2), a3 = mul_bf16x2(col[4 * q + 3], inv2);
+                        lo[q] = e4m3x4(bf16lo(a0), bf16lo(a1), bf16lo(a2), bf16lo(a3));
+                        hi[q] = e4m3x4(bf16hi(a0), bf16hi(a1), bf16hi(a2), bf16hi(a3));
                     }
-                }
-                const int64_t pos = rt * kTile + 32 * b;  // first output column (token) of the block
-                uint8_t *dlo = P.qT + gcol * P.ldqT + pos;
-                uint8_t *dhi = dlo + P.ldqT;
-                const int64_t limit = GROUPED ? P.ldqT : P.R;  // grouped tiles write padding zeros too
-                if (pos + 32 <= limit && (P.ldqT & 15) == 0) {
-                    stg_v4(dlo, make_uint4(lo[0], lo[1], lo[2], lo[3]));
-                    stg_v4(dlo + 16, make_uint4(lo[4], lo[5], lo[6], lo[7]));
-                    stg_v4(dhi, make_uint4(hi[0], hi[1], hi[2], hi[3]));
-                    stg_v4(dhi + 16, make_uint4(hi[4], hi[5], hi[6], hi[7]));
-                } else {
+                    if (Xlo > 127 || Xhi > 127) {  // non-finite blocks: NaN codes with the sign kept
 #pragma unroll
-                    for (int j = 0; j < 32; j++) {
-                        if (pos + j < limit) {
-                            dlo[j] = static_cast<uint8_t>(lo[j >> 2] >> (8 * (j & 3)));
-                            dhi[j] = static_cast<uint8_t>(hi[j >> 2] >> (8 * (j & 3)));
+                        for (int q = 0; q < 8; q++) {
+                            uint32_t sl = 0, sh = 0;
+#pragma unroll
+                            for (int j = 0; j < 4; j++) {
+                                sl |= (0x7Fu | ((col[4 * q + j] >> 8) & 0x80u)) << (8 * j);
+                                sh |= (0x7Fu | ((col[4 * q + j] >> 24) & 0x80u)) << (8 * j);
+                            }
+                            if (Xlo > 127) lo[q] = sl;
+                            if (Xhi > 127) hi[q] = sh;
+                        }
+                    }
+                    const int64_t pos = rt * kTile + 32 * b;  // first output column (token) of the block
+                    uint8_t *dlo = P.qT + gcol * P.ldqT + pos;
+                    uint8_t *dhi = dlo + P.ldqT;
+                    const int64_t limit = GROUPED ? P.ldqT : P.R;  // grouped tiles write padding zeros too
+                    if (pos + 32 <= limit && (P.ldqT & 15) == 0) {
+                        stg_v4(dlo, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+                        stg_v4(dlo + 16, make_uint4(lo[4], lo[5], lo[6], lo[7]));
+                        stg_v4(dhi, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+                        stg_v4(dhi + 16, make_uint4(hi[4], hi[5], hi[6], hi[7]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j++) {
+                            if (pos + j < limit) {
+                                dlo[j] = static_cast<uint8_t>(lo[j >> 2] >> (8 * (j & 3)));
+                                dhi[j] = static_cast<uint8_t>(hi[j >> 2] >> (8 * (j & 3)));
+                            }
                         }
                     }
                 }
             }
         }
-        __syncthreads();
+        if (!__syncthreads_and(ok)) break;
+        {
+            const int64_t tn = t + kRing * static_cast<int64_t>(gridDim.x);
+            if (warp == 0 && tn < n_tiles) issue(tn, buf);
+        }
         if (ROWS && GROUPED && tid >= kThreads - kTile && tid - (kThreads - kTile) < nvalid) {
             // A group's rows start anywhere inside a 128-row scale tile: each
             // row's word goes to its own place, and only this tile's rows.
@@ -735,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
     // prefetched ones) land before shared memory goes away; bounded as well
     if (tid == 0 && t < n_tiles) {
         const uint64_t t0 = global_timer_ns();
-        for (uint32_t j = 0; j < static_cast<uint32_t>(kRing) - 1; j++) {
+        for (uint32_t j = 0; j < static_cast<uint32_t>(kRing); j++) {
             const uint32_t kk = k + j;
             if (t + j * static_cast<int64_t>(gridDim.x) >= n_tiles) break;
             while (!mbar_try_wait(bar0 + 8 * (kk % kRing), (kk / kRing) & 1)) {
