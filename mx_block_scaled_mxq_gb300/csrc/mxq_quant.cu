@@ -37,6 +37,12 @@ __device__ __forceinline__ void stg_v4(void *p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
+// 32 bytes in one store (a whole L2 sector); p must be 32-byte aligned.
+__device__ __forceinline__ void stg_v8(void *p, uint4 a, uint4 b) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w),
+                 "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
 
 // Four fp32 values -> four E4M3 codes (a in the low byte); the two halves are
 // packed by register pairing.
@@ -543,6 +549,10 @@ __global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
         fence_mbar_init();
     }
     const bool tables = GROUPED && P.E <= kQuantTableE;
+    // 32-byte code stores where the output rows allow them (block starts are
+    // multiples of 32 bytes from the row start)
+    const bool row_v8 = ROWS && ((reinterpret_cast<uintptr_t>(P.q_row) | static_cast<uintptr_t>(P.C)) & 31) == 0;
+    const bool col_v8 = ((reinterpret_cast<uintptr_t>(P.qT) | static_cast<uintptr_t>(P.ldqT)) & 31) == 0;
     int64_t *g_off = g_tab, *g_pre = g_tab + (kQuantTableE + 1);
     if (tables && warp == 0) {
         // one scan of the offsets per CTA instead of one per tile
@@ -624,30 +634,55 @@ __global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
         if (ok) {
 
             if (ROWS) {
+                // ---- row pass: thread (row, blk) quantizes one 32-element block ----
+                // Its four 16-byte chunks are read starting at chunk g, which
+                // differs between the 8 threads of each quarter-warp that share
+                // a bank window (blk & 1 x g covers 8 distinct 16-byte slots),
+                // so the reads are conflict-free; the codes are put back in
+                // column order before the two 16-byte stores.
+                const int blk = tid & 3;
+                const int g = (blk >> 1) + 2 * ((tid >> 2) & 1);
+                const int64_t gc = c0 + 32 * blk;
 #pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    const int id = tid + kThreads * i;
-                    const int row = id >> 4, ch = id & 15;
-                    const int64_t gc = c0 + ch * 8;
-                    const bool valid = row < nvalid && gc < P.C;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(tile + row * (kTile * 2) + ch * 16);
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                    uint32_t a = amax8_bf16(w);
-                    a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
-                    a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+                for (int it = 0; it < 2; it++) {
+                    const int row = (tid >> 2) + 64 * it;
+                    const uint8_t *src = tile + row * (kTile * 2) + 64 * blk;
+                    uint32_t w[4][4];
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * ((j + g) & 3));
+                        w[j][0] = v.x; w[j][1] = v.y; w[j][2] = v.z; w[j][3] = v.w;
+                    }
+                    const uint32_t a = max(max(amax8_bf16(w[0]), amax8_bf16(w[1])), max(amax8_bf16(w[2]), amax8_bf16(w[3])));
                     const int X = mx8_exp_from_bf16(a);
+                    const bool valid = row < nvalid && gc < P.C;
                     if (valid) {
-                        const uint2 codes = e4m3_codes8(w, X);
-                        asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(P.q_row + (src0 + row) * P.C + gc),
-                                     "r"(codes.x), "r"(codes.y)
-                                     : "memory");
+                        uint2 cd[4];
+#pragma unroll
+                        for (int j = 0; j < 4; j++) cd[j] = e4m3_codes8(w[j], X);
+                        // cd[j] holds chunk (j + g) & 3: rotate back by g (1, then 2)
+                        if (g & 1) {
+                            const uint2 t = cd[3];
+                            cd[3] = cd[2]; cd[2] = cd[1]; cd[1] = cd[0]; cd[0] = t;
+                        }
+                        if (g & 2) {
+                            uint2 t = cd[0]; cd[0] = cd[2]; cd[2] = t;
+                            t = cd[1]; cd[1] = cd[3]; cd[3] = t;
+                        }
+                        uint8_t *dst = P.q_row + (src0 + row) * P.C + gc;
+                        const uint4 lo4 = make_uint4(cd[0].x, cd[0].y, cd[1].x, cd[1].y);
+                        const uint4 hi4 = make_uint4(cd[2].x, cd[2].y, cd[3].x, cd[3].y);
+                        if (row_v8) {
+                            stg_v8(dst, lo4, hi4);
+                        } else {
+                            stg_v4(dst, lo4);
+                            stg_v4(dst + 16, hi4);
+                        }
                     }
-                    if ((lane & 3) == 0) {
-                        if (GROUPED)  // row-major staging: row r's four blocks form word r
-                            srow_atom[4 * row + (ch >> 2)] = gc < P.C ? mx8_scale_byte(X) : 0;
-                        else
-                            srow_atom[16 * (row & 31) + 4 * (row >> 5) + (ch >> 2)] = valid ? mx8_scale_byte(X) : 0;
-                    }
+                    if (GROUPED)  // row-major staging: row r's four blocks form word r
+                        srow_atom[4 * row + blk] = gc < P.C ? mx8_scale_byte(X) : 0;
+                    else
+                        srow_atom[16 * (row & 31) + 4 * (row >> 5) + blk] = valid ? mx8_scale_byte(X) : 0;
                 }
             }
 
@@ -697,7 +732,10 @@ __global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
                     uint8_t *dlo = P.qT + gcol * P.ldqT + pos;
                     uint8_t *dhi = dlo + P.ldqT;
                     const int64_t limit = GROUPED ? P.ldqT : P.R;  // grouped tiles write padding zeros too
-                    if (pos + 32 <= limit && (P.ldqT & 15) == 0) {
+                    if (pos + 32 <= limit && col_v8) {
+                        stg_v8(dlo, make_uint4(lo[0], lo[1], lo[2], lo[3]), make_uint4(lo[4], lo[5], lo[6], lo[7]));
+                        stg_v8(dhi, make_uint4(hi[0], hi[1], hi[2], hi[3]), make_uint4(hi[4], hi[5], hi[6], hi[7]));
+                    } else if (pos + 32 <= limit && (P.ldqT & 15) == 0) {
                         stg_v4(dlo, make_uint4(lo[0], lo[1], lo[2], lo[3]));
                         stg_v4(dlo + 16, make_uint4(lo[4], lo[5], lo[6], lo[7]));
                         stg_v4(dhi, make_uint4(hi[0], hi[1], hi[2], hi[3]));

@@ -38,7 +38,10 @@ def test_row_quant_bit_exact(mxq, R, C, kind):
     assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
 
 
-COL_SHAPES = [(256, 512), (96, 64), (100, 64), (130, 136), (33, 8), (1, 32), (4096, 384), (200, 1024)]
+# (80, 256) and (144, 96): a transposed-code row pitch that is a multiple of 16
+# bytes but not of 32 (the 16-byte store path of the column pass)
+COL_SHAPES = [(256, 512), (96, 64), (100, 64), (130, 136), (33, 8), (1, 32), (4096, 384), (200, 1024), (80, 256),
+              (144, 96)]
 
 
 @pytest.mark.parametrize("R,C", COL_SHAPES)
@@ -168,6 +171,35 @@ def test_dual_quant_strided_views(mxq, R, C, pad, shift):
     assert np.array_equal(q.cpu().numpy(), oq)
     assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
     assert np.array_equal(qT.cpu().numpy(), oqT)
+    assert np.array_equal(sT.cpu().numpy(), oracle.swizzle_scales(osT))
+
+
+@pytest.mark.parametrize("grouped", [False, True])
+def test_dual_quant_outputs_16_but_not_32_byte_aligned(mxq, grouped):
+    """Output buffers that start 16 bytes past a 32-byte boundary take the
+    16-byte store path; codes and scales are unchanged."""
+    R, C = 384, 256
+    x = _inputs(R, C, "heavy", seed=9)
+    off = mxq_inputs.offsets_from_sizes([100, 0, 284])
+    t_pad = mxq.mxq_grouped_padded_rows(R, 3) if grouped else R
+    def at16(n):  # a buffer of n bytes at 16 mod 32
+        buf = torch.full((n + 48,), 0xAB, dtype=torch.uint8, device=DEV)
+        o = (-buf.data_ptr()) % 32 + 16
+        return buf[o:o + n]
+    q, s = at16(R * C), at16(mxq.mxq_scale_bytes(R, C // 32))
+    qT, sT = at16(C * t_pad), at16(mxq.mxq_scale_bytes(C, t_pad // 32))
+    assert q.data_ptr() % 32 == 16 and qT.data_ptr() % 32 == 16
+    xd = x.to(DEV)
+    if grouped:
+        mxq.mxq_quantize_grouped_dual(xd, R, C, torch.from_numpy(off).to(DEV), 3, t_pad, q, s, qT, sT)
+        oqT, osT = oracle.mxfp8_quant_cols_grouped(x, off, t_pad)
+    else:
+        mxq.mxq_quantize(xd, mxq.BF16, R, C, C, -1, mxq.E4M3, 1, q, s, qT, sT)
+        oqT, osT = oracle.mxfp8_quant_cols(x)
+    oq, os_ = oracle.mxfp8_quant_rows(x)
+    assert np.array_equal(q.cpu().numpy().reshape(R, C), oq)
+    assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
+    assert np.array_equal(qT.cpu().numpy().reshape(C, t_pad), oqT)
     assert np.array_equal(sT.cpu().numpy(), oracle.swizzle_scales(osT))
 
 
