@@ -26,6 +26,12 @@ namespace {
 constexpr int kTile = 128;
 constexpr int kThreads = 256;
 
+// 32 bytes in one load; p must be 32-byte aligned.
+__device__ __forceinline__ void ldg_nc_v8(const void *p, uint4 &a, uint4 &b) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p));
+}
 __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
     uint4 r;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -180,6 +186,8 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile, c0 = static_cast<int64_t>(blockIdx.x) * kTile;
     // all of this thread's loads first (8 or 16 x 16 B in flight), then compute
     constexpr int kVec = sizeof(InT) == 4 ? 2 : 1;
+    // fp32 rows: one 32-byte load per 8 elements where x is 32-byte aligned (ldx % 8 == 0)
+    const bool al32 = kVec == 2 && (reinterpret_cast<uintptr_t>(x) & 31) == 0;
     uint4 v[8][kVec];
 #pragma unroll
     for (int i = 0; i < 8; i++) {
@@ -189,8 +197,12 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
         for (int h = 0; h < kVec; h++) v[i][h] = make_uint4(0, 0, 0, 0);
         if (gr < R && gc < C) {
             const InT *src = x + gr * ldx + gc;
+            if (kVec == 2 && al32) {
+                ldg_nc_v8(src, v[i][0], v[i][kVec - 1]);
+            } else {
 #pragma unroll
-            for (int h = 0; h < kVec; h++) v[i][h] = ldg_nc_v4(reinterpret_cast<const uint32_t *>(src) + 4 * h);
+                for (int h = 0; h < kVec; h++) v[i][h] = ldg_nc_v4(reinterpret_cast<const uint32_t *>(src) + 4 * h);
+            }
         }
     }
 #pragma unroll
@@ -803,12 +815,20 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restr
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t wstride = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+    // one 32-byte access per thread where both tensors are 32-byte aligned
+    const bool al32 = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 31) == 0;
     for (int64_t wb = warp0 * 32; wb < nchunks; wb += wstride * 32) {
         const int64_t g = wb + lane;
         const bool valid = g < nchunks;  // uniform over the 4 lanes of a block (nchunks % 4 == 0)
         float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         if (valid) {
-            const uint4 a = ldg_nc_v4(x + 8 * g), b = ldg_nc_v4(x + 8 * g + 4);
+            uint4 a, b;
+            if (al32) {
+                ldg_nc_v8(x + 8 * g, a, b);
+            } else {
+                a = ldg_nc_v4(x + 8 * g);
+                b = ldg_nc_v4(x + 8 * g + 4);
+            }
             v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
             v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
         }
@@ -841,8 +861,14 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restr
             if (lane < 8 && wb + 4 * lane < nchunks) mask[wb / 4 + lane] = w;
         }
         if (!valid) continue;
-        stg_v4(y + 8 * g, make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3])));
-        stg_v4(y + 8 * g + 4, make_uint4(__float_as_uint(o[4]), __float_as_uint(o[5]), __float_as_uint(o[6]), __float_as_uint(o[7])));
+        const uint4 o0 = make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
+        const uint4 o1 = make_uint4(__float_as_uint(o[4]), __float_as_uint(o[5]), __float_as_uint(o[6]), __float_as_uint(o[7]));
+        if (al32) {
+            stg_v8(y + 8 * g, o0, o1);
+        } else {
+            stg_v4(y + 8 * g, o0);
+            stg_v4(y + 8 * g + 4, o1);
+        }
     }
 }
 
@@ -925,17 +951,28 @@ __global__ void __launch_bounds__(kThreads) k_ste_backward_vec(const float *__re
                                                                const uint32_t *__restrict__ mask, float *gx,
                                                                int64_t nchunks) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const bool al32 = ((reinterpret_cast<uintptr_t>(gy) | reinterpret_cast<uintptr_t>(gx)) & 31) == 0;
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < nchunks; g += stride) {
         const uint32_t bits = (__ldg(mask + g / 4) >> (8 * (g & 3))) & 0xFFu;
-        uint4 a = ldg_nc_v4(gy + 8 * g), b = ldg_nc_v4(gy + 8 * g + 4);
+        uint4 a, b;
+        if (al32) {
+            ldg_nc_v8(gy + 8 * g, a, b);
+        } else {
+            a = ldg_nc_v4(gy + 8 * g);
+            b = ldg_nc_v4(gy + 8 * g + 4);
+        }
         if (bits) {
             a.x = (bits & 1u) ? 0u : a.x;    a.y = (bits & 2u) ? 0u : a.y;
             a.z = (bits & 4u) ? 0u : a.z;    a.w = (bits & 8u) ? 0u : a.w;
             b.x = (bits & 16u) ? 0u : b.x;   b.y = (bits & 32u) ? 0u : b.y;
             b.z = (bits & 64u) ? 0u : b.z;   b.w = (bits & 128u) ? 0u : b.w;
         }
-        stg_v4(gx + 8 * g, a);
-        stg_v4(gx + 8 * g + 4, b);
+        if (al32) {
+            stg_v8(gx + 8 * g, a, b);
+        } else {
+            stg_v4(gx + 8 * g, a);
+            stg_v4(gx + 8 * g + 4, b);
+        }
     }
 }
 

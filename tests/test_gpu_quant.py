@@ -138,6 +138,41 @@ def test_packed_mxfp4_bit_exact(mxq, dtype, R, C):
     assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
 
 
+def _f32_at16(a: np.ndarray) -> torch.Tensor:
+    """a copy of `a` on the GPU whose data starts 16 bytes past a 32-byte boundary"""
+    buf = torch.empty(a.size + 12, dtype=torch.float32, device=DEV)
+    o = ((-buf.data_ptr()) % 32 + 16) // 4
+    t = buf[o:o + a.size].view(a.shape)
+    t.copy_(torch.from_numpy(a))
+    assert t.data_ptr() % 32 == 16
+    return t
+
+
+def test_fp32_vector_paths_16_but_not_32_byte_aligned(mxq):
+    """fp32 MXFP4 QDQ, clipped-STE forward/backward and packed quant on
+    buffers 16 bytes past a 32-byte boundary take the 16-byte access path;
+    results unchanged."""
+    R, C = 64, 256
+    a = mxq_inputs.mxfp4_large(R, C, seed=21)
+    x = _f32_at16(a)
+    y = _f32_at16(np.zeros_like(a))
+    mxq.mxq_qdq_mxfp4(x, y, R, C, 32, 6.0)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), oracle.mxfp4_qdq(a).view(np.uint32))
+    m = torch.empty((R, C // 32), dtype=torch.int32, device=DEV)
+    mxq.mxq_mxfp4_ste_forward(x, y, m, R, C, 32, 6.0)
+    ref_m = oracle.mxfp4_saturation_mask(a)
+    assert np.array_equal(m.cpu().numpy().view(np.uint32), ref_m)
+    gy = mxq_inputs.mxfp4_small((R, C), seed=22)
+    g = _f32_at16(gy)
+    gx = _f32_at16(np.zeros_like(gy))
+    mxq.mxq_mxfp4_ste_backward(g, m, R, C, gx)
+    assert np.array_equal(gx.cpu().numpy().view(np.uint32), oracle.mxfp4_ste_backward(gy, ref_m).view(np.uint32))
+    q, s = mxq.quantize_mxfp4(x)
+    oq, os_ = oracle.mxfp4_quant(a)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
+
+
 # ------------------------------------------------------------------ full sizes
 
 def test_full_size_linear_operands_dual_quant(mxq):
