@@ -464,18 +464,23 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
 // ============================================================================
 // Persistent column quant (optionally dual / grouped) with TMA staging.
 // Same output as k_quant_cols; each CTA walks tiles blockIdx.x, +gridDim.x, ...
-// and keeps a two-deep ring of 128 x 128 bf16 tiles in shared memory: warp 0
-// issues the next tile's cp.async.bulk.tensor load before the CTA works on the
-// current one, so HBM reads overlap the quantization.  Grid = CTAs resident on
-// all SMs (3 per SM).  Waits are bounded: a timeout sets the device error word
-// and the CTA stops after its copies have landed.
+// and keeps a ring of 128 x 128 bf16 tiles in shared memory (QuantRing): warp
+// 0 keeps the cp.async.bulk.tensor loads of the next tiles in flight while the
+// CTA works on the current one, so HBM reads overlap the quantization.  Grid =
+// CTAs resident on all SMs.  Waits are bounded: a timeout sets the device
+// error word and the CTA stops after its copies have landed.
 // ============================================================================
 constexpr uint32_t kTileBytes = kTile * kTile * 2;
-// Tiles a CTA keeps in its ring: one being quantized, kRing - 1 loading.
-// Two slots at three CTAs per SM beat three slots at two CTAs per SM by 7%
-// (dual quant of 131072 x 7168: 730 vs 787 us): the kernel needs the warps
-// more than the deeper prefetch.
-constexpr int kRing = 2, kRingCtasPerSm = kRing == 2 ? 3 : 2;
+// Tiles a CTA keeps in its ring (one being quantized, the rest loading) and
+// the CTAs per SM that leaves room for.  The plain quant runs best with two
+// slots at three CTAs per SM (dual quant of 131072 x 7168: 661 vs 673 us with
+// three slots at two); the per-group quant, whose tiles start at arbitrary
+// rows and end early at group boundaries, with three slots at two
+// (grouped dual of 32768 x 7168: 174 vs 184 us).
+template <bool GROUPED>
+struct QuantRing {
+    static constexpr int kSlots = GROUPED ? 3 : 2, kCtasPerSm = GROUPED ? 2 : 3;
+};
 
 // Groups whose offsets and padded starts a CTA keeps in shared memory.
 constexpr int kQuantTableE = 256;
@@ -538,9 +543,10 @@ __device__ void grouped_tile_source(const ColParams &P, int64_t rt, int lane, in
 }
 
 template <bool ROWS, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, kRingCtasPerSm)
+__global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
     k_quant_cols_tma(const __grid_constant__ CUtensorMap tmX, ColParams P, int64_t n_tiles, int64_t ct_tiles,
                      unsigned int *err) {
+    constexpr int kRing = QuantRing<GROUPED>::kSlots;
     extern __shared__ __align__(128) uint8_t ring[];  // kRing x kTileBytes
     // scale tiles staged per tile, two deep: tile k + 1's passes fill one while
     // tile k's are still being stored from the other
@@ -1040,7 +1046,7 @@ bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cud
     unsigned int *err = nullptr;
     cudaError_t e = device_error_word(&err);
     if (e != cudaSuccess) { *res = e; return true; }
-    const int smem = kRing * static_cast<int>(kTileBytes);
+    const int smem = QuantRing<GROUPED>::kSlots * static_cast<int>(kTileBytes);
     static int per_sm[64] = {0}, sms[64] = {0};
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) { *res = e; return true; }
