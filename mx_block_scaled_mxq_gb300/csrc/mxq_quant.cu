@@ -177,6 +177,22 @@ __device__ __forceinline__ float qdq_one(float x, const E2M1Thr &T) {
 // E4M3 code of E2M1 codebook index i (0, .5, 1, 1.5, 2, 3, 4, 6), byte i.
 constexpr unsigned long long kE2M1AsE4M3 = 0x4C4844403C383000ull;
 
+// E4M3 codes of the MXFP4 values of 8 bf16 (4 packed words, element 2k in the
+// low half of word k) under thresholds T: sign | the E4M3 code of the E2M1
+// value; the NaN code 0x7F | sign for a non-finite block.
+__device__ __forceinline__ uint2 mx4_as_e4m3_codes8(const uint32_t (&w)[4], const E2M1Thr &T, bool nonfinite) {
+    uint32_t b[2] = {0, 0};
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const uint32_t bits = (k & 1) ? (w[k >> 1] & 0xFFFF0000u) : (w[k >> 1] << 16);
+        const uint32_t mag =
+            nonfinite ? 0x7Fu
+                      : static_cast<uint32_t>((kE2M1AsE4M3 >> (8 * e2m1_index(fabsf(__uint_as_float(bits)), T))) & 0xFFu);
+        b[k >> 2] |= (((bits >> 24) & 0x80u) | mag) << (8 * (k & 3));
+    }
+    return make_uint2(b[0], b[1]);
+}
+
 template <typename InT, int FMT>
 __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__ x, int64_t R, int64_t C,
                                                          int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
@@ -307,6 +323,7 @@ struct ColParams {
     int64_t kb_col_tiles;
     const int64_t *offsets;  // GROUPED: E+1 device offsets
     int E;
+    float sf;                // MXFP4 scale factor (row pass in FMT 2)
 };
 
 template <bool ROWS, bool GROUPED>
@@ -542,7 +559,9 @@ __device__ void grouped_tile_source(const ColParams &P, int64_t rt, int lane, in
     nvalid = 0;  // a padding tile past the last group: all zeros
 }
 
-template <bool ROWS, bool GROUPED>
+// COLS = false leaves out the column pass (a row quant alone); FMT selects the
+// row pass's format: 0 MXFP8, 2 MXFP4 values as E4M3 codes (scale factor P.sf).
+template <bool ROWS, bool GROUPED, bool COLS = true, int FMT = 0>
 __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
     k_quant_cols_tma(const __grid_constant__ CUtensorMap tmX, ColParams P, int64_t n_tiles, int64_t ct_tiles,
                      unsigned int *err) {
@@ -672,12 +691,24 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
                         w[j][0] = v.x; w[j][1] = v.y; w[j][2] = v.z; w[j][3] = v.w;
                     }
                     const uint32_t a = max(max(amax8_bf16(w[0]), amax8_bf16(w[1])), max(amax8_bf16(w[2]), amax8_bf16(w[3])));
-                    const int X = mx8_exp_from_bf16(a);
+                    int X = 0;            // FMT 0: MXFP8 scale exponent
+                    E2M1Thr T{};          // FMT 2: MXFP4 thresholds
+                    bool nonfinite = false;
+                    uint8_t sbyte;
+                    if (FMT == 0) {
+                        X = mx8_exp_from_bf16(a);
+                        sbyte = mx8_scale_byte(X);
+                    } else {
+                        nonfinite = (a << 16) >= 0x7F800000u;
+                        const int e = nonfinite ? 0 : mx4_exp(__uint_as_float(a << 16), P.sf);
+                        sbyte = nonfinite ? 0xFF : static_cast<uint8_t>(e + 127);
+                        T = e2m1_thresholds(e);
+                    }
                     const bool valid = row < nvalid && gc < P.C;
                     if (valid) {
                         uint2 cd[4];
 #pragma unroll
-                        for (int j = 0; j < 4; j++) cd[j] = e4m3_codes8(w[j], X);
+                        for (int j = 0; j < 4; j++) cd[j] = FMT == 0 ? e4m3_codes8(w[j], X) : mx4_as_e4m3_codes8(w[j], T, nonfinite);
                         // cd[j] holds chunk (j + g) & 3: rotate back by g (1, then 2)
                         if (g & 1) {
                             const uint2 t = cd[3];
@@ -698,14 +729,14 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
                         }
                     }
                     if (GROUPED)  // row-major staging: row r's four blocks form word r
-                        srow_atom[4 * row + blk] = gc < P.C ? mx8_scale_byte(X) : 0;
+                        srow_atom[4 * row + blk] = gc < P.C ? sbyte : 0;
                     else
-                        srow_atom[16 * (row & 31) + 4 * (row >> 5) + blk] = valid ? mx8_scale_byte(X) : 0;
+                        srow_atom[16 * (row & 31) + 4 * (row >> 5) + blk] = valid ? sbyte : 0;
                 }
             }
 
             // ---- column pass: thread (p, b) = (column pair, 32-row block) ----
-            {
+            if constexpr (COLS) {
                 const int p = tid & 63, b = tid >> 6;
                 uint32_t col[32];
 #pragma unroll
@@ -786,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
         if (ROWS && !GROUPED && tid < 32) {
             const uint4 v = *reinterpret_cast<const uint4 *>(srow_atom + 16 * tid);
             stg_v4(P.s_row + (rt * P.kb_row_tiles + ct) * 512 + 16 * tid, v);
-        } else if (tid >= 32 && tid < 64) {
+        } else if (COLS && tid >= 32 && tid < 64) {
             const int l = tid - 32;
             const uint4 v = *reinterpret_cast<const uint4 *>(scol_atom + 16 * l);
             stg_v4(P.sT + (ct * P.kb_col_tiles + rt) * 512 + 16 * l, v);
@@ -1008,11 +1039,30 @@ int grid_for(int64_t work_items, int per_cta) {
 }  // namespace
 
 // ---------------------------------------------------------------- launchers
+namespace {
+// Persistent TMA-staged launch of k_quant_cols_tma; returns false (no launch)
+// where x takes no tensor map.
+template <bool ROWS, bool GROUPED, bool COLS = true, int FMT = 0>
+bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cudaError_t *res);
+}  // namespace
+
 cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, int64_t C, int64_t ldx, uint8_t *q,
                               uint8_t *s, cudaStream_t st, float sf) {
     const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((R + kTile - 1) / kTile));
     const int64_t kb_tiles = ((C / 32) + 3) / 4;
     const uint16_t *xb = static_cast<const uint16_t *>(x);
+    if (!fp32_in && (fmt == 0 || fmt == 2)) {
+        // the persistent TMA-staged kernel, row pass only
+        ColParams P{};
+        P.x = xb; P.R = R; P.C = C; P.ldx = ldx;
+        P.q_row = q; P.s_row = s; P.kb_row_tiles = kb_tiles;
+        P.sf = sf;
+        const int64_t row_tiles = (R + kTile - 1) / kTile;
+        cudaError_t res = cudaSuccess;
+        if (fmt == 0 ? launch_cols_tma<true, false, false, 0>(P, row_tiles, st, &res)
+                     : launch_cols_tma<true, false, false, 2>(P, row_tiles, st, &res))
+            return res;
+    }
     if (fmt == 0) {
         k_quant_rows<uint16_t, 0><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf);
     } else if (fmt == 2) {
@@ -1033,7 +1083,7 @@ namespace {
 // per-group quant whose groups are all empty writes only padding), or an
 // unaligned base or row stride, which the C entry points reject before they
 // get here -- so the caller runs the one-tile-per-CTA kernel.
-template <bool ROWS, bool GROUPED>
+template <bool ROWS, bool GROUPED, bool COLS, int FMT>
 bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cudaError_t *res) {
     if ((reinterpret_cast<uintptr_t>(P.x) & 15) || (P.ldx % 8) || P.C >= (1ll << 31) || P.R >= (1ll << 31) ||
         P.R == 0)
@@ -1052,9 +1102,9 @@ bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cud
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) { *res = e; return true; }
     if (dev < 0 || dev >= 64) { *res = cudaErrorInvalidDevice; return true; }
     if (per_sm[dev] == 0) {
-        if ((e = cudaFuncSetAttribute(k_quant_cols_tma<ROWS, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((e = cudaFuncSetAttribute(k_quant_cols_tma<ROWS, GROUPED, COLS, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       smem)) != cudaSuccess ||
-            (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev], k_quant_cols_tma<ROWS, GROUPED>, kThreads,
+            (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev], k_quant_cols_tma<ROWS, GROUPED, COLS, FMT>, kThreads,
                                                                smem)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
             per_sm[dev] = 0;
@@ -1067,7 +1117,7 @@ bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cud
     const int64_t n_tiles = row_tiles * ct_tiles;
     const int64_t grid = n_tiles < static_cast<int64_t>(per_sm[dev]) * sms[dev] ? n_tiles
                                                                                  : static_cast<int64_t>(per_sm[dev]) * sms[dev];
-    k_quant_cols_tma<ROWS, GROUPED><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tm, P, n_tiles, ct_tiles, err);
+    k_quant_cols_tma<ROWS, GROUPED, COLS, FMT><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tm, P, n_tiles, ct_tiles, err);
     *res = cudaGetLastError();
     return true;
 }

@@ -105,6 +105,41 @@ def test_w4a16_full_size_sampled_rows(mxq):
                 oracle.qat_linear_ref(x[torch.from_numpy(rows)], w, quantize_input=False))
 
 
+def _r256(n: int) -> int:
+    return (n + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("M,N,K", [(96, 160, 352), (256, 128, 512)])
+@pytest.mark.parametrize("sf", [6.0, 7.5])
+def test_w4a4_operands_are_the_mxfp4_quant_as_e4m3(mxq, M, N, K, sf):
+    """The W4A4 forward holds Q(x) and Q(w) in its workspace as E4M3 codes under
+    the MXFP4 E8M0 scales (codes, then scales, each from a 256-byte boundary,
+    x first).  Every code must be the E4M3 code of the oracle's E2M1 value
+    (sign kept) and every scale byte the oracle's, padding included."""
+    x = _bf16(mxq_inputs.mxfp4_large(M, K, seed=M + K))
+    w = _bf16(mxq_inputs.mxfp4_large(N, K, seed=N + K + 1))
+    ws_bytes = mxq.mxq_qat_linear_workspace_bytes(M, N, K, 1)
+    ws = torch.full((ws_bytes,), 0xAB, dtype=torch.uint8, device=DEV)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    mxq.mxq_qat_linear_fwd(x.to(DEV), w.to(DEV), None, M, N, K, 1, sf, y, ws, ws_bytes)
+    wsh = ws.cpu().numpy()
+    # E4M3 code of each E2M1 codebook value, looked up in the E4M3 decode table
+    t8, t4 = oracle.e4m3_decode_table(), oracle.e2m1_decode_table()
+    as_e4m3 = np.array([int(np.flatnonzero(t8 == t4[i])[0]) for i in range(8)], dtype=np.uint8)
+    off = 0
+    for t, R in ((x, M), (w, N)):
+        nib, sc = oracle.mxfp4_quant(t.to(torch.float32).numpy(), sf)
+        codes = np.empty((R, K), np.uint8)
+        codes[:, 0::2], codes[:, 1::2] = nib & 0xF, nib >> 4
+        want = as_e4m3[codes & 7] | np.where(codes & 8, 0x80, 0).astype(np.uint8)
+        got = wsh[off:off + R * K].reshape(R, K)
+        assert np.array_equal(got, want)
+        off += _r256(R * K)
+        nsb = mxq.mxq_scale_bytes(R, K // 32)
+        assert np.array_equal(wsh[off:off + nsb], oracle.swizzle_scales(sc))
+        off += _r256(nsb)
+
+
 @pytest.mark.parametrize("shape", [(64, 256), (4096, 4096), (3, 96)])
 @pytest.mark.parametrize("sf", [6.0, 7.5])
 def test_bf16_qdq_bit_exact(mxq, shape, sf):
