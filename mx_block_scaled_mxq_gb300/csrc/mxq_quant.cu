@@ -148,12 +148,15 @@ __device__ __forceinline__ E2M1Thr e2m1_thresholds(int e) {
     r.t[4] = 2.5f * r.s;  r.t[5] = 3.5f * r.s;  r.t[6] = 5.0f * r.s;
     return r;
 }
-// Codebook index of |x|: the number of midpoints <= |x| / 2^e (exact compare).
+// Codebook index of |x|: the number of midpoints <= |x| / 2^e, found by a
+// three-level binary search over the same exact thresholds (midpoint t[3]
+// first, then t[1] or t[5], then t[0], t[2], t[4] or t[6]).
 __device__ __forceinline__ uint32_t e2m1_index(float ax, const E2M1Thr &T) {
-    uint32_t i = 0;
-#pragma unroll
-    for (int k = 0; k < 7; k++) i += ax >= T.t[k] ? 1u : 0u;
-    return i;
+    const bool c1 = ax >= T.t[3];
+    const bool c2 = ax >= (c1 ? T.t[5] : T.t[1]);
+    const float t3 = c1 ? (c2 ? T.t[6] : T.t[4]) : (c2 ? T.t[2] : T.t[0]);
+    const bool c3 = ax >= t3;
+    return (c1 ? 4u : 0u) + (c2 ? 2u : 0u) + (c3 ? 1u : 0u);
 }
 // {0, .5, 1, 1.5, 2, 3, 4, 6}
 __device__ __forceinline__ float e2m1_value(uint32_t i) {
