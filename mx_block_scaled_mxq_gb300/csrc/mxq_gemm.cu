@@ -443,6 +443,7 @@ __device__ __forceinline__ bool kblock_bf16_cg1(uint32_t d_tmem, uint32_t a_lo, 
 // Descriptors are assembled from per-stage 32-bit low words (start address
 // >> 4) and constant high words; +32 bytes of K is +2 in the low word.
 // Returns whether the next stage's data has landed.
+template <bool MC>
 __device__ __forceinline__ bool kblock_mxf8_cg1(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t sfa_t,
                                                 uint32_t sfb_t, uint32_t sa_lo, uint32_t sb_lo, uint32_t accumulate,
                                                 uint32_t bar_empty_s, uint32_t bar_full_next, uint32_t parity_next) {
@@ -450,53 +451,76 @@ __device__ __forceinline__ bool kblock_mxf8_cg1(uint32_t d_tmem, uint32_t a_lo, 
     constexpr uint32_t kSfHi = (128u >> 4) | (1u << 14);                 // SBO 128, version 1, no swizzle
     constexpr uint32_t kId0 = (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(128 >> 4) << 24);
     uint32_t ready;
-    asm volatile(
-        "{\n\t.reg .pred pn, pa, p1;\n\t.reg .b64 da, db, ds;\n\t.reg .b32 ta, tb, tt;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n\t"
-        "mov.b64 ds, {%9, %11};\n\t"
-        "tcgen05.cp.cta_group::1.32x128b.warpx4 [%7], ds;\n\t"
-        "mov.b64 ds, {%10, %11};\n\t"
-        "tcgen05.cp.cta_group::1.32x128b.warpx4 [%8], ds;\n\t"
-        "add.u32 tt, %10, 32;\n\t"
-        "mov.b64 ds, {tt, %11};\n\t"
-        "add.u32 tt, %8, 4;\n\t"
-        "tcgen05.cp.cta_group::1.32x128b.warpx4 [tt], ds;\n\t"
-        "setp.ne.b32 pa, %3, 0;\n\t"
-        "setp.eq.u32 p1, 0, 0;\n\t"
-        "mov.b64 da, {%5, %12};\n\t"
-        "mov.b64 db, {%6, %12};\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %13, [%7], [%8], pa;\n\t"
-        "add.u32 ta, %5, 2;\n\t"
-        "add.u32 tb, %6, 2;\n\t"
-        "mov.b64 da, {ta, %12};\n\t"
-        "mov.b64 db, {tb, %12};\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %14, [%7], [%8], p1;\n\t"
-        "add.u32 ta, %5, 4;\n\t"
-        "add.u32 tb, %6, 4;\n\t"
-        "mov.b64 da, {ta, %12};\n\t"
-        "mov.b64 db, {tb, %12};\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %15, [%7], [%8], p1;\n\t"
-        "add.u32 ta, %5, 6;\n\t"
-        "add.u32 tb, %6, 6;\n\t"
-        "mov.b64 da, {ta, %12};\n\t"
-        "mov.b64 db, {tb, %12};\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %16, [%7], [%8], p1;\n\t"
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%17];\n\t"
-        "selp.u32 %0, 1, 0, pn;\n\t}"
-        : "=r"(ready)
-        : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(sfa_t),
-          "r"(sfb_t), "r"(sa_lo), "r"(sb_lo), "n"(kSfHi), "n"(kAbHi), "n"(kId0), "n"(kId0 | (1u << 4) | (1u << 29)),
-          "n"(kId0 | (2u << 4) | (2u << 29)), "n"(kId0 | (3u << 4) | (3u << 29)), "r"(bar_empty_s)
-        : "memory");
+#define MXQ_KBLOCK_MXF8_BODY \
+    "{\n\t.reg .pred pn, pa, p1;\n\t.reg .b64 da, db, ds;\n\t.reg .b32 ta, tb, tt;\n\t" \
+    "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n\t" \
+    "mov.b64 ds, {%9, %11};\n\t" \
+    "tcgen05.cp.cta_group::1.32x128b.warpx4 [%7], ds;\n\t" \
+    "mov.b64 ds, {%10, %11};\n\t" \
+    "tcgen05.cp.cta_group::1.32x128b.warpx4 [%8], ds;\n\t" \
+    "add.u32 tt, %10, 32;\n\t" \
+    "mov.b64 ds, {tt, %11};\n\t" \
+    "add.u32 tt, %8, 4;\n\t" \
+    "tcgen05.cp.cta_group::1.32x128b.warpx4 [tt], ds;\n\t" \
+    "setp.ne.b32 pa, %3, 0;\n\t" \
+    "setp.eq.u32 p1, 0, 0;\n\t" \
+    "mov.b64 da, {%5, %12};\n\t" \
+    "mov.b64 db, {%6, %12};\n\t" \
+    "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %13, [%7], [%8], pa;\n\t" \
+    "add.u32 ta, %5, 2;\n\t" \
+    "add.u32 tb, %6, 2;\n\t" \
+    "mov.b64 da, {ta, %12};\n\t" \
+    "mov.b64 db, {tb, %12};\n\t" \
+    "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %14, [%7], [%8], p1;\n\t" \
+    "add.u32 ta, %5, 4;\n\t" \
+    "add.u32 tb, %6, 4;\n\t" \
+    "mov.b64 da, {ta, %12};\n\t" \
+    "mov.b64 db, {tb, %12};\n\t" \
+    "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %15, [%7], [%8], p1;\n\t" \
+    "add.u32 ta, %5, 6;\n\t" \
+    "add.u32 tb, %6, 6;\n\t" \
+    "mov.b64 da, {ta, %12};\n\t" \
+    "mov.b64 db, {tb, %12};\n\t" \
+    "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %16, [%7], [%8], p1;\n\t"
+    if constexpr (MC) {
+        // the stage is released in both CTAs of the cluster (B came to both)
+        asm volatile(MXQ_KBLOCK_MXF8_BODY
+                     "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%17], %18;\n\t"
+                     "selp.u32 %0, 1, 0, pn;\n\t}"
+                     : "=r"(ready)
+                     : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "r"(a_lo), "r"(b_lo),
+                       "r"(sfa_t), "r"(sfb_t), "r"(sa_lo), "r"(sb_lo), "n"(kSfHi), "n"(kAbHi), "n"(kId0),
+                       "n"(kId0 | (1u << 4) | (1u << 29)), "n"(kId0 | (2u << 4) | (2u << 29)),
+                       "n"(kId0 | (3u << 4) | (3u << 29)), "r"(bar_empty_s), "h"(static_cast<uint16_t>(3))
+                     : "memory");
+    } else {
+        asm volatile(MXQ_KBLOCK_MXF8_BODY
+                     "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%17];\n\t"
+                     "selp.u32 %0, 1, 0, pn;\n\t}"
+                     : "=r"(ready)
+                     : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "r"(a_lo), "r"(b_lo),
+                       "r"(sfa_t), "r"(sfb_t), "r"(sa_lo), "r"(sb_lo), "n"(kSfHi), "n"(kAbHi), "n"(kId0),
+                       "n"(kId0 | (1u << 4) | (1u << 29)), "n"(kId0 | (2u << 4) | (2u << 29)),
+                       "n"(kId0 | (3u << 4) | (3u << 29)), "r"(bar_empty_s)
+                     : "memory");
+    }
+#undef MXQ_KBLOCK_MXF8_BODY
     return ready != 0;
 }
 
-template <int CG, int KIND, bool BIAS>
+// MC (single-CTA tiles only): CTA pairs in a cluster take the two 128-row
+// halves of a 256-row tile; each CTA loads its half of B and multicasts it
+// to both, so B is read from L2 once per pair, and a stage is released only
+// when both CTAs' MMAs are done with it (commit multicast, empty count 2).
+template <int CG, int KIND, bool BIAS, bool MC = false>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                 const __grid_constant__ CUtensorMap tmC, const Params p) {
     using C = Cfg<CG>;
+    static_assert(!MC || (CG == 1 && KIND == kMXF8), "B multicast: single-CTA block-scaled tiles");
+    constexpr int TG = MC ? 2 : CG;               // tile geometry: 128 * TG rows per work unit
+    constexpr bool CLUSTER = CG == 2 || MC;       // CTAs work in pairs
     constexpr int STAGES = C::STAGES;
     // the epilogue's 64-column quarter after which the scale-slot columns are read
     constexpr int kHeadQuarter = (STAGES * SF_STRIDE - 1) / 64;
@@ -521,16 +545,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t bar_accf1 = bar_accf + 24, bar_acce1 = bar_accf + 32;
     const uint32_t bar_headf0 = bar_accf + 40, bar_headf1 = bar_accf + 48;
     uint32_t rank = 0;
-    if constexpr (CG == 2) rank = cluster_ctarank();
+    if constexpr (CLUSTER) rank = cluster_ctarank();
     const bool leader = rank == 0;
-    const int64_t first = CG == 2 ? blockIdx.x >> 1 : blockIdx.x;
-    const int64_t step = CG == 2 ? gridDim.x >> 1 : gridDim.x;
+    const int64_t first = CLUSTER ? blockIdx.x >> 1 : blockIdx.x;
+    const int64_t step = CLUSTER ? gridDim.x >> 1 : gridDim.x;
 
     // once any CTA has given up, the rest of the grid does no work
     if (threadIdx.x == 0) *abort_flag = *reinterpret_cast<volatile unsigned int *>(&g_device_error) != 0 ? 1 : 0;
     __syncthreads();
-    // (a CTA pair must pass its cluster barriers together, so only CG = 1 returns here)
-    if constexpr (CG == 1) {
+    // (a CTA pair must pass its cluster barriers together, so only lone CTAs return here)
+    if constexpr (!CLUSTER) {
         if (*abort_flag) return;  // before any TMEM allocation
     }
 
@@ -546,7 +570,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             for (int s = 0; s < STAGES; s++) {
                 mbar_init(bar_full + 8 * s, 1);
-                mbar_init(bar_empty + 8 * s, 1);
+                mbar_init(bar_empty + 8 * s, MC ? 2 : 1);  // MC: both CTAs' MMAs release a stage
             }
             mbar_init(bar_accf, 1);
             mbar_init(bar_accf1, 1);
@@ -568,13 +592,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
     tc_fence_before();
-    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    // (MC: the peer's barriers must be initialized before any multicast reaches them)
+    if constexpr (CLUSTER) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     GroupTables gt{nullptr, nullptr};
     if (p.mode != kDense && p.E <= kMaxTableE) {
         int64_t *off = reinterpret_cast<int64_t *>(smem + C::OFF_GRP), *pre = off + kMaxTableE + 1;
-        build_group_tables<CG>(p, off, pre, warp, lane);
+        build_group_tables<TG>(p, off, pre, warp, lane);
         __syncthreads();
         gt.off = off;
         gt.pre = pre;
@@ -592,7 +617,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------------------------------------------- TMA producer
         uint32_t g = 0;  // k-blocks issued by this CTA (lane 0)
         for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
-            const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
+            const TileInfo ti = resolve_tile<TG>(p, tile, lane, rank, gt);
             if (!ti.valid) break;  // grouped-row tiles past the real count come last
             int stop = 0;
             if (lane == 0) {
@@ -612,9 +637,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         (void)sfb_s;
                     } else if constexpr (CG == 1) {
                         const uint32_t fb = bar_full + 8 * s;
+                        // (MC: the peer's half of B also lands here and counts here)
                         mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + C::SFA_BYTES + 512u * ti.b_atoms);
                         tma_load_2d(sa_s, &tmA, fb, ka, static_cast<int>(ti.a_row0));
-                        tma_load_2d(sb_s, &tmB, fb, kb_, static_cast<int>(ti.b_row0));
+                        if constexpr (MC)
+                            tma_load_2d_mc(sb_s + rank * (C::B_BYTES / 2), &tmB, fb, kb_, static_cast<int>(ti.b_row0),
+                                           3);
+                        else
+                            tma_load_2d(sb_s, &tmB, fb, kb_, static_cast<int>(ti.b_row0));
                         bulk_load(sfa_s, p.sa + (ti.a_ratom * p.sa_kt + ti.a_katom0 + kb) * 512, 512, fb);
                         for (int h = 0; h < ti.b_atoms; h++)
                             bulk_load(sfb_s + 512 * h, p.sb + ((ti.b_ratom + h) * p.sb_kt + ti.b_katom0 + kb) * 512,
@@ -639,8 +669,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
         }
+        if constexpr (MC) {
+            // every release of this CTA's last stages, the peer's included, has
+            // arrived before the CTA can leave (the peer's commits target this
+            // CTA's barriers); bounded
+            if (lane == 0 && !*abort_flag)
+                for (uint32_t j = g > STAGES ? g - STAGES : 0; j < g; j++)
+                    mbar_wait_drain(bar_empty + 8 * (j % STAGES), (j / STAGES) & 1);
+        }
         if (lane == 0 && *abort_flag) {  // let this CTA's copies land before it exits
-            if constexpr (CG == 1) {
+            if constexpr (MC) {
+                // own loads and the peer's multicasts land on this CTA's barriers;
+                // a peer that stopped may never send its half, so wait bounded
+                for (uint32_t j = g > STAGES ? g - STAGES : 0; j < g; j++)
+                    mbar_wait_drain(bar_full + 8 * (j % STAGES), (j / STAGES) & 1);
+                spin_ns(2000000);
+            } else if constexpr (CG == 1) {
                 for (uint32_t j = g > STAGES ? g - STAGES : 0; j < g; j++)
                     mbar_wait_drain(bar_full + 8 * (j % STAGES), (j / STAGES) & 1);
             } else {
@@ -656,7 +700,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t a_lo0 = (sbase + C::OFF_A) >> 4, b_lo0 = (sbase + C::OFF_B) >> 4;
             const uint32_t sa_lo0 = (sbase + C::OFF_SFA) >> 4, sb_lo0 = (sbase + C::OFF_SFB) >> 4;
             for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
-                const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
+                const TileInfo ti = resolve_tile<TG>(p, tile, lane, rank, gt);
                 if (!ti.valid) break;
                 if (ti.nkb == 0) continue;  // empty group: the epilogue writes zeros
                 int stop = 0;
@@ -693,7 +737,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                         bar_empty + 8 * s, bar_full + 8 * s1, ph1);
                             } else {
                                 const uint32_t sf_t = sf_base + s * SF_STRIDE;
-                                ready = kblock_mxf8_cg1(d_tmem, a_lo0 + s * (C::A_BYTES >> 4),
+                                ready = kblock_mxf8_cg1<MC>(d_tmem, a_lo0 + s * (C::A_BYTES >> 4),
                                                         b_lo0 + s * (C::B_BYTES >> 4), sf_t, sf_t + 4,
                                                         sa_lo0 + s * (C::SFA_BYTES >> 4),
                                                         sb_lo0 + s * (C::SFB_BYTES >> 4), kb0 != 0 ? 1u : 0u,
@@ -750,6 +794,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 tc_mma_mxf8(d_tmem, ad, bd, make_idesc<CG, KIND>(j), sfa_t, sfb_t, acc);
                         }
                         if constexpr (CG == 2) tc_commit_pair_mc(bar_empty + 8 * s, 3);
+                        else if constexpr (MC) tc_commit_mc(bar_empty + 8 * s, 3);
                         else tc_commit(bar_empty + 8 * s);
                         ready = false;
                     }
@@ -776,7 +821,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t st_slots = sbase + C::OFF_STORE + 2 * 2048 * sub;  // this warp's two staging slots
         uint32_t st_count = 0;                                            // blocks this warp has stored
         for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
-            const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
+            const TileInfo ti = resolve_tile<TG>(p, tile, lane, rank, gt);
             if (!ti.valid) break;
             const int64_t grow = ti.out_row0 + 32 * sub + lane;
             const bool row_ok = grow >= ti.row_lo && grow < ti.row_hi;
@@ -943,7 +988,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp >= 2 && lane == 0) bulk_wait_all();  // staged stores done before shared memory goes away
     tc_fence_before();
-    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    if constexpr (CLUSTER) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         if constexpr (CG == 2) tmem_dealloc_pair(tmem, TMEM_COLS);
@@ -1025,19 +1070,31 @@ int cta_group_for(const GemmProblem &) {
     return forced == 2 ? 2 : 1;
 }
 
-template <int CG, int KIND, bool BIAS>
+// B multicast across CTA pairs for dense and weight-gradient problems (whose
+// M tiles of one N tile share B); MXQ_GEMM_MC=0 turns it off.
+bool b_multicast_for(const GemmProblem &g) {
+    static int enabled = [] {
+        const char *v = getenv("MXQ_GEMM_MC");
+        return v ? atoi(v) : 1;
+    }();
+    return enabled != 0 && (g.mode == kDense || g.mode == kGroupedK);
+}
+
+template <int CG, int KIND, bool BIAS, bool MC = false>
 cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     using C = Cfg<CG>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(k_gemm<CG, KIND, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        attr_err = cudaFuncSetAttribute(k_gemm<CG, KIND, BIAS, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
     CUtensorMap tmA, tmB, tmSA, tmSB, tmC;
     const int64_t esz = KIND == kBF16 ? 2 : 1;  // operand bytes per element (tensor maps run over bytes)
-    if (!make_tmap(&tmA, g.a, g.a_rows, esz * g.a_k, C::BM) || !make_tmap(&tmB, g.b, g.b_rows, esz * g.b_k, C::B_ROWS))
+    // (MC: each CTA loads a 128-row half of B)
+    if (!make_tmap(&tmA, g.a, g.a_rows, esz * g.a_k, C::BM) ||
+        !make_tmap(&tmB, g.b, g.b_rows, esz * g.b_k, MC ? C::B_ROWS / 2 : C::B_ROWS))
         return cudaErrorInvalidValue;
     if (CG == 2) {
         if (!make_scale_tmap(&tmSA, g.sa, scale_bytes_of(g.a_rows, g.a_k)) ||
@@ -1047,7 +1104,8 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         tmSA = tmA;  // unused
         tmSB = tmB;
     }
-    p.m_tiles = static_cast<int>((g.M + C::TILE_M - 1) / C::TILE_M);
+    constexpr int64_t kUnitRows = MC ? 2 * C::TILE_M : C::TILE_M;  // rows per CTA (pair)
+    p.m_tiles = static_cast<int>((g.M + kUnitRows - 1) / kUnitRows);
     // output tensor map for the epilogue's TMA stores (all experts' outputs
     // stacked for the grouped weight gradient); without one (ldc not a
     // multiple of 8, or rows past the 32-bit TMA coordinate range) every
@@ -1057,7 +1115,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     p.vec_store = (g.ldc % 8 == 0 && (reinterpret_cast<uintptr_t>(g.c) & 15) == 0) ? 1 : 0;
     if (!p.tma_store) tmC = tmA;  // unused
     if (g.mode == kDense) p.total_tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    else if (g.mode == kGroupedRows) p.total_tiles = ((g.T + C::TILE_M - 1) / C::TILE_M + g.E) * p.n_tiles;
+    else if (g.mode == kGroupedRows) p.total_tiles = ((g.T + kUnitRows - 1) / kUnitRows + g.E) * p.n_tiles;
     else p.total_tiles = static_cast<int64_t>(g.E) * p.m_tiles * p.n_tiles;
     if (p.total_tiles <= 0) return cudaSuccess;
 
@@ -1073,7 +1131,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cfg.stream = st;
-    if (CG == 2) {
+    if (CG == 2 || MC) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
@@ -1082,10 +1140,10 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         cfg.numAttrs = 1;
     }
     if (resident[dev] == 0) {
-        if (CG == 2) {
+        if (CG == 2 || MC) {
             cfg.gridDim = dim3(2);
             int clusters = 0;
-            e = cudaOccupancyMaxActiveClusters(&clusters, k_gemm<CG, KIND, BIAS>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&clusters, k_gemm<CG, KIND, BIAS, MC>, &cfg);
             if (e != cudaSuccess) return e;
             resident[dev] = clusters > 0 ? clusters : 1;
         } else {
@@ -1094,8 +1152,8 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         }
     }
     const int64_t units = p.total_tiles < resident[dev] ? p.total_tiles : resident[dev];
-    cfg.gridDim = dim3(static_cast<unsigned>(units * CG));
-    return cudaLaunchKernelEx(&cfg, k_gemm<CG, KIND, BIAS>, tmA, tmB, tmSA, tmSB, tmC, p);
+    cfg.gridDim = dim3(static_cast<unsigned>(units * (MC ? 2 : CG)));
+    return cudaLaunchKernelEx(&cfg, k_gemm<CG, KIND, BIAS, MC>, tmA, tmB, tmSA, tmSB, tmC, p);
 }
 
 }  // namespace
@@ -1184,7 +1242,8 @@ cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
         return p.bias ? launch_cg<1, kBF16, true>(g, p, st) : launch_cg<1, kBF16, false>(g, p, st);
     }
     if (p.bias) return launch_cg<1, kMXF8, true>(g, p, st);
-    return cta_group_for(g) == 2 ? launch_cg<2, kMXF8, false>(g, p, st) : launch_cg<1, kMXF8, false>(g, p, st);
+    if (cta_group_for(g) == 2) return launch_cg<2, kMXF8, false>(g, p, st);
+    return b_multicast_for(g) ? launch_cg<1, kMXF8, false, true>(g, p, st) : launch_cg<1, kMXF8, false>(g, p, st);
 }
 
 }  // namespace mxq
