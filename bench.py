@@ -52,8 +52,8 @@ GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f
 # full-size launches (profiles/k_gemm__bench_launches_dram.md), keyed by a
 # hash of the kernel source; when the source has changed since, traffic is null.
 GEMM_DRAM_TRAFFIC = {
-    "3beaad66eca8b7ca": {"linear_dw_gemm": 259180032, "moe_fwd_gemm": 1493929472,
-                         "moe_dx_gemm": 1531132672, "moe_dw_gemm": 2234405376},
+    "d2891f5f9bd48727": {"linear_dw_gemm": 287821568, "moe_fwd_gemm": 1499957504,
+                         "moe_dx_gemm": 1531104768, "moe_dw_gemm": 2236594688},
 }
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
@@ -526,7 +526,8 @@ def main():
         "data": "synthetic (seeded: N(0,1) X, N(0,0.02) W, N(0,1e-3) dY; Dirichlet(0.5) groups; t(3) MXFP4 input)",
         "config": {"workload": WORKLOAD, "mode": args.mode, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (step touches > 8 GB)", "step_gemm_flop": STEP_FLOP},
-        "roofline": {"bound": "tensor", "kernel": "k_gemm<1,MXF8,0> (tcgen05 kind::mxf8f6f4)",
+        "roofline": {"bound": "tensor",
+                     "kernel": "k_gemm<1,MXF8,0,MC> (tcgen05 kind::mxf8f6f4; B-multicast CTA pairs for dense and dW)",
                      "achieved": round(achieved, 1) if achieved else None,
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / fp8_peak, 4) if achieved else None,
