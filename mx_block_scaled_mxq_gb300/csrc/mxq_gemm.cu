@@ -35,6 +35,10 @@
 // deeper ring hides more load latency.  Each CTA holds its own rows' A scales
 // and all of B's scales; every load of both CTAs completes on the even CTA's
 // stage barrier.
+// MC (B multicast, CG = 1, dense and weight-gradient problems): a cluster of
+// two single-CTA tiles takes the two 128-row halves of a 256-row work unit;
+// each CTA multicasts its 128-row half of the B tile into both CTAs, so L2
+// serves B once per pair, and a stage is freed by both CTAs' MMA commits.
 // TMEM: two accumulator banks of 256 columns; a tile in one bank keeps the
 // scale slots of stage s in columns [16 s, 16 s + 12) of the other bank
 // (A: 4 columns, B: 2 x 4 columns).  Every wait is bounded (mxq_device.cuh).
