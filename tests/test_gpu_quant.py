@@ -266,6 +266,21 @@ def test_grouped_dual_quant_bit_exact(mxq, sizes, C):
     assert np.array_equal(sT, oracle.swizzle_scales(osT))
 
 
+def test_grouped_dual_quant_300_groups(mxq):
+    """More groups than the kernel keeps in shared-memory tables (256): the
+    per-tile group lookup scans the offsets in global memory instead."""
+    sizes = np.random.default_rng(300).integers(0, 40, size=300)
+    off = mxq_inputs.offsets_from_sizes(sizes)
+    x = _inputs(int(off[-1]), 64, "heavy", seed=300)
+    q, s, qT, sT, t_pad = _grouped_dual(mxq, x, off)
+    oq, os_ = oracle.mxfp8_quant_rows(x)
+    assert np.array_equal(q, oq)
+    assert np.array_equal(s, oracle.swizzle_scales(os_))
+    oqT, osT = oracle.mxfp8_quant_cols_grouped(x, off, t_pad)
+    assert np.array_equal(qT, oqT)
+    assert np.array_equal(sT, oracle.swizzle_scales(osT))
+
+
 def test_grouped_dual_quant_full_size_moe_dy(mxq):
     """The MoE layer's dY, 32768 x 4096 bf16 in 32 Dirichlet(0.5) groups: every
     byte of the four outputs against the oracle."""
