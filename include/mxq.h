@@ -115,9 +115,9 @@ mxq_status mxq_quantize(const void *x, mxq_dtype dtype, int64_t rows, int64_t co
 /* Per-group column MXFP8 quant for the grouped weight gradient ([TT] MoE
  * MXFP8 mode, "grouped dynamic MX quant"): x bf16 [rows x cols] (leading
  * dim cols), group e = rows [off[e], off[e+1]) with d_offsets a DEVICE array
- * of E+1 int64 (non-decreasing, off[0] = 0, off[E] = rows; not checked on the
- * device).  Blocks of 32 rows restart at every group start and a group's last
- * block is zero-padded.  Group e is written at padded column P_e =
+ * of E+1 int64 (non-decreasing, off[0] = 0, off[E] = rows; checked on the
+ * device as described below).  Blocks of 32 rows restart at every group
+ * start and a group's last block is zero-padded.  Group e is written at padded column P_e =
  * sum_{j<e} ceil128(n_j) of q_colT [cols x t_pad] (leading dim t_pad) and its
  * scales into s_colT swz(cols, t_pad/32).  Every byte of both outputs is
  * written (padding = 0).  t_pad % 128 == 0 and
@@ -126,6 +126,24 @@ mxq_status mxq_quantize(const void *x, mxq_dtype dtype, int64_t rows, int64_t co
 mxq_status mxq_quantize_grouped_col(const void *x_bf16, int64_t rows, int64_t cols,
                                     const int64_t *d_offsets, int E, int64_t t_pad,
                                     void *q_colT, void *s_colT, mxq_stream_t stream);
+
+/* Group offsets, as every grouped entry point takes them: E+1 int64 values
+ * with off[0] = 0, off[e] <= off[e+1] and off[E] = T (the number of token
+ * rows); group e is rows [off[e], off[e+1]) and may be empty.  ([TT] MoE
+ * MXFP8 mode: the token counts per expert that the grouped matmul splits its
+ * rows by.)
+ * Every grouped kernel checks its DEVICE offsets before it reads or writes
+ * anything that depends on them.  Malformed offsets make the kernel skip all
+ * of its work (its outputs are left unwritten) and set bit 2 of the device
+ * error word, which mxq_poll_device_error reports as MXQ_ERR_INVALID_ARG;
+ * no access outside the caller's buffers happens.
+ * mxq_validate_group_offsets applies the same rule to a HOST copy and returns
+ * MXQ_ERR_INVALID_ARG with the first violation in mxq_last_error_string()
+ * (no CUDA call).  mxq_check_group_offsets launches, on `stream`, one warp
+ * that reads d_offsets[0..E] and nothing else and sets the same bit when they
+ * are malformed. */
+mxq_status mxq_validate_group_offsets(const int64_t *offsets, int E, int64_t T);
+mxq_status mxq_check_group_offsets(const int64_t *d_offsets, int E, int64_t T, mxq_stream_t stream);
 
 /* Grouped dual-axis MXFP8 quant: the per-group column quant above and the
  * plain row quant of the same x from one read of x, as the MoE layer needs
@@ -347,10 +365,11 @@ mxq_status mxq_linear_fwd_noalloc(const void *x, const void *w, int64_t M, int64
 const char *mxq_last_error_string(void);
 
 /* Synchronizes the current device, then reads and clears the device-side
- * error word that kernels set when a wait gives up (bit 0: an mbarrier wait
- * timed out; bit 1: a tensor-memory allocation failed).  Returns
- * MXQ_ERR_TIMEOUT if any bit was set (*word receives the bits), MXQ_OK
- * otherwise.  word may be NULL. */
+ * error word that kernels set when they give up (bit 0: an mbarrier wait
+ * timed out; bit 1: a tensor-memory allocation failed; bit 2: a grouped
+ * kernel found its group offsets malformed and did no work).  Returns
+ * MXQ_ERR_INVALID_ARG if bit 2 was set, else MXQ_ERR_TIMEOUT if any bit was
+ * set (*word receives the bits), MXQ_OK otherwise.  word may be NULL. */
 mxq_status mxq_poll_device_error(uint32_t *word);
 
 /* Failure-detection self-test (no counterpart on the pages): launches one

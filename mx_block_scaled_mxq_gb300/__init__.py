@@ -31,7 +31,7 @@ __all__ = [
     "mxq_mxfp4_ste_forward", "mxq_mxfp4_ste_backward", "mxfp4_ste_forward", "mxfp4_ste_backward",
     "mxq_qat_linear_workspace_bytes", "mxq_qat_linear_fwd", "qat_linear_fwd", "mxq_qdq_mxfp4_bf16",
     "mxq_linear_weight_cache_bytes", "mxq_linear_wq_ctx_bytes", "mxq_linear_quantize_weight", "mxq_linear_fwd_wq",
-    "mxq_linear_bwd_dx_wq", "mxq_selftest_wait_timeout",
+    "mxq_linear_bwd_dx_wq", "mxq_selftest_wait_timeout", "mxq_validate_group_offsets", "mxq_check_group_offsets",
 ]
 
 BF16, F32 = 0, 1
@@ -81,6 +81,8 @@ _SIGNATURES = {
     "mxq_last_error_string": (ctypes.c_char_p, []),
     "mxq_poll_device_error": (_I32, [ctypes.POINTER(ctypes.c_uint32)]),
     "mxq_selftest_wait_timeout": (_I32, [ctypes.c_uint32, _P, _P]),
+    "mxq_validate_group_offsets": (_I32, [_P, _I32, _I64]),
+    "mxq_check_group_offsets": (_I32, [_P, _I32, _I64, _P]),
 }
 
 
@@ -245,12 +247,27 @@ def mxq_selftest_wait_timeout(timeout_ms, d_gave_up, stream=None):
 
 
 def mxq_poll_device_error():
-    """Returns the device error bits (0 = none); raises on a CUDA failure."""
+    """Returns the device error bits (0 = none; bit 2 = malformed group
+    offsets); raises on a CUDA failure."""
     w = ctypes.c_uint32(0)
     st = load().mxq_poll_device_error(ctypes.byref(w))
-    if st not in (0, 5):
+    if st not in (0, 1, 5) or (st == 1 and not w.value & 4):
         _check(st, "mxq_poll_device_error")
     return int(w.value)
+
+
+def mxq_validate_group_offsets(offsets, E, T):
+    """Host-side check of group offsets (a host int64 array of E+1 values);
+    raises MXQError (MXQ_ERR_INVALID_ARG) with the first violation."""
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+    if a.size < E + 1:
+        raise ValueError("offsets holds fewer than E+1 values")
+    _check(load().mxq_validate_group_offsets(a.ctypes.data, E, T), "mxq_validate_group_offsets")
+
+
+def mxq_check_group_offsets(d_offsets, E, T, stream=None):
+    _check(load().mxq_check_group_offsets(_p(d_offsets), E, T, _s(stream)), "mxq_check_group_offsets")
 
 
 # ---------------------------------------------------------------- allocation helpers

@@ -171,8 +171,38 @@ mxq_status mxq_poll_device_error(uint32_t *word) {
     e = mxq::read_and_clear_device_error(&w);
     if (e != cudaSuccess) return fail(MXQ_ERR_CUDA, "read device error word: %s", cudaGetErrorString(e));
     if (word) *word = w;
+    if (w & 4u)
+        return fail(MXQ_ERR_INVALID_ARG,
+                    "a grouped kernel found its group offsets malformed (they must rise from off[0] = 0 to "
+                    "off[E] = T without decreasing) and skipped its work (device error bits 0x%x)",
+                    w);
     if (w) return fail(MXQ_ERR_TIMEOUT, "a kernel reported device error bits 0x%x", w);
     return ok();
+}
+
+mxq_status mxq_validate_group_offsets(const int64_t *offsets, int E, int64_t T) {
+    if (!offsets) return fail(MXQ_ERR_INVALID_ARG, "offsets is null");
+    if (E < 1 || E > 4096) return fail(MXQ_ERR_INVALID_ARG, "E must be in [1, 4096]");
+    if (T < 0) return fail(MXQ_ERR_INVALID_ARG, "T must be >= 0");
+    if (offsets[0] != 0) return fail(MXQ_ERR_INVALID_ARG, "off[0] = %lld, must be 0", (long long)offsets[0]);
+    for (int e = 0; e < E; e++)
+        if (offsets[e + 1] < offsets[e])
+            return fail(MXQ_ERR_INVALID_ARG, "off[%d] = %lld < off[%d] = %lld: offsets must not decrease", e + 1,
+                        (long long)offsets[e + 1], e, (long long)offsets[e]);
+    if (offsets[E] != T)
+        return fail(MXQ_ERR_INVALID_ARG, "off[E] = %lld, must equal T = %lld", (long long)offsets[E], (long long)T);
+    return ok();
+}
+
+mxq_status mxq_check_group_offsets(const int64_t *d_offsets, int E, int64_t T, mxq_stream_t stream) {
+    if (!d_offsets || (reinterpret_cast<uintptr_t>(d_offsets) & 7))
+        return fail(MXQ_ERR_INVALID_ARG, "d_offsets must be a non-null 8-byte aligned device pointer");
+    if (E < 1 || E > 4096) return fail(MXQ_ERR_INVALID_ARG, "E must be in [1, 4096]");
+    if (T < 0) return fail(MXQ_ERR_INVALID_ARG, "T must be >= 0");
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    return cuda_result(mxq::launch_check_offsets(d_offsets, E, T, reinterpret_cast<cudaStream_t>(stream)),
+                       "mxq_check_group_offsets launch");
 }
 
 mxq_status mxq_quantize(const void *x, mxq_dtype dtype, int64_t rows, int64_t cols, int64_t ldx, int axis,
@@ -371,6 +401,7 @@ mxq_status mxq_grouped_gemm(mxq_gg_kind kind, const uint8_t *a, const uint8_t *s
             return fail(MXQ_ERR_INVALID_ARG, "t_pad must be a multiple of 128 and >= mxq_grouped_padded_rows(T, E)");
         if (t_pad > (1ll << 31)) return fail(MXQ_ERR_UNSUPPORTED, "t_pad above 2^31");
         g.mode = mxq::kGroupedK;
+        g.T = T;
         g.a = a; g.sa = sa; g.a_rows = N; g.a_k = t_pad;
         g.b = b; g.sb = sb; g.b_rows = K; g.b_k = t_pad;
         g.M = N; g.N = K; g.ldc = K;

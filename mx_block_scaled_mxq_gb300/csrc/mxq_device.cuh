@@ -11,8 +11,10 @@ namespace mxq {
 
 // Bits of the device-side error word a kernel sets when it gives up.
 // Bit 0: a bounded wait timed out.  Bit 1: a tensor-memory allocation failed.
+// Bit 2: a grouped kernel found its group offsets malformed and did no work.
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrTmemAlloc = 2u;
+constexpr unsigned kErrBadOffsets = 4u;
 constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;  // 4 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -80,6 +82,21 @@ __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, vol
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           unsigned int *err) {
     return mbar_wait_for(bar, parity, abort, err, kWaitTimeoutNs);
+}
+
+// Group offsets off[0..E] are well formed when off[0] == 0, off[e] <= off[e+1]
+// for every e, and off[E] == T; together these put every offset in [0, T].
+// Run by all 32 lanes of one warp, which read off[0..E] and nothing else; the
+// result is the same in every lane.  Every grouped kernel calls this before
+// anything it does depends on an offset.
+__device__ __forceinline__ bool group_offsets_valid(const int64_t *off, int E, int64_t T, int lane) {
+    bool ok = true;
+    for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        if (e < E) ok = ok && off[e] <= off[e + 1];
+    }
+    if (lane == 0) ok = ok && off[0] == 0 && off[E] == T;
+    return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------- TMA / bulk copies
@@ -197,25 +214,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
         : "memory");
-}
-// TMA load of a 2-D box multicast to the CTAs of `mask` in the cluster: the box
-// lands at the same shared-memory offset `dst` in each of them and completes
-// on the mbarrier at offset `bar` in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, uint32_t bar, int x, int y,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-        : "memory");
-}
-// Single-CTA commit whose arrival goes to the mbarrier at offset `bar` in
-// each CTA of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
-                     "r"(bar),
-                 "h"(mask)
-                 : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");

@@ -35,10 +35,8 @@
 // deeper ring hides more load latency.  Each CTA holds its own rows' A scales
 // and all of B's scales; every load of both CTAs completes on the even CTA's
 // stage barrier.
-// MC (B multicast, CG = 1, dense and weight-gradient problems): a cluster of
-// two single-CTA tiles takes the two 128-row halves of a 256-row work unit;
-// each CTA multicasts its 128-row half of the B tile into both CTAs, so L2
-// serves B once per pair, and a stage is freed by both CTAs' MMA commits.
+// Every TMA load lands in the shared memory of the CTA that issues it (no
+// cluster multicast).
 // TMEM: two accumulator banks of 256 columns; a tile in one bank keeps the
 // scale slots of stage s in columns [16 s, 16 s + 12) of the other bank
 // (A: 4 columns, B: 2 x 4 columns).  Every wait is bounded (mxq_device.cuh).
@@ -101,6 +99,7 @@ struct Params {
     int64_t M, N, ldc, K;
     const int64_t *offsets;
     int E;
+    int64_t T;                         // grouped modes: token rows, the value off[E] must hold
     int64_t b_row_per_expert, b_k_per_expert, c_expert_stride;
     int m_tiles, n_tiles;  // tile counts (m in units of 128 * CG rows)
     int n_fastest;         // kDense tile order: 1 = n fastest (A is the larger operand)
@@ -447,7 +446,6 @@ __device__ __forceinline__ bool kblock_bf16_cg1(uint32_t d_tmem, uint32_t a_lo, 
 // Descriptors are assembled from per-stage 32-bit low words (start address
 // >> 4) and constant high words; +32 bytes of K is +2 in the low word.
 // Returns whether the next stage's data has landed.
-template <bool MC>
 __device__ __forceinline__ bool kblock_mxf8_cg1(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t sfa_t,
                                                 uint32_t sfb_t, uint32_t sa_lo, uint32_t sb_lo, uint32_t accumulate,
                                                 uint32_t bar_empty_s, uint32_t bar_full_next, uint32_t parity_next) {
@@ -486,45 +484,26 @@ __device__ __forceinline__ bool kblock_mxf8_cg1(uint32_t d_tmem, uint32_t a_lo, 
     "mov.b64 da, {ta, %12};\n\t" \
     "mov.b64 db, {tb, %12};\n\t" \
     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%4], da, db, %16, [%7], [%8], p1;\n\t"
-    if constexpr (MC) {
-        // the stage is released in both CTAs of the cluster (B came to both)
-        asm volatile(MXQ_KBLOCK_MXF8_BODY
-                     "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%17], %18;\n\t"
-                     "selp.u32 %0, 1, 0, pn;\n\t}"
-                     : "=r"(ready)
-                     : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "r"(a_lo), "r"(b_lo),
-                       "r"(sfa_t), "r"(sfb_t), "r"(sa_lo), "r"(sb_lo), "n"(kSfHi), "n"(kAbHi), "n"(kId0),
-                       "n"(kId0 | (1u << 4) | (1u << 29)), "n"(kId0 | (2u << 4) | (2u << 29)),
-                       "n"(kId0 | (3u << 4) | (3u << 29)), "r"(bar_empty_s), "h"(static_cast<uint16_t>(3))
-                     : "memory");
-    } else {
-        asm volatile(MXQ_KBLOCK_MXF8_BODY
-                     "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%17];\n\t"
-                     "selp.u32 %0, 1, 0, pn;\n\t}"
-                     : "=r"(ready)
-                     : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "r"(a_lo), "r"(b_lo),
-                       "r"(sfa_t), "r"(sfb_t), "r"(sa_lo), "r"(sb_lo), "n"(kSfHi), "n"(kAbHi), "n"(kId0),
-                       "n"(kId0 | (1u << 4) | (1u << 29)), "n"(kId0 | (2u << 4) | (2u << 29)),
-                       "n"(kId0 | (3u << 4) | (3u << 29)), "r"(bar_empty_s)
-                     : "memory");
-    }
+    asm volatile(MXQ_KBLOCK_MXF8_BODY
+                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%17];\n\t"
+                 "selp.u32 %0, 1, 0, pn;\n\t}"
+                 : "=r"(ready)
+                 : "r"(bar_full_next), "r"(parity_next), "r"(accumulate), "r"(d_tmem), "r"(a_lo), "r"(b_lo),
+                   "r"(sfa_t), "r"(sfb_t), "r"(sa_lo), "r"(sb_lo), "n"(kSfHi), "n"(kAbHi), "n"(kId0),
+                   "n"(kId0 | (1u << 4) | (1u << 29)), "n"(kId0 | (2u << 4) | (2u << 29)),
+                   "n"(kId0 | (3u << 4) | (3u << 29)), "r"(bar_empty_s)
+                 : "memory");
 #undef MXQ_KBLOCK_MXF8_BODY
     return ready != 0;
 }
 
-// MC (single-CTA tiles only): CTA pairs in a cluster take the two 128-row
-// halves of a 256-row tile; each CTA loads its half of B and multicasts it
-// to both, so B is read from L2 once per pair, and a stage is released only
-// when both CTAs' MMAs are done with it (commit multicast, empty count 2).
-template <int CG, int KIND, bool BIAS, bool MC = false>
+template <int CG, int KIND, bool BIAS>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                 const __grid_constant__ CUtensorMap tmC, const Params p) {
     using C = Cfg<CG>;
-    static_assert(!MC || (CG == 1 && KIND == kMXF8), "B multicast: single-CTA block-scaled tiles");
-    constexpr int TG = MC ? 2 : CG;               // tile geometry: 128 * TG rows per work unit
-    constexpr bool CLUSTER = CG == 2 || MC;       // CTAs work in pairs
+    constexpr bool CLUSTER = CG == 2;             // CTAs work in pairs
     constexpr int STAGES = C::STAGES;
     // the epilogue's 64-column quarter after which the scale-slot columns are read
     constexpr int kHeadQuarter = (STAGES * SF_STRIDE - 1) / 64;
@@ -574,7 +553,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             for (int s = 0; s < STAGES; s++) {
                 mbar_init(bar_full + 8 * s, 1);
-                mbar_init(bar_empty + 8 * s, MC ? 2 : 1);  // MC: both CTAs' MMAs release a stage
+                mbar_init(bar_empty + 8 * s, 1);
             }
             mbar_init(bar_accf, 1);
             mbar_init(bar_accf1, 1);
@@ -596,14 +575,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
     tc_fence_before();
-    // (MC: the peer's barriers must be initialized before any multicast reaches them)
     if constexpr (CLUSTER) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     GroupTables gt{nullptr, nullptr};
-    if (p.mode != kDense && p.E <= kMaxTableE) {
+    if (p.mode != kDense) {
+        // malformed offsets: no tile is decoded from them, no load or store is issued
+        if (warp == 0 && !group_offsets_valid(p.offsets, p.E, p.T, lane) && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(&g_device_error, kErrBadOffsets);
+        }
+        __syncthreads();
+    }
+    if (p.mode != kDense && p.E <= kMaxTableE && !*abort_flag) {
         int64_t *off = reinterpret_cast<int64_t *>(smem + C::OFF_GRP), *pre = off + kMaxTableE + 1;
-        build_group_tables<TG>(p, off, pre, warp, lane);
+        build_group_tables<CG>(p, off, pre, warp, lane);
         __syncthreads();
         gt.off = off;
         gt.pre = pre;
@@ -621,7 +607,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------------------------------------------- TMA producer
         uint32_t g = 0;  // k-blocks issued by this CTA (lane 0)
         for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
-            const TileInfo ti = resolve_tile<TG>(p, tile, lane, rank, gt);
+            const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
             if (!ti.valid) break;  // grouped-row tiles past the real count come last
             int stop = 0;
             if (lane == 0) {
@@ -641,14 +627,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         (void)sfb_s;
                     } else if constexpr (CG == 1) {
                         const uint32_t fb = bar_full + 8 * s;
-                        // (MC: the peer's half of B also lands here and counts here)
                         mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + C::SFA_BYTES + 512u * ti.b_atoms);
                         tma_load_2d(sa_s, &tmA, fb, ka, static_cast<int>(ti.a_row0));
-                        if constexpr (MC)
-                            tma_load_2d_mc(sb_s + rank * (C::B_BYTES / 2), &tmB, fb, kb_, static_cast<int>(ti.b_row0),
-                                           3);
-                        else
-                            tma_load_2d(sb_s, &tmB, fb, kb_, static_cast<int>(ti.b_row0));
+                        tma_load_2d(sb_s, &tmB, fb, kb_, static_cast<int>(ti.b_row0));
                         bulk_load(sfa_s, p.sa + (ti.a_ratom * p.sa_kt + ti.a_katom0 + kb) * 512, 512, fb);
                         for (int h = 0; h < ti.b_atoms; h++)
                             bulk_load(sfb_s + 512 * h, p.sb + ((ti.b_ratom + h) * p.sb_kt + ti.b_katom0 + kb) * 512,
@@ -673,22 +654,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
         }
-        if constexpr (MC) {
-            // every release of this CTA's last stages, the peer's included, has
-            // arrived before the CTA can leave (the peer's commits target this
-            // CTA's barriers); bounded
-            if (lane == 0 && !*abort_flag)
-                for (uint32_t j = g > STAGES ? g - STAGES : 0; j < g; j++)
-                    mbar_wait_drain(bar_empty + 8 * (j % STAGES), (j / STAGES) & 1);
-        }
         if (lane == 0 && *abort_flag) {  // let this CTA's copies land before it exits
-            if constexpr (MC) {
-                // own loads and the peer's multicasts land on this CTA's barriers;
-                // a peer that stopped may never send its half, so wait bounded
-                for (uint32_t j = g > STAGES ? g - STAGES : 0; j < g; j++)
-                    mbar_wait_drain(bar_full + 8 * (j % STAGES), (j / STAGES) & 1);
-                spin_ns(2000000);
-            } else if constexpr (CG == 1) {
+            if constexpr (CG == 1) {
                 for (uint32_t j = g > STAGES ? g - STAGES : 0; j < g; j++)
                     mbar_wait_drain(bar_full + 8 * (j % STAGES), (j / STAGES) & 1);
             } else {
@@ -704,7 +671,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t a_lo0 = (sbase + C::OFF_A) >> 4, b_lo0 = (sbase + C::OFF_B) >> 4;
             const uint32_t sa_lo0 = (sbase + C::OFF_SFA) >> 4, sb_lo0 = (sbase + C::OFF_SFB) >> 4;
             for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
-                const TileInfo ti = resolve_tile<TG>(p, tile, lane, rank, gt);
+                const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
                 if (!ti.valid) break;
                 if (ti.nkb == 0) continue;  // empty group: the epilogue writes zeros
                 int stop = 0;
@@ -741,7 +708,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                         bar_empty + 8 * s, bar_full + 8 * s1, ph1);
                             } else {
                                 const uint32_t sf_t = sf_base + s * SF_STRIDE;
-                                ready = kblock_mxf8_cg1<MC>(d_tmem, a_lo0 + s * (C::A_BYTES >> 4),
+                                ready = kblock_mxf8_cg1(d_tmem, a_lo0 + s * (C::A_BYTES >> 4),
                                                         b_lo0 + s * (C::B_BYTES >> 4), sf_t, sf_t + 4,
                                                         sa_lo0 + s * (C::SFA_BYTES >> 4),
                                                         sb_lo0 + s * (C::SFB_BYTES >> 4), kb0 != 0 ? 1u : 0u,
@@ -798,7 +765,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 tc_mma_mxf8(d_tmem, ad, bd, make_idesc<CG, KIND>(j), sfa_t, sfb_t, acc);
                         }
                         if constexpr (CG == 2) tc_commit_pair_mc(bar_empty + 8 * s, 3);
-                        else if constexpr (MC) tc_commit_mc(bar_empty + 8 * s, 3);
                         else tc_commit(bar_empty + 8 * s);
                         ready = false;
                     }
@@ -825,7 +791,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t st_slots = sbase + C::OFF_STORE + 2 * 2048 * sub;  // this warp's two staging slots
         uint32_t st_count = 0;                                            // blocks this warp has stored
         for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
-            const TileInfo ti = resolve_tile<TG>(p, tile, lane, rank, gt);
+            const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
             if (!ti.valid) break;
             const int64_t grow = ti.out_row0 + 32 * sub + lane;
             const bool row_ok = grow >= ti.row_lo && grow < ti.row_hi;
@@ -1074,31 +1040,20 @@ int cta_group_for(const GemmProblem &) {
     return forced == 2 ? 2 : 1;
 }
 
-// B multicast across CTA pairs for dense and weight-gradient problems (whose
-// M tiles of one N tile share B); MXQ_GEMM_MC=0 turns it off.
-bool b_multicast_for(const GemmProblem &g) {
-    static int enabled = [] {
-        const char *v = getenv("MXQ_GEMM_MC");
-        return v ? atoi(v) : 1;
-    }();
-    return enabled != 0 && (g.mode == kDense || g.mode == kGroupedK);
-}
-
-template <int CG, int KIND, bool BIAS, bool MC = false>
+template <int CG, int KIND, bool BIAS>
 cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     using C = Cfg<CG>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(k_gemm<CG, KIND, BIAS, MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        attr_err = cudaFuncSetAttribute(k_gemm<CG, KIND, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
     CUtensorMap tmA, tmB, tmSA, tmSB, tmC;
     const int64_t esz = KIND == kBF16 ? 2 : 1;  // operand bytes per element (tensor maps run over bytes)
-    // (MC: each CTA loads a 128-row half of B)
     if (!make_tmap(&tmA, g.a, g.a_rows, esz * g.a_k, C::BM) ||
-        !make_tmap(&tmB, g.b, g.b_rows, esz * g.b_k, MC ? C::B_ROWS / 2 : C::B_ROWS))
+        !make_tmap(&tmB, g.b, g.b_rows, esz * g.b_k, C::B_ROWS))
         return cudaErrorInvalidValue;
     if (CG == 2) {
         if (!make_scale_tmap(&tmSA, g.sa, scale_bytes_of(g.a_rows, g.a_k)) ||
@@ -1108,7 +1063,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         tmSA = tmA;  // unused
         tmSB = tmB;
     }
-    constexpr int64_t kUnitRows = MC ? 2 * C::TILE_M : C::TILE_M;  // rows per CTA (pair)
+    constexpr int64_t kUnitRows = C::TILE_M;  // rows per CTA (pair)
     p.m_tiles = static_cast<int>((g.M + kUnitRows - 1) / kUnitRows);
     // output tensor map for the epilogue's TMA stores (all experts' outputs
     // stacked for the grouped weight gradient); without one (ldc not a
@@ -1135,7 +1090,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cfg.stream = st;
-    if (CG == 2 || MC) {
+    if (CG == 2) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
@@ -1144,10 +1099,10 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         cfg.numAttrs = 1;
     }
     if (resident[dev] == 0) {
-        if (CG == 2 || MC) {
+        if (CG == 2) {
             cfg.gridDim = dim3(2);
             int clusters = 0;
-            e = cudaOccupancyMaxActiveClusters(&clusters, k_gemm<CG, KIND, BIAS, MC>, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&clusters, k_gemm<CG, KIND, BIAS>, &cfg);
             if (e != cudaSuccess) return e;
             resident[dev] = clusters > 0 ? clusters : 1;
         } else {
@@ -1156,8 +1111,8 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         }
     }
     const int64_t units = p.total_tiles < resident[dev] ? p.total_tiles : resident[dev];
-    cfg.gridDim = dim3(static_cast<unsigned>(units * (MC ? 2 : CG)));
-    return cudaLaunchKernelEx(&cfg, k_gemm<CG, KIND, BIAS, MC>, tmA, tmB, tmSA, tmSB, tmC, p);
+    cfg.gridDim = dim3(static_cast<unsigned>(units * CG));
+    return cudaLaunchKernelEx(&cfg, k_gemm<CG, KIND, BIAS>, tmA, tmB, tmSA, tmSB, tmC, p);
 }
 
 }  // namespace
@@ -1210,6 +1165,19 @@ __global__ void k_selftest_wait(uint64_t timeout_ns, int *gave_up) {
 }
 }  // namespace
 
+namespace {
+// Group-offset check on its own: one warp reads off[0..E] (nothing else) and
+// sets kErrBadOffsets when they are malformed.
+__global__ void k_check_offsets(const int64_t *off, int E, int64_t T) {
+    if (!group_offsets_valid(off, E, T, threadIdx.x & 31) && threadIdx.x == 0) atomicOr(&g_device_error, kErrBadOffsets);
+}
+}  // namespace
+
+cudaError_t launch_check_offsets(const int64_t *d_off, int E, int64_t T, cudaStream_t st) {
+    k_check_offsets<<<1, 32, 0, st>>>(d_off, E, T);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, int *d_gave_up, cudaStream_t st) {
     k_selftest_wait<<<1, 32, 0, st>>>(timeout_ns, d_gave_up);
     return cudaGetLastError();
@@ -1232,7 +1200,7 @@ cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
     p.c = static_cast<__nv_bfloat16 *>(g.c);
     p.M = g.M; p.N = g.N; p.ldc = g.ldc;
     p.K = g.kind == kBF16 ? 2 * g.K : g.K;  // the mainloop counts contraction bytes
-    p.offsets = g.offsets; p.E = g.E;
+    p.offsets = g.offsets; p.E = g.E; p.T = g.T;
     p.b_row_per_expert = g.b_row_per_expert;
     p.b_k_per_expert = g.b_k_per_expert;
     p.c_expert_stride = g.c_expert_stride;
@@ -1247,7 +1215,7 @@ cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
     }
     if (p.bias) return launch_cg<1, kMXF8, true>(g, p, st);
     if (cta_group_for(g) == 2) return launch_cg<2, kMXF8, false>(g, p, st);
-    return b_multicast_for(g) ? launch_cg<1, kMXF8, false, true>(g, p, st) : launch_cg<1, kMXF8, false>(g, p, st);
+    return launch_cg<1, kMXF8, false>(g, p, st);
 }
 
 }  // namespace mxq

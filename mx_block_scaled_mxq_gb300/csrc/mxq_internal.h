@@ -68,6 +68,9 @@ cudaError_t device_error_word(unsigned int **out);
 // Self-test of the bounded waits: a kernel whose wait nothing completes gives
 // up after timeout_ns, sets the error word and writes 1 to *d_gave_up.
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, int *d_gave_up, cudaStream_t st);
+// Checks group offsets on the device (one warp reads d_off[0..E] only) and sets
+// the bad-offsets bit of the device error word when they are malformed.
+cudaError_t launch_check_offsets(const int64_t *d_off, int E, int64_t T, cudaStream_t st);
 // Reads the device error word set by bounded waits that gave up, then clears it.
 cudaError_t read_and_clear_device_error(unsigned int *word);
 

@@ -327,6 +327,7 @@ struct ColParams {
     const int64_t *offsets;  // GROUPED: E+1 device offsets
     int E;
     float sf;                // MXFP4 scale factor (row pass in FMT 2)
+    unsigned int *err;       // GROUPED: device error word (malformed offsets)
 };
 
 template <bool ROWS, bool GROUPED>
@@ -343,6 +344,17 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
     int64_t src0 = rt * kTile;  // first source row of the tile
     int nvalid;                 // rows of the tile that hold data
     if (GROUPED) {
+        // malformed offsets: this CTA reads and writes nothing
+        __shared__ int sh_bad;
+        if (warp == 0) {
+            const bool good = group_offsets_valid(P.offsets, P.E, P.R, lane);
+            if (lane == 0) {
+                sh_bad = good ? 0 : 1;
+                if (!good) atomicOr(P.err, kErrBadOffsets);
+            }
+        }
+        __syncthreads();
+        if (sh_bad) return;
         if (tid == 0) sh_nvalid = 0;
         __syncwarp();
         if (warp == 0) {
@@ -594,6 +606,14 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
     const bool row_v8 = ROWS && ((reinterpret_cast<uintptr_t>(P.q_row) | static_cast<uintptr_t>(P.C)) & 31) == 0;
     const bool col_v8 = ((reinterpret_cast<uintptr_t>(P.qT) | static_cast<uintptr_t>(P.ldqT)) & 31) == 0;
     int64_t *g_off = g_tab, *g_pre = g_tab + (kQuantTableE + 1);
+    if (GROUPED && warp == 0) {
+        // malformed offsets: no tile is decoded from them, no load or store is issued
+        const bool good = group_offsets_valid(P.offsets, P.E, P.R, lane);
+        if (lane == 0 && !good) {
+            abort_flag = 1;
+            atomicOr(err, kErrBadOffsets);
+        }
+    }
     if (tables && warp == 0) {
         // one scan of the offsets per CTA instead of one per tile
         int64_t run = 0;
@@ -616,6 +636,7 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
         }
     }
     __syncthreads();
+    if (GROUPED && abort_flag) return;  // (uniform: set before the barrier)
 
     // warp 0: resolve tile t into slot `buf` and start its load
     auto issue = [&](int64_t t, int buf) {
@@ -1151,7 +1172,8 @@ cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, c
     P.q_row = q_row; P.s_row = s_row; P.kb_row_tiles = ((C / 32) + 3) / 4;
     P.qT = qT; P.sT = sT; P.ldqT = t_pad; P.kb_col_tiles = (t_pad / 32 + 3) / 4;
     P.offsets = d_off; P.E = E;
-    cudaError_t res = cudaSuccess;
+    cudaError_t res = device_error_word(&P.err);
+    if (res != cudaSuccess) return res;
     if (q_row && T > 0) {
         if (launch_cols_tma<true, true>(P, t_pad / kTile, st, &res)) return res;
         // no tensor map for x: the row quant on its own, then the column quant

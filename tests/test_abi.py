@@ -124,3 +124,29 @@ def test_host_validation_rejects_before_launch(lib):
     assert _status(m.mxq_linear_fwd, FAKE, FAKE, 64, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 16, 0) == INV
     assert _status(m.mxq_linear_fwd, FAKE, FAKE, 64, 64, 64, 7, FAKE, FAKE, FAKE, 1 << 30, 0) == INV
     assert "workspace" in m.mxq_last_error_string() or "mode" in m.mxq_last_error_string()
+
+
+def test_group_offsets_validated_on_the_host(lib):
+    """The rule every grouped kernel applies to its device offsets, checked
+    here on host arrays: off[0] = 0, non-decreasing, off[E] = T."""
+    INV = 1
+    ok = [0, 10, 10, 300, 300]
+    assert _status(m.mxq_validate_group_offsets, ok, 4, 300) == 0
+    assert _status(m.mxq_validate_group_offsets, [0, 0], 1, 0) == 0            # one empty group
+    bad = {
+        "off[0]": ([5, 10, 10, 300, 300], 300),                                 # does not start at 0
+        "decrease": ([0, 200, 100, 300, 300], 300),                             # non-monotone
+        "negative": ([0, -8, 10, 300, 300], 300),                               # negative (and decreasing)
+        "must equal T": ([0, 10, 10, 300, 299], 300),                           # off[E] != T
+        "past T": ([0, 10, 400, 500, 600], 300),                                # rows past the tensor
+    }
+    for what, (off, T) in bad.items():
+        assert _status(m.mxq_validate_group_offsets, off, 4, T) == INV, what
+    assert _status(m.mxq_validate_group_offsets, [0, 2, 1], 2, 1) == INV
+    assert "must not decrease" in m.mxq_last_error_string()
+    assert _status(m.mxq_validate_group_offsets, ok, 0, 300) == INV           # E out of range
+    assert _status(m.mxq_validate_group_offsets, ok, 4, -1) == INV            # negative T
+    # the device checker rejects bad arguments on the host, before any launch
+    assert _status(m.mxq_check_group_offsets, None, 4, 300, 0) == INV
+    assert _status(m.mxq_check_group_offsets, FAKE + 4, 4, 300, 0) == INV
+    assert _status(m.mxq_check_group_offsets, FAKE, 0, 300, 0) == INV
