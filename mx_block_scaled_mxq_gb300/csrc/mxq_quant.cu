@@ -135,36 +135,50 @@ __device__ __forceinline__ int mx4_exp(float amax, float sf) {
     const int e = lhs >= rhs ? e0 + 1 : e0;
     return min(e, 127);
 }
-__device__ __forceinline__ float pow2(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
-
-struct E2M1Thr {
-    float t[7];  // midpoints * 2^e
-    float s;     // 2^e
+// The MXFP4 element rule ("AMCT FakeQuant 模拟伪量化工具包", section 2) in the
+// input's own scale.  With the block scale s = 2^e, an element's magnitude
+// y = |x| / s is snapped to the codebook {0, .5, 1, 1.5, 2, 3, 4, 6}, a
+// midpoint going up.  Above 1 the codebook is every value with one mantissa
+// bit, so snapping there is rounding |x|'s mantissa to one bit, half away from
+// zero: add half of bit 22 and clear the bits below it -- the exponent is
+// untouched, so no division by s is needed -- then clamp at 6 s.  Below s the
+// two midpoints 0.25 s and 0.75 s decide between 0, s/2 and s.  Everything is
+// integer arithmetic on the fp32 bit patterns of non-negative values, whose
+// order is the order of the values (an overflow to +inf included).
+struct Mx4Blk {
+    uint32_t s, half_s, t025, t075, six_s;  // fp32 bits of s, s/2, s/4, 3s/4, 6s (+inf when 6s overflows)
+    int e;
 };
-__device__ __forceinline__ E2M1Thr e2m1_thresholds(int e) {
-    E2M1Thr r;
-    r.s = pow2(e);
-    r.t[0] = 0.25f * r.s; r.t[1] = 0.75f * r.s; r.t[2] = 1.25f * r.s; r.t[3] = 1.75f * r.s;
-    r.t[4] = 2.5f * r.s;  r.t[5] = 3.5f * r.s;  r.t[6] = 5.0f * r.s;
-    return r;
+__device__ __forceinline__ Mx4Blk mx4_block(int e) {  // e in [-30, 127]
+    Mx4Blk B;
+    B.e = e;
+    B.s = static_cast<uint32_t>(e + 127) << 23;
+    B.half_s = static_cast<uint32_t>(e + 126) << 23;
+    B.t025 = static_cast<uint32_t>(e + 125) << 23;
+    B.t075 = B.half_s | 0x400000u;
+    B.six_s = e <= 125 ? (static_cast<uint32_t>(e + 129) << 23) | 0x400000u : 0x7F800000u;
+    return B;
 }
-// Codebook index of |x|: the number of midpoints <= |x| / 2^e, found by a
-// three-level binary search over the same exact thresholds (midpoint t[3]
-// first, then t[1] or t[5], then t[0], t[2], t[4] or t[6]).
-__device__ __forceinline__ uint32_t e2m1_index(float ax, const E2M1Thr &T) {
-    const bool c1 = ax >= T.t[3];
-    const bool c2 = ax >= (c1 ? T.t[5] : T.t[1]);
-    const float t3 = c1 ? (c2 ? T.t[6] : T.t[4]) : (c2 ? T.t[2] : T.t[0]);
-    const bool c3 = ax >= t3;
-    return (c1 ? 4u : 0u) + (c2 ? 2u : 0u) + (c3 ? 1u : 0u);
+// |x| snapped to (codebook value) x s, as fp32 bits; ax = |x|'s bits, finite.
+__device__ __forceinline__ uint32_t mx4_snap(uint32_t ax, const Mx4Blk &B) {
+    const uint32_t r = min((ax + 0x200000u) & 0xFFC00000u, B.six_s);
+    const uint32_t lo = ax >= B.t075 ? B.s : (ax >= B.t025 ? B.half_s : 0u);
+    return ax >= B.s ? r : lo;
 }
-// {0, .5, 1, 1.5, 2, 3, 4, 6}
-__device__ __forceinline__ float e2m1_value(uint32_t i) {
-    return i < 5 ? 0.5f * static_cast<float>(i) : (i == 7 ? 6.0f : static_cast<float>(i) - 2.0f);
+// Codebook index (0..7) of the snapped magnitude: above s, the rounded bits
+// hold value 2^k (1 + m/2) x s, index 2 + 2 k + m.
+__device__ __forceinline__ uint32_t mx4_index(uint32_t ax, const Mx4Blk &B) {
+    const uint32_t r = min((ax + 0x200000u) & 0xFFC00000u, B.six_s);
+    const uint32_t lo = ax >= B.t075 ? 2u : (ax >= B.t025 ? 1u : 0u);
+    return ax >= B.s ? (r >> 22) - static_cast<uint32_t>(2 * B.e + 252) : lo;
 }
-__device__ __forceinline__ float qdq_one(float x, const E2M1Thr &T) {
-    const float ax = fabsf(x);
-    return copysignf(e2m1_value(e2m1_index(ax, T)) * T.s, x);
+// E4M3 code of the snapped magnitude's codebook value (0.5 -> 0x30, 1 -> 0x38,
+// ..., 6 -> 0x4C): above s it is the rounded bits' exponent and top mantissa
+// bit, rebased from the fp32 bias 127 + e to the E4M3 bias 7.
+__device__ __forceinline__ uint32_t mx4_e4m3_code(uint32_t ax, const Mx4Blk &B) {
+    const uint32_t r = min((ax + 0x200000u) & 0xFFC00000u, B.six_s);
+    const uint32_t lo = ax >= B.t075 ? 0x38u : (ax >= B.t025 ? 0x30u : 0u);
+    return ax >= B.s ? (r >> 20) - static_cast<uint32_t>(0x3C0 + 8 * B.e) : lo;
 }
 
 // ============================================================================
@@ -177,20 +191,15 @@ __device__ __forceinline__ float qdq_one(float x, const E2M1Thr &T) {
 // MXFP4 formats take the scale factor sf (6 by default).
 // Each thread owns 8 chunks of 8 elements; 4 lanes form one 32-block.
 // ============================================================================
-// E4M3 code of E2M1 codebook index i (0, .5, 1, 1.5, 2, 3, 4, 6), byte i.
-constexpr unsigned long long kE2M1AsE4M3 = 0x4C4844403C383000ull;
-
 // E4M3 codes of the MXFP4 values of 8 bf16 (4 packed words, element 2k in the
-// low half of word k) under thresholds T: sign | the E4M3 code of the E2M1
-// value; the NaN code 0x7F | sign for a non-finite block.
-__device__ __forceinline__ uint2 mx4_as_e4m3_codes8(const uint32_t (&w)[4], const E2M1Thr &T, bool nonfinite) {
+// low half of word k) under block B: sign | the E4M3 code of the E2M1 value;
+// the NaN code 0x7F | sign for a non-finite block.
+__device__ __forceinline__ uint2 mx4_as_e4m3_codes8(const uint32_t (&w)[4], const Mx4Blk &B, bool nonfinite) {
     uint32_t b[2] = {0, 0};
 #pragma unroll
     for (int k = 0; k < 8; k++) {
         const uint32_t bits = (k & 1) ? (w[k >> 1] & 0xFFFF0000u) : (w[k >> 1] << 16);
-        const uint32_t mag =
-            nonfinite ? 0x7Fu
-                      : static_cast<uint32_t>((kE2M1AsE4M3 >> (8 * e2m1_index(fabsf(__uint_as_float(bits)), T))) & 0xFFu);
+        const uint32_t mag = nonfinite ? 0x7Fu : mx4_e4m3_code(bits & 0x7FFFFFFFu, B);
         b[k >> 2] |= (((bits >> 24) & 0x80u) | mag) << (8 * (k & 3));
     }
     return make_uint2(b[0], b[1]);
@@ -264,13 +273,14 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
             const bool nonfinite = a >= 0x7F800000u;
             const int e = nonfinite ? 0 : mx4_exp(__uint_as_float(a), sf);
             sbyte = nonfinite ? 0xFF : static_cast<uint8_t>(e + 127);
-            const E2M1Thr T = e2m1_thresholds(e);
+            const Mx4Blk B = mx4_block(e);
             if (FMT == 1) {
                 uint32_t packed = 0;
 #pragma unroll
                 for (int k = 0; k < 8; k++) {
-                    const uint32_t idx = nonfinite ? 7u : e2m1_index(fabsf(v[k]), T);
-                    const uint32_t nib = ((__float_as_uint(v[k]) >> 28) & 8u) | idx;
+                    const uint32_t bits = __float_as_uint(v[k]);
+                    const uint32_t idx = nonfinite ? 7u : mx4_index(bits & 0x7FFFFFFFu, B);
+                    const uint32_t nib = ((bits >> 28) & 8u) | idx;
                     packed |= nib << (4 * k);
                 }
                 if (valid) {
@@ -282,10 +292,9 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
                 uint32_t lo = 0, hi = 0;
 #pragma unroll
                 for (int k = 0; k < 8; k++) {
-                    const uint32_t mag = nonfinite ? 0x7Fu
-                                                   : static_cast<uint32_t>(
-                                                         (kE2M1AsE4M3 >> (8 * e2m1_index(fabsf(v[k]), T))) & 0xFFu);
-                    const uint32_t code = ((__float_as_uint(v[k]) >> 24) & 0x80u) | mag;
+                    const uint32_t bits = __float_as_uint(v[k]);
+                    const uint32_t mag = nonfinite ? 0x7Fu : mx4_e4m3_code(bits & 0x7FFFFFFFu, B);
+                    const uint32_t code = ((bits >> 24) & 0x80u) | mag;
                     if (k < 4) lo |= code << (8 * k);
                     else hi |= code << (8 * (k - 4));
                 }
@@ -716,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
                     }
                     const uint32_t a = max(max(amax8_bf16(w[0]), amax8_bf16(w[1])), max(amax8_bf16(w[2]), amax8_bf16(w[3])));
                     int X = 0;            // FMT 0: MXFP8 scale exponent
-                    E2M1Thr T{};          // FMT 2: MXFP4 thresholds
+                    Mx4Blk T{};           // FMT 2: MXFP4 block constants
                     bool nonfinite = false;
                     uint8_t sbyte;
                     if (FMT == 0) {
@@ -726,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
                         nonfinite = (a << 16) >= 0x7F800000u;
                         const int e = nonfinite ? 0 : mx4_exp(__uint_as_float(a << 16), P.sf);
                         sbyte = nonfinite ? 0xFF : static_cast<uint8_t>(e + 127);
-                        T = e2m1_thresholds(e);
+                        T = mx4_block(e);
                     }
                     const bool valid = row < nvalid && gc < P.C;
                     if (valid) {
@@ -866,69 +875,80 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
 // straight-through estimator (|x| > 6 * block scale; one 32-bit word per
 // block, bit i = element i of the block; 0 for a block with a non-finite
 // element, whose scale is not finite).
-//  Vector path (cols % 32 == 0, 16-byte aligned): 8 floats per thread, 4
-//  lanes per block.  General path: one warp per block of 32 (ragged rows).
-// Warp-uniform grid-stride loops so that every shuffle has all 32 lanes.
+//  Vector path (cols % 32 == 0, 16-byte aligned): a CTA takes a window of
+//  kEwChunks x 256 chunks of 8 floats; thread t handles chunks t and t + 256
+//  of it, both loaded before any arithmetic, and the 4 lanes holding one
+//  32-element block exchange their maxima by shuffles.  General path: one
+//  warp per block of 32 (ragged rows).
+// Loops are warp-uniform so that every shuffle has all 32 lanes.
 // ============================================================================
+constexpr int kEwChunks = 2;  // 8-element chunks per thread in flight
+constexpr int64_t kEwWindow = static_cast<int64_t>(kThreads) * kEwChunks;
+
 template <bool MASK>
 __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restrict__ x, float *y,
                                                             uint32_t *__restrict__ mask, int64_t nchunks, float sf) {
-    const int lane = threadIdx.x & 31;
-    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    const int64_t wstride = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-    // one 32-byte access per thread where both tensors are 32-byte aligned
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // one 32-byte access per chunk where both tensors are 32-byte aligned
     const bool al32 = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 31) == 0;
-    for (int64_t wb = warp0 * 32; wb < nchunks; wb += wstride * 32) {
-        const int64_t g = wb + lane;
-        const bool valid = g < nchunks;  // uniform over the 4 lanes of a block (nchunks % 4 == 0)
-        float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (valid) {
-            uint4 a, b;
-            if (al32) {
-                ldg_nc_v8(x + 8 * g, a, b);
+    for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kEwWindow; w0 < nchunks;
+         w0 += static_cast<int64_t>(gridDim.x) * kEwWindow) {
+        uint4 in[kEwChunks][2];
+#pragma unroll
+        for (int u = 0; u < kEwChunks; u++) {
+            const int64_t g = w0 + u * kThreads + threadIdx.x;
+            in[u][0] = in[u][1] = make_uint4(0, 0, 0, 0);
+            if (g < nchunks) {
+                if (al32) {
+                    ldg_nc_v8(x + 8 * g, in[u][0], in[u][1]);
+                } else {
+                    in[u][0] = ldg_nc_v4(x + 8 * g);
+                    in[u][1] = ldg_nc_v4(x + 8 * g + 4);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kEwChunks; u++) {
+            const int64_t g = w0 + u * kThreads + threadIdx.x;
+            const uint32_t v[8] = {in[u][0].x, in[u][0].y, in[u][0].z, in[u][0].w,
+                                   in[u][1].x, in[u][1].y, in[u][1].z, in[u][1].w};
+            uint32_t a = 0;
+#pragma unroll
+            for (int k = 0; k < 8; k++) a = max(a, v[k] & 0x7FFFFFFFu);
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            uint32_t o[8];
+            uint32_t bits = 0;
+            if (a >= 0x7F800000u) {
+#pragma unroll
+                for (int k = 0; k < 8; k++) o[k] = 0x7FC00000u;
             } else {
-                a = ldg_nc_v4(x + 8 * g);
-                b = ldg_nc_v4(x + 8 * g + 4);
+                const Mx4Blk B = mx4_block(mx4_exp(__uint_as_float(a), sf));
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const uint32_t ax = v[k] & 0x7FFFFFFFu;
+                    o[k] = mx4_snap(ax, B) | (v[k] & 0x80000000u);
+                    if (MASK) bits |= (ax > B.six_s ? 1u : 0u) << k;
+                }
             }
-            v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
-            v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
-        }
-        uint32_t a = 0;
-#pragma unroll
-        for (int k = 0; k < 8; k++) a = max(a, __float_as_uint(v[k]) & 0x7FFFFFFFu);
-        a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
-        float o[8];
-        uint32_t bits = 0;
-        if (a >= 0x7F800000u) {
-#pragma unroll
-            for (int k = 0; k < 8; k++) o[k] = __uint_as_float(0x7FC00000u);
-        } else {
-            const E2M1Thr T = e2m1_thresholds(mx4_exp(__uint_as_float(a), sf));
-            const float limit = 6.0f * T.s;  // +inf for e = 127: nothing saturates
-#pragma unroll
-            for (int k = 0; k < 8; k++) {
-                o[k] = qdq_one(v[k], T);
-                if (MASK) bits |= (fabsf(v[k]) > limit ? 1u : 0u) << k;
+            if (MASK) {
+                // the block's word from its 4 lanes, then lanes 0-7 write the
+                // warp's 8 consecutive words
+                const int64_t wb = w0 + u * kThreads + 32 * warp;  // the warp's first chunk
+                uint32_t w = bits << (8 * (lane & 3));
+                w |= __shfl_xor_sync(0xffffffffu, w, 1);
+                w |= __shfl_xor_sync(0xffffffffu, w, 2);
+                w = __shfl_sync(0xffffffffu, w, (4 * lane) & 31);
+                if (lane < 8 && wb + 4 * lane < nchunks) mask[wb / 4 + lane] = w;
             }
-        }
-        if (MASK) {
-            // the block's word from its 4 lanes, then lanes 0-7 write the warp's
-            // 8 consecutive words
-            uint32_t w = bits << (8 * (lane & 3));
-            w |= __shfl_xor_sync(0xffffffffu, w, 1);
-            w |= __shfl_xor_sync(0xffffffffu, w, 2);
-            w = __shfl_sync(0xffffffffu, w, (4 * lane) & 31);
-            if (lane < 8 && wb + 4 * lane < nchunks) mask[wb / 4 + lane] = w;
-        }
-        if (!valid) continue;
-        const uint4 o0 = make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
-        const uint4 o1 = make_uint4(__float_as_uint(o[4]), __float_as_uint(o[5]), __float_as_uint(o[6]), __float_as_uint(o[7]));
-        if (al32) {
-            stg_v8(y + 8 * g, o0, o1);
-        } else {
-            stg_v4(y + 8 * g, o0);
-            stg_v4(y + 8 * g + 4, o1);
+            if (g >= nchunks) continue;
+            const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]), o1 = make_uint4(o[4], o[5], o[6], o[7]);
+            if (al32) {
+                stg_v8(y + 8 * g, o0, o1);
+            } else {
+                stg_v4(y + 8 * g, o0);
+                stg_v4(y + 8 * g + 4, o1);
+            }
         }
     }
 }
@@ -946,93 +966,114 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restr
         const int64_t r = k / nb, b = k % nb;
         const int64_t c = 32 * b + lane;
         const bool valid = c < cols;
-        const float v = valid ? x[r * cols + c] : 0.0f;
-        uint32_t a = __float_as_uint(v) & 0x7FFFFFFFu;
+        const uint32_t v = valid ? __float_as_uint(x[r * cols + c]) : 0u;
+        const uint32_t ax = v & 0x7FFFFFFFu;
+        uint32_t a = ax;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
-        float out;
+        uint32_t out;
         bool sat = false;
         if (a >= 0x7F800000u) {
-            out = __uint_as_float(0x7FC00000u);
+            out = 0x7FC00000u;
         } else {
-            const E2M1Thr T = e2m1_thresholds(mx4_exp(__uint_as_float(a), sf));
-            out = qdq_one(v, T);
-            sat = valid && fabsf(v) > 6.0f * T.s;
+            const Mx4Blk B = mx4_block(mx4_exp(__uint_as_float(a), sf));
+            out = mx4_snap(ax, B) | (v & 0x80000000u);
+            sat = valid && ax > B.six_s;
         }
         if (MASK) {
             const uint32_t w = __ballot_sync(0xffffffffu, sat);
             if (lane == 0) mask[k] = w;
         }
-        if (valid) y[r * cols + c] = out;
+        if (valid) y[r * cols + c] = __uint_as_float(out);
     }
 }
 
 // MXFP4 quant-dequant of bf16 to bf16 (cols % 32 == 0, 16-byte aligned): 8
-// elements per thread, 4 lanes per block.  Every result (codebook value x
-// 2^e, or NaN for a non-finite block) is exact in bf16, so the fp32 result's
-// upper half is the bf16 result.
+// elements per chunk, 4 lanes per block, the vector path's windows.  Every
+// result (codebook value x 2^e, or NaN for a non-finite block) is exact in
+// bf16, so the fp32 result's upper half is the bf16 result.
 __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_bf16(const uint16_t *__restrict__ x, uint16_t *y,
                                                              int64_t nchunks, float sf) {
-    const int lane = threadIdx.x & 31;
-    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    const int64_t wstride = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-    for (int64_t wb = warp0 * 32; wb < nchunks; wb += wstride * 32) {
-        const int64_t g = wb + lane;
-        const bool valid = g < nchunks;
-        uint4 in = make_uint4(0, 0, 0, 0);
-        if (valid) in = ldg_nc_v4(x + 8 * g);
-        const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-        float v[8];
+    for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kEwWindow; w0 < nchunks;
+         w0 += static_cast<int64_t>(gridDim.x) * kEwWindow) {
+        uint4 in[kEwChunks];
 #pragma unroll
-        for (int k = 0; k < 4; k++) { v[2 * k] = bf16lo(w[k]); v[2 * k + 1] = bf16hi(w[k]); }
-        const uint32_t (&w4)[4] = w;
-        uint32_t a = amax8_bf16(w4) << 16;  // |bf16| bits as fp32 bits
-        a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
-        if (!valid) continue;
-        uint32_t o[4];
-        if (a >= 0x7F800000u) {
-#pragma unroll
-            for (int k = 0; k < 4; k++) o[k] = 0x7FC07FC0u;
-        } else {
-            const E2M1Thr T = e2m1_thresholds(mx4_exp(__uint_as_float(a), sf));
-#pragma unroll
-            for (int k = 0; k < 4; k++)
-                o[k] = (__float_as_uint(qdq_one(v[2 * k], T)) >> 16) |
-                       (__float_as_uint(qdq_one(v[2 * k + 1], T)) & 0xFFFF0000u);
+        for (int u = 0; u < kEwChunks; u++) {
+            const int64_t g = w0 + u * kThreads + threadIdx.x;
+            in[u] = g < nchunks ? ldg_nc_v4(x + 8 * g) : make_uint4(0, 0, 0, 0);
         }
-        stg_v4(y + 8 * g, make_uint4(o[0], o[1], o[2], o[3]));
+#pragma unroll
+        for (int u = 0; u < kEwChunks; u++) {
+            const int64_t g = w0 + u * kThreads + threadIdx.x;
+            const uint32_t w[4] = {in[u].x, in[u].y, in[u].z, in[u].w};
+            uint32_t a = amax8_bf16(w) << 16;  // |bf16| bits as fp32 bits
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            if (g >= nchunks) continue;
+            uint32_t o[4];
+            if (a >= 0x7F800000u) {
+#pragma unroll
+                for (int k = 0; k < 4; k++) o[k] = 0x7FC07FC0u;
+            } else {
+                const Mx4Blk B = mx4_block(mx4_exp(__uint_as_float(a), sf));
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const uint32_t lo = w[k] << 16, hi = w[k] & 0xFFFF0000u;
+                    const uint32_t qlo = mx4_snap(lo & 0x7FFFFFFFu, B) | (lo & 0x80000000u);
+                    const uint32_t qhi = mx4_snap(hi & 0x7FFFFFFFu, B) | (hi & 0x80000000u);
+                    o[k] = (qlo >> 16) | qhi;
+                }
+            }
+            stg_v4(y + 8 * g, make_uint4(o[0], o[1], o[2], o[3]));
+        }
     }
 }
 
 // Clipped straight-through estimator, backward: gx = gy except +0.0 where the
-// forward's saturation mask is set.  Vector path: 8 floats per thread (cols %
-// 32 == 0, 16-byte aligned); general path: one warp per block.
+// forward's saturation mask is set.  Vector path (cols % 32 == 0, 16-byte
+// aligned): the QDQ's windows, two 32-byte chunks and their mask words loaded
+// per thread before any store; general path: one warp per block.
 __global__ void __launch_bounds__(kThreads) k_ste_backward_vec(const float *__restrict__ gy,
                                                                const uint32_t *__restrict__ mask, float *gx,
                                                                int64_t nchunks) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     const bool al32 = ((reinterpret_cast<uintptr_t>(gy) | reinterpret_cast<uintptr_t>(gx)) & 31) == 0;
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; g < nchunks; g += stride) {
-        const uint32_t bits = (__ldg(mask + g / 4) >> (8 * (g & 3))) & 0xFFu;
-        uint4 a, b;
-        if (al32) {
-            ldg_nc_v8(gy + 8 * g, a, b);
-        } else {
-            a = ldg_nc_v4(gy + 8 * g);
-            b = ldg_nc_v4(gy + 8 * g + 4);
+    for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kEwWindow; w0 < nchunks;
+         w0 += static_cast<int64_t>(gridDim.x) * kEwWindow) {
+        uint4 in[kEwChunks][2];
+        uint32_t mw[kEwChunks];
+#pragma unroll
+        for (int u = 0; u < kEwChunks; u++) {
+            const int64_t g = w0 + u * kThreads + threadIdx.x;
+            in[u][0] = in[u][1] = make_uint4(0, 0, 0, 0);
+            mw[u] = 0;
+            if (g < nchunks) {
+                mw[u] = __ldg(mask + g / 4);
+                if (al32) {
+                    ldg_nc_v8(gy + 8 * g, in[u][0], in[u][1]);
+                } else {
+                    in[u][0] = ldg_nc_v4(gy + 8 * g);
+                    in[u][1] = ldg_nc_v4(gy + 8 * g + 4);
+                }
+            }
         }
-        if (bits) {
-            a.x = (bits & 1u) ? 0u : a.x;    a.y = (bits & 2u) ? 0u : a.y;
-            a.z = (bits & 4u) ? 0u : a.z;    a.w = (bits & 8u) ? 0u : a.w;
-            b.x = (bits & 16u) ? 0u : b.x;   b.y = (bits & 32u) ? 0u : b.y;
-            b.z = (bits & 64u) ? 0u : b.z;   b.w = (bits & 128u) ? 0u : b.w;
-        }
-        if (al32) {
-            stg_v8(gx + 8 * g, a, b);
-        } else {
-            stg_v4(gx + 8 * g, a);
-            stg_v4(gx + 8 * g + 4, b);
+#pragma unroll
+        for (int u = 0; u < kEwChunks; u++) {
+            const int64_t g = w0 + u * kThreads + threadIdx.x;
+            if (g >= nchunks) continue;
+            const uint32_t bits = (mw[u] >> (8 * (g & 3))) & 0xFFu;
+            uint4 a = in[u][0], b = in[u][1];
+            if (bits) {
+                a.x = (bits & 1u) ? 0u : a.x;    a.y = (bits & 2u) ? 0u : a.y;
+                a.z = (bits & 4u) ? 0u : a.z;    a.w = (bits & 8u) ? 0u : a.w;
+                b.x = (bits & 16u) ? 0u : b.x;   b.y = (bits & 32u) ? 0u : b.y;
+                b.z = (bits & 64u) ? 0u : b.z;   b.w = (bits & 128u) ? 0u : b.w;
+            }
+            if (al32) {
+                stg_v8(gx + 8 * g, a, b);
+            } else {
+                stg_v4(gx + 8 * g, a);
+                stg_v4(gx + 8 * g + 4, b);
+            }
         }
     }
 }
@@ -1051,6 +1092,14 @@ __global__ void __launch_bounds__(kThreads) k_ste_backward_gen(const float *__re
         const bool sat = (__ldg(mask + k) >> lane) & 1u;
         gx[r * cols + c] = sat ? 0.0f : gy[r * cols + c];
     }
+}
+
+// CTAs for the windowed elementwise kernels: one window each, so the hardware
+// hands out short CTAs as SMs free up (no persistent loop whose last round
+// runs part-empty); capped, with the kernels looping past the cap.
+int grid_windows(int64_t nchunks) {
+    const int64_t g = (nchunks + kEwWindow - 1) / kEwWindow;
+    return static_cast<int>(g < 1 ? 1 : (g > (1 << 20) ? (1 << 20) : g));
 }
 
 int grid_for(int64_t work_items, int per_cta) {
@@ -1191,7 +1240,7 @@ cudaError_t launch_qdq_mxfp4(const float *x, float *y, uint32_t *mask, int64_t r
     const bool vec = (cols % 32 == 0) && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) == 0;
     if (vec) {
         const int64_t nchunks = rows * cols / 8;
-        const int grid = grid_for(nchunks, kThreads * 2);
+        const int grid = grid_windows(nchunks);
         if (mask) k_qdq_mxfp4_vec<true><<<grid, kThreads, 0, st>>>(x, y, mask, nchunks, sf);
         else k_qdq_mxfp4_vec<false><<<grid, kThreads, 0, st>>>(x, y, nullptr, nchunks, sf);
     } else {
@@ -1206,7 +1255,7 @@ cudaError_t launch_qdq_mxfp4(const float *x, float *y, uint32_t *mask, int64_t r
 cudaError_t launch_qdq_mxfp4_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols, float sf,
                                   cudaStream_t st) {
     const int64_t nchunks = rows * cols / 8;
-    k_qdq_mxfp4_bf16<<<grid_for(nchunks, kThreads * 2), kThreads, 0, st>>>(x, y, nchunks, sf);
+    k_qdq_mxfp4_bf16<<<grid_windows(nchunks), kThreads, 0, st>>>(x, y, nchunks, sf);
     return cudaGetLastError();
 }
 
@@ -1215,7 +1264,7 @@ cudaError_t launch_ste_backward(const float *gy, const uint32_t *mask, float *gx
     const bool vec = (cols % 32 == 0) && ((reinterpret_cast<uintptr_t>(gy) | reinterpret_cast<uintptr_t>(gx)) & 15) == 0;
     if (vec) {
         const int64_t nchunks = rows * cols / 8;
-        k_ste_backward_vec<<<grid_for(nchunks, kThreads * 2), kThreads, 0, st>>>(gy, mask, gx, nchunks);
+        k_ste_backward_vec<<<grid_windows(nchunks), kThreads, 0, st>>>(gy, mask, gx, nchunks);
     } else {
         const int64_t nblocks = rows * ((cols + 31) / 32);
         k_ste_backward_gen<<<grid_for(nblocks, kThreads / 32), kThreads, 0, st>>>(gy, mask, gx, rows, cols);
