@@ -14,7 +14,7 @@
 //
 // Persistent: each CTA (CG = 1) or CTA pair (CG = 2) walks its share of the
 // tiles; the stage ring and the accumulator phases run across tiles.
-// A CTA has 6 warps; the output tile is (128 * CG) x 256, K steps of 128 bytes:
+// A CTA has 10 warps; the output tile is (128 * CG) x 256, K steps of 128 bytes:
 //   warp 0     TMA producer: A/B code tiles (128B-swizzled) by
 //              cp.async.bulk.tensor, 512-byte scale tiles (cp.async.bulk for
 //              CG = 1, 2-D TMA for CG = 2);
@@ -23,12 +23,13 @@
 //              32x128b.warpx4) and issues 4 tcgen05.mma.kind::mxf8f6f4.block_scale
 //              (M = 128 * CG, N = 256, K = 32) per stage; tcgen05.commit frees
 //              the stage (in both CTAs of a pair);
-//   warps 2-5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane
-//              sub-partition each) into registers as bf16 (RNE), release of the
-//              accumulator to the MMA warp, then stores that overlap the next
-//              tile's mainloop: 32 x 32 blocks staged in shared memory and
-//              written by TMA (cp.async.bulk.tensor), or, for a warp whose 32
-//              rows straddle an expert boundary, masked 16-byte row stores.
+//   warps 2-9  epilogue, two per TMEM lane sub-partition, each taking 128 of
+//              the 256 columns: tcgen05.ld of the fp32 accumulator into
+//              registers as bf16 (RNE), release of the accumulator to the MMA
+//              warp, then stores that overlap the next tile's mainloop: 32 x 32
+//              blocks staged in shared memory and written by TMA
+//              (cp.async.bulk.tensor), or, for a warp whose 32 rows straddle an
+//              expert boundary, masked 16-byte row stores.
 // CG = 2 pairs two SMs on one 256 x 256 tile: each CTA loads 128 rows of A and
 // 128 of the 256 rows of B (32 KB per stage, 6 stages), so per SM the operand
 // traffic and the shared memory per stage are two thirds of CG = 1's, and the
@@ -57,7 +58,16 @@ __device__ unsigned int g_device_error = 0;
 
 namespace {
 
-constexpr int BN = 256, BK = 128, THREADS = 192;
+constexpr int BN = 256, BK = 128;
+// Epilogue warps: two per TMEM lane quadrant, each draining and storing
+// kEpiCols of the tile's 256 accumulator columns, so short-contraction tiles
+// (the grouped weight gradient's small experts) are drained at twice the rate
+// of one warp per quadrant.  Warps 0 and 1 are the producer and the MMA issuer.
+constexpr int kEpiWarps = 8;
+constexpr int kEpiCols = BN * 4 / kEpiWarps, kEpiChunks = kEpiCols / 32;
+constexpr int THREADS = 64 + 32 * kEpiWarps;
+// 2 KB store-staging slots per epilogue warp (shared memory holds 16 KB of them)
+constexpr int kStoreSlots = 8 / kEpiWarps;
 constexpr uint32_t TMEM_COLS = 512, SF_STRIDE = 16;
 constexpr int kMaxTableE = 256;  // experts whose group tables are kept in shared memory
 // Epilogue stores: true = 32 x 32 blocks staged in shared memory and written
@@ -83,9 +93,9 @@ struct Cfg {
     static constexpr uint32_t NUM_BARS = 2 * STAGES + 7;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 256;
     static constexpr uint32_t OFF_GRP = OFF_MISC + 256;  // group tables (grouped modes, E <= kMaxTableE)
-    // epilogue store staging: 4 warps x 2 slots x (32 rows x 64 bytes), 1024-aligned
+    // epilogue store staging: kEpiWarps x kStoreSlots x (32 rows x 64 bytes), 1024-aligned
     static constexpr uint32_t OFF_STORE = (OFF_GRP + 2 * 8 * (kMaxTableE + 1) + 1023) / 1024 * 1024;
-    static constexpr uint32_t SMEM_ALLOC = OFF_STORE + 4 * 2 * 2048 + 1024;  // + slack to align the base
+    static constexpr uint32_t SMEM_ALLOC = OFF_STORE + kEpiWarps * kStoreSlots * 2048 + 1024;  // + slack to align the base
     static_assert(NUM_BARS * 8 <= 256, "barrier area");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
@@ -505,9 +515,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     using C = Cfg<CG>;
     constexpr bool CLUSTER = CG == 2;             // CTAs work in pairs
     constexpr int STAGES = C::STAGES;
-    // the epilogue's 64-column quarter after which the scale-slot columns are read
-    constexpr int kHeadQuarter = (STAGES * SF_STRIDE - 1) / 64;
-    static_assert(kHeadQuarter < 4, "scale slots fit in one bank");
+    // the scale-slot columns [0, STAGES * 16) are drained by the epilogue warps
+    // of column part 0, in their 64-column step kHeadStep
+    constexpr int kHeadStep = (STAGES * SF_STRIDE - 1) / 64;
+    static_assert(STAGES * SF_STRIDE <= kEpiCols, "scale slots lie in column part 0");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -557,9 +568,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             mbar_init(bar_accf, 1);
             mbar_init(bar_accf1, 1);
-            // one arrival per epilogue warp (of both CTAs of a pair)
-            mbar_init(bar_acce, 4 * CG);
-            mbar_init(bar_acce1, 4 * CG);
+            // one arrival per epilogue warp (of both CTAs of a pair); the head
+            // is read by the 4 warps of column part 0
+            mbar_init(bar_acce, kEpiWarps * CG);
+            mbar_init(bar_acce1, kEpiWarps * CG);
             mbar_init(bar_headf0, 4 * CG);
             mbar_init(bar_headf1, 4 * CG);
             mbar_init(bar_drain, 1);
@@ -786,91 +798,59 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------------------------------------------- epilogue
         // Drain the accumulator into registers (bf16), release it to the MMA
         // warp, then store: the global stores overlap the next tile's mainloop.
-        const int sub = warp & 3;
+        // Two warps per TMEM lane quadrant: warp `ew` drains rows 32 sub ..
+        // 32 sub + 31 (its quadrant) of columns [kEpiCols part, +kEpiCols).
+        const int ew = warp - 2, sub = warp & 3, part = ew >> 2;
         uint32_t acc_it = 0;
-        const uint32_t st_slots = sbase + C::OFF_STORE + 2 * 2048 * sub;  // this warp's two staging slots
-        uint32_t st_count = 0;                                            // blocks this warp has stored
+        const uint32_t st_slots = sbase + C::OFF_STORE + kStoreSlots * 2048 * ew;  // this warp's staging slots
+        uint32_t st_count = 0;                                                     // blocks this warp has stored
         for (int64_t tile = first; run && tile < p.total_tiles; tile += step) {
             const TileInfo ti = resolve_tile<CG>(p, tile, lane, rank, gt);
             if (!ti.valid) break;
             const int64_t grow = ti.out_row0 + 32 * sub + lane;
             const bool row_ok = grow >= ti.row_lo && grow < ti.row_hi;
             __nv_bfloat16 *crow = p.c + ti.c_off + grow * p.ldc;
+            const int64_t pcol0 = ti.col0 + kEpiCols * part;  // first column of this warp's part
             if (ti.nkb == 0) {  // empty group: its weight gradient is zero
                 if (row_ok) {
-                    int64_t col = ti.col0;
-                    for (; col + 8 <= ti.col_hi; col += 8) *reinterpret_cast<uint4 *>(crow + col) = make_uint4(0, 0, 0, 0);
-                    for (; col < ti.col_hi; col++) crow[col] = __float2bfloat16_rn(0.0f);
+                    const int64_t pend = min(ti.col_hi, pcol0 + kEpiCols);
+                    int64_t col = pcol0;
+                    for (; col + 8 <= pend; col += 8) *reinterpret_cast<uint4 *>(crow + col) = make_uint4(0, 0, 0, 0);
+                    for (; col < pend; col++) crow[col] = __float2bfloat16_rn(0.0f);
                 }
                 continue;
             }
             const uint32_t bank = acc_it & 1;
             if (!mbar_wait(bank ? bar_accf1 : bar_accf, (acc_it >> 1) & 1, abort_flag, &g_device_error)) break;
             tc_fence_after();
-            const uint32_t acc_t = tmem + 256 * bank;
-            // four quarters of 2 x 32 columns: two TMEM loads in flight per wait
-            uint32_t pk[BN / 2];
-#pragma unroll
-            for (int h = 0; h < 4; h++) {
-                uint32_t r[2][32];
-#pragma unroll
-                for (int q = 0; q < 2; q++) {
-                    const int ch = 2 * h + q;
-                    if (ti.col0 + 32 * ch < ti.col_hi)  // warp-uniform
-                        tmem_ld_32x32b_x32(acc_t + (static_cast<uint32_t>(32 * sub) << 16) + 32 * ch, r[q]);
-                }
-                tc_wait_ld();
-                if (h == kHeadQuarter) {  // head read: the next tile may put its scales there
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (CG == 2) mbar_arrive_cluster(lead_headf0 + 8 * bank);
-                        else mbar_arrive(bar_headf0 + 8 * bank);
-                    }
-                }
-#pragma unroll
-                for (int q = 0; q < 2; q++) {
-                    const int ch = 2 * h + q;
-                    if (ti.col0 + 32 * ch < ti.col_hi) {
-                        if constexpr (BIAS) add_bias32(r[q], p.bias, ti.col0 + 32 * ch, ti.col_hi);
-#pragma unroll
-                        for (int i = 0; i < 16; i++)
-                            pk[16 * ch + i] =
-                                pack_bf16x2(__uint_as_float(r[q][2 * i]), __uint_as_float(r[q][2 * i + 1]));
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (CG == 2) mbar_arrive_cluster(bank ? lead_acce + 24 : lead_acce);
-                else mbar_arrive(bank ? bar_acce1 : bar_acce);
-            }
-            acc_it++;
-            // TMA stores take whole 32-row boxes: this warp's rows must all belong
-            // to the tile's output (always for dense problems, where the tensor
-            // map clips rows past M; grouped tiles mask rows of other experts).
+            const uint32_t acc_t = tmem + 256 * bank + (static_cast<uint32_t>(32 * sub) << 16);
+            // How this warp's 32 x 32 blocks are stored (warp-uniform):
+            //  1: 4 x 4 transposes of 16-byte chunks inside each group of 4 lanes
+            //     (two xor-shuffle rounds, in place) leave lane 4g + c with chunk
+            //     c of rows 4g .. 4g + 3, so each store instruction writes 8 rows
+            //     x 64 contiguous bytes; rows outside the tile's output are
+            //     masked per lane, a block cut by the last column goes row by row;
+            //  2: staged in a 64-byte-swizzled slot (conflict-free 16-byte writes)
+            //     and stored by TMA, which takes whole 32-row boxes -- this warp's
+            //     rows must all belong to the tile's output (always for dense
+            //     problems, where the tensor map clips rows past M and columns
+            //     past N; grouped tiles mask rows of other experts);
+            //  0: each lane stores its own row.
             const int64_t wrow0 = ti.out_row0 + 32 * sub;
-            if (!kEpilogueTma && p.vec_store) {
-                // Per 32 x 32 block: a 4 x 4 transpose of 16-byte chunks inside each
-                // group of 4 lanes (two xor-shuffle rounds, in place) leaves lane
-                // 4g + c with chunk c of rows 4g .. 4g + 3, so each store
-                // instruction writes 8 rows x 64 contiguous bytes.  Rows outside the
-                // tile's output are masked per lane; a block cut by the last column
-                // goes row by row.
-                const int c4 = lane & 3;
-                const int64_t r0 = wrow0 + 4 * (lane >> 2);
-                uint8_t *wp = reinterpret_cast<uint8_t *>(p.c + ti.c_off + r0 * p.ldc + ti.col0 + 8 * c4);
-                const int64_t rstride = p.ldc * 2;
-                unsigned rmask = 0;
+            const int smode = (!kEpilogueTma && p.vec_store) ? 1
+                              : (p.tma_store && (p.mode == kDense || (wrow0 >= ti.row_lo && wrow0 + 32 <= ti.row_hi)))
+                                  ? 2
+                                  : 0;
+            const int c4 = lane & 3;
+            const int64_t r0 = wrow0 + 4 * (lane >> 2);
+            unsigned rmask = 0;
 #pragma unroll
-                for (int k = 0; k < 4; k++) rmask |= (r0 + k >= ti.row_lo && r0 + k < ti.row_hi ? 1u : 0u) << k;
-#pragma unroll
-                for (int ch = 0; ch < BN / 32; ch++) {
-                    const int64_t col = ti.col0 + 32 * ch;
-                    if (col >= ti.col_hi) break;  // warp-uniform
-                    uint32_t *m = pk + 16 * ch;    // chunk j, word w at m[4 * j + w]
-                    if (col + 32 <= ti.col_hi) {
+            for (int k = 0; k < 4; k++) rmask |= (r0 + k >= ti.row_lo && r0 + k < ti.row_hi ? 1u : 0u) << k;
+            auto store_chunk = [&](int lc, uint32_t (&m)[16]) {
+                const int64_t col = pcol0 + 32 * lc;
+                if (col >= ti.col_hi) return;  // warp-uniform
+                if (smode == 1) {
+                    if (col + 32 <= ti.col_hi) {  // m: chunk j, word w at m[4 * j + w]
 #pragma unroll
                         for (int j = 0; j < 4; j += 2)
 #pragma unroll
@@ -889,70 +869,90 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 if (lane & 2) m[4 * j + w] = rcv;
                                 else m[4 * j + 8 + w] = rcv;
                             }
+                        uint8_t *wp = reinterpret_cast<uint8_t *>(p.c + ti.c_off + r0 * p.ldc + col + 8 * c4);
 #pragma unroll
                         for (int k = 0; k < 4; k++)
                             if (rmask & (1u << k))
-                                *reinterpret_cast<uint4 *>(wp + k * rstride + 64 * ch) =
+                                *reinterpret_cast<uint4 *>(wp + k * p.ldc * 2) =
                                     make_uint4(m[4 * k], m[4 * k + 1], m[4 * k + 2], m[4 * k + 3]);
-                    } else if (row_ok) {
-#pragma unroll
-                        for (int i = 0; i < 32; i++)
-                            if (col + i < ti.col_hi)
-                                reinterpret_cast<uint16_t *>(crow)[col + i] =
-                                    static_cast<uint16_t>(m[i >> 1] >> (16 * (i & 1)));
+                        return;
                     }
-                }
-                continue;
-            }
-            if (p.tma_store && (p.mode == kDense || (wrow0 >= ti.row_lo && wrow0 + 32 <= ti.row_hi))) {
-                // Stage each 32 x 32 block in a 64-byte-swizzled slot (conflict-free
-                // 16-byte writes) and store it with TMA; columns past N are clipped
-                // by the tensor map.
-                const int64_t trow = ti.c_off / p.ldc + wrow0;
-#pragma unroll
-                for (int ch = 0; ch < BN / 32; ch++) {
-                    const int64_t col = ti.col0 + 32 * ch;
-                    if (col >= ti.col_hi) break;  // warp-uniform
-                    const uint32_t slot = st_slots + 2048 * (st_count & 1);
-                    if (st_count >= 2) {
-                        if (lane == 0) bulk_wait_read_le1();
+                } else if (smode == 2) {
+                    const uint32_t slot = st_slots + 2048 * (st_count % kStoreSlots);
+                    if (st_count >= static_cast<uint32_t>(kStoreSlots)) {  // the slot's previous store has read it
+                        if (lane == 0) bulk_wait_read<kStoreSlots - 1>();
                         __syncwarp();
                     }
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
                         const uint32_t dst = slot + 64 * lane + 16 * (q ^ ((lane >> 1) & 3));
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[16 * ch + 4 * q]),
-                                     "r"(pk[16 * ch + 4 * q + 1]), "r"(pk[16 * ch + 4 * q + 2]), "r"(pk[16 * ch + 4 * q + 3])
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(m[4 * q]),
+                                     "r"(m[4 * q + 1]), "r"(m[4 * q + 2]), "r"(m[4 * q + 3])
                                      : "memory");
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmC, slot, static_cast<int>(col), static_cast<int>(trow));
+                        tma_store_2d(&tmC, slot, static_cast<int>(col), static_cast<int>(ti.c_off / p.ldc + wrow0));
                         bulk_commit_group();
                     }
                     st_count++;
+                    return;
                 }
-                continue;
-            }
-            if (!row_ok) continue;
-#pragma unroll
-            for (int ch = 0; ch < BN / 32; ch++) {
-                const int64_t col = ti.col0 + 32 * ch;
+                if (!row_ok) return;
                 if (col + 32 <= ti.col_hi) {
                     uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
 #pragma unroll
-                    for (int i = 0; i < 4; i++)
-                        dst[i] = make_uint4(pk[16 * ch + 4 * i], pk[16 * ch + 4 * i + 1], pk[16 * ch + 4 * i + 2],
-                                            pk[16 * ch + 4 * i + 3]);
-                } else if (col < ti.col_hi) {
+                    for (int i = 0; i < 4; i++) dst[i] = make_uint4(m[4 * i], m[4 * i + 1], m[4 * i + 2], m[4 * i + 3]);
+                } else {
 #pragma unroll
                     for (int i = 0; i < 32; i++)
                         if (col + i < ti.col_hi)
-                            reinterpret_cast<uint16_t *>(crow)[col + i] =
-                                static_cast<uint16_t>(pk[16 * ch + (i >> 1)] >> (16 * (i & 1)));
+                            reinterpret_cast<uint16_t *>(crow)[col + i] = static_cast<uint16_t>(m[i >> 1] >> (16 * (i & 1)));
+                }
+            };
+            // Drain this warp's part: two TMEM loads in flight per wait, rounded
+            // to bf16 as they arrive; the accumulator goes back to the MMA warp
+            // as soon as the last load has landed, and the stores follow.
+            uint32_t pk[kEpiChunks][16];
+#pragma unroll
+            for (int h = 0; h < kEpiChunks / 2; h++) {
+                uint32_t r[2][32];
+#pragma unroll
+                for (int q = 0; q < 2; q++) {
+                    const int ch = kEpiChunks * part + 2 * h + q;
+                    if (ti.col0 + 32 * ch < ti.col_hi)  // warp-uniform
+                        tmem_ld_32x32b_x32(acc_t + 32 * ch, r[q]);
+                }
+                tc_wait_ld();
+                if (part == 0 && h == kHeadStep) {  // head read: the next tile may put its scales there
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 2) mbar_arrive_cluster(lead_headf0 + 8 * bank);
+                        else mbar_arrive(bar_headf0 + 8 * bank);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 2; q++) {
+                    const int ch = kEpiChunks * part + 2 * h + q;
+                    if (ti.col0 + 32 * ch < ti.col_hi) {
+                        if constexpr (BIAS) add_bias32(r[q], p.bias, ti.col0 + 32 * ch, ti.col_hi);
+#pragma unroll
+                        for (int i = 0; i < 16; i++)
+                            pk[2 * h + q][i] = pack_bf16x2(__uint_as_float(r[q][2 * i]), __uint_as_float(r[q][2 * i + 1]));
+                    }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 2) mbar_arrive_cluster(bank ? lead_acce + 24 : lead_acce);
+                else mbar_arrive(bank ? bar_acce1 : bar_acce);
+            }
+            acc_it++;
+#pragma unroll
+            for (int lc = 0; lc < kEpiChunks; lc++) store_chunk(lc, pk[lc]);
         }
     }
 
