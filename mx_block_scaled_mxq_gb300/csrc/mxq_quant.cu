@@ -180,6 +180,67 @@ __device__ __forceinline__ uint32_t mx4_e4m3_code(uint32_t ax, const Mx4Blk &B) 
     const uint32_t lo = ax >= B.t075 ? 0x38u : (ax >= B.t025 ? 0x30u : 0u);
     return ax >= B.s ? (r >> 20) - static_cast<uint32_t>(0x3C0 + 8 * B.e) : lo;
 }
+// The same rule through the hardware E2M1 conversion, which rounds to nearest
+// with ties to the even code and saturates at +-6: it agrees with the rule
+// everywhere but on the midpoints whose lower neighbour is the even code --
+// y = 1/4 and y = 1.25 x 2^k (k = 0, 1, 2: 1.25, 2.5, 5) -- where the rule
+// goes up.  Moving |x| one ulp up exactly there (x's bits + 1; the scaled
+// value is then no longer a tie) makes the conversion go up too; elsewhere
+// the ulp moves no value across a midpoint, since every midpoint is an fp32
+// value of that exponent.  y = x 2^-e is exact (a power-of-two scaling; a
+// result too small for a normal fp32 rounds to zero either way).
+__device__ __forceinline__ float mx4_scaled(uint32_t xb, uint32_t t025, float inv_s) {
+    const bool tie = (xb & 0x7FFFFFu) == 0x200000u || (xb & 0x7FFFFFFFu) == t025;
+    return __uint_as_float(xb + (tie ? 1u : 0u)) * inv_s;
+}
+// Two bf16 at once, one per 16-bit half of w: each moved one bf16 ulp up in
+// magnitude where it sits on such a midpoint (mantissa pattern 1.25, or equal
+// to s/4, whose bf16 bits are t025x2 in both halves); one bf16 ulp moves no
+// value across a midpoint either.  A half h <= 0x7FFF is zero exactly when
+// h + 0x7FFF leaves bit 15 clear (no carry reaches the other half).
+__device__ __forceinline__ uint32_t mx4_untie2(uint32_t w, uint32_t t025x2) {
+    const uint32_t m = (w & 0x007F007Fu) ^ 0x00200020u;  // zero half: mantissa pattern 1.25
+    const uint32_t q = (w & 0x7FFF7FFFu) ^ t025x2;       // zero half: |x| = s/4
+    const uint32_t z = ~((m + 0x7FFF7FFFu) & (q + 0x7FFF7FFFu)) & 0x80008000u;
+    return w + (z >> 15);
+}
+// 2^-e for a block exponent e in [-30, 127] (2^-127 is a subnormal).
+__device__ __forceinline__ float mx4_inv_scale(int e) {
+    return __uint_as_float(e <= 126 ? static_cast<uint32_t>(127 - e) << 23 : 0x00400000u);
+}
+// E2M1 codes (sign | index) of two scaled values: lo in the low nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+    uint16_t r;
+    asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\tcvt.u16.u8 %0, b;\n\t}" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// bf16 pair of the rule's values of two scaled values lo, hi (RNE E2M1
+// conversion, tie-fixed inputs) times 2^e: lo in the low half (exact: a
+// codebook value times a power of two).
+__device__ __forceinline__ uint32_t e2m1_qdq_bf16x2(float lo, float hi, float s) {
+    float f0, f1;
+    asm("{\n\t.reg .b8 b;\n\t.reg .b32 h;\n\t.reg .f16 a0, a1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b, %3, %2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h, b;\n\t"
+        "mov.b32 {a0, a1}, h;\n\t"
+        "cvt.f32.f16 %0, a0;\n\t"
+        "cvt.f32.f16 %1, a1;\n\t}"
+        : "=f"(f0), "=f"(f1) : "f"(lo), "f"(hi));
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f1 * s), "f"(f0 * s));
+    return r;
+}
+// E4M3 codes (low byte: lo) of the E2M1 values of two scaled values lo, hi
+// (every E2M1 value is an E4M3 value: both decodings are exact).
+__device__ __forceinline__ uint32_t e2m1_as_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("{\n\t.reg .b8 b;\n\t.reg .b32 h;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h, b;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f16x2 %0, h;\n\t}"
+        : "=h"(r) : "f"(lo), "f"(hi));
+    return r;
+}
 
 // ============================================================================
 // Row quant: 128 x 128 tile per CTA, blocks along cols (cols % 32 == 0).
@@ -195,14 +256,20 @@ __device__ __forceinline__ uint32_t mx4_e4m3_code(uint32_t ax, const Mx4Blk &B) 
 // low half of word k) under block B: sign | the E4M3 code of the E2M1 value;
 // the NaN code 0x7F | sign for a non-finite block.
 __device__ __forceinline__ uint2 mx4_as_e4m3_codes8(const uint32_t (&w)[4], const Mx4Blk &B, bool nonfinite) {
-    uint32_t b[2] = {0, 0};
+    uint32_t c[4];
+    if (nonfinite) {
 #pragma unroll
-    for (int k = 0; k < 8; k++) {
-        const uint32_t bits = (k & 1) ? (w[k >> 1] & 0xFFFF0000u) : (w[k >> 1] << 16);
-        const uint32_t mag = nonfinite ? 0x7Fu : mx4_e4m3_code(bits & 0x7FFFFFFFu, B);
-        b[k >> 2] |= (((bits >> 24) & 0x80u) | mag) << (8 * (k & 3));
+        for (int k = 0; k < 4; k++) c[k] = 0x007F007Fu | ((w[k] >> 8) & 0x00800080u);
+    } else {
+        const float inv = mx4_inv_scale(B.e);
+        const uint32_t t2 = (B.t025 >> 16) * 0x10001u;
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const uint32_t u = mx4_untie2(w[k], t2);
+            c[k] = e2m1_as_e4m3x2(__uint_as_float(u << 16) * inv, __uint_as_float(u & 0xFFFF0000u) * inv);
+        }
     }
-    return make_uint2(b[0], b[1]);
+    return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
 }
 
 template <typename InT, int FMT>
@@ -988,45 +1055,123 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restr
     }
 }
 
-// MXFP4 quant-dequant of bf16 to bf16 (cols % 32 == 0, 16-byte aligned): 8
-// elements per chunk, 4 lanes per block, the vector path's windows.  Every
-// result (codebook value x 2^e, or NaN for a non-finite block) is exact in
-// bf16, so the fp32 result's upper half is the bf16 result.
+// MXFP4 quant-dequant of bf16 to bf16 (cols % 32 == 0, 16-byte aligned): a
+// thread takes whole 32-element blocks (four 16-byte chunks each), two blocks
+// in flight; a CTA takes a window of 2 x 256 blocks.  Every result (codebook
+// value x 2^e, or NaN for a non-finite block) is exact in bf16.
+constexpr int64_t kBlkWindow = static_cast<int64_t>(kThreads) * 2;
 __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_bf16(const uint16_t *__restrict__ x, uint16_t *y,
-                                                             int64_t nchunks, float sf) {
-    for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kEwWindow; w0 < nchunks;
-         w0 += static_cast<int64_t>(gridDim.x) * kEwWindow) {
-        uint4 in[kEwChunks];
+                                                             int64_t nblocks, float sf) {
+    for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kBlkWindow; w0 < nblocks;
+         w0 += static_cast<int64_t>(gridDim.x) * kBlkWindow) {
+        uint4 in[2][4];
 #pragma unroll
-        for (int u = 0; u < kEwChunks; u++) {
-            const int64_t g = w0 + u * kThreads + threadIdx.x;
-            in[u] = g < nchunks ? ldg_nc_v4(x + 8 * g) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < 2; u++) {
+            const int64_t b = w0 + u * kThreads + threadIdx.x;
+#pragma unroll
+            for (int j = 0; j < 4; j++) in[u][j] = b < nblocks ? ldg_nc_v4(x + 32 * b + 8 * j) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < kEwChunks; u++) {
-            const int64_t g = w0 + u * kThreads + threadIdx.x;
-            const uint32_t w[4] = {in[u].x, in[u].y, in[u].z, in[u].w};
-            uint32_t a = amax8_bf16(w) << 16;  // |bf16| bits as fp32 bits
-            a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
-            a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
-            if (g >= nchunks) continue;
-            uint32_t o[4];
+        for (int u = 0; u < 2; u++) {
+            const int64_t b = w0 + u * kThreads + threadIdx.x;
+            if (b >= nblocks) continue;
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                w[4 * j] = in[u][j].x; w[4 * j + 1] = in[u][j].y; w[4 * j + 2] = in[u][j].z; w[4 * j + 3] = in[u][j].w;
+            }
+            uint32_t m2 = 0;
+#pragma unroll
+            for (int k = 0; k < 16; k++) m2 = __vmaxu2(m2, w[k] & 0x7FFF7FFFu);
+            const uint32_t a = max(m2 & 0xFFFFu, m2 >> 16) << 16;  // |bf16| bits as fp32 bits
+            uint32_t o[16];
             if (a >= 0x7F800000u) {
 #pragma unroll
-                for (int k = 0; k < 4; k++) o[k] = 0x7FC07FC0u;
+                for (int k = 0; k < 16; k++) o[k] = 0x7FC07FC0u;
             } else {
-                const Mx4Blk B = mx4_block(mx4_exp(__uint_as_float(a), sf));
+                const int e = mx4_exp(__uint_as_float(a), sf);
+                const float inv = mx4_inv_scale(e), sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+                const uint32_t t2 = static_cast<uint32_t>(e + 125) * 0x800080u;  // s/4 as bf16, both halves
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const uint32_t lo = w[k] << 16, hi = w[k] & 0xFFFF0000u;
-                    const uint32_t qlo = mx4_snap(lo & 0x7FFFFFFFu, B) | (lo & 0x80000000u);
-                    const uint32_t qhi = mx4_snap(hi & 0x7FFFFFFFu, B) | (hi & 0x80000000u);
-                    o[k] = (qlo >> 16) | qhi;
+                for (int k = 0; k < 16; k++) {
+                    const uint32_t v = mx4_untie2(w[k], t2);
+                    o[k] = e2m1_qdq_bf16x2(__uint_as_float(v << 16) * inv, __uint_as_float(v & 0xFFFF0000u) * inv, sc);
                 }
             }
-            stg_v4(y + 8 * g, make_uint4(o[0], o[1], o[2], o[3]));
+#pragma unroll
+            for (int j = 0; j < 4; j++) stg_v4(y + 32 * b + 8 * j, make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]));
         }
     }
+}
+
+// Packed MXFP4 quant of an [R x C] tensor (fp32 or bf16, leading dim ldx)
+// with R and C multiples of 128, so that every scale tile is whole and has no
+// padding.  A CTA takes a block of 64 rows x 128 columns: thread t quantizes
+// the 32-element block t % 4 of row t / 4 (all of its loads issued first, one
+// scale decision per block) into 16 bytes of nibbles (even element in the low
+// nibble); the 4 lanes holding a row's 4 blocks put its scale bytes together,
+// one 16-byte row-group word of its scale tile, stored as one word.
+template <typename InT>
+__global__ void __launch_bounds__(kThreads) k_pack_mxfp4(const InT *__restrict__ x, int64_t ldx,
+                                                         uint8_t *__restrict__ q, int64_t ldq,
+                                                         uint8_t *__restrict__ s, int64_t kb_tiles, float sf) {
+    constexpr int kWords = sizeof(InT) == 4 ? 32 : 16;  // 32-bit words of one block
+    const int t = threadIdx.x, lane = t & 31, blk = t & 3;
+    const int64_t r = static_cast<int64_t>(blockIdx.y) * 64 + (t >> 2);
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * 128 + 32 * blk;
+    uint32_t w[kWords];
+    const InT *src = x + r * ldx + c;
+#pragma unroll
+    for (int j = 0; j < kWords / 8; j++) {
+        uint4 lo, hi;
+        ldg_nc_v8(reinterpret_cast<const uint32_t *>(src) + 8 * j, lo, hi);
+        w[8 * j] = lo.x; w[8 * j + 1] = lo.y; w[8 * j + 2] = lo.z; w[8 * j + 3] = lo.w;
+        w[8 * j + 4] = hi.x; w[8 * j + 5] = hi.y; w[8 * j + 6] = hi.z; w[8 * j + 7] = hi.w;
+    }
+    uint32_t a = 0;
+    if (sizeof(InT) == 4) {
+#pragma unroll
+        for (int k = 0; k < kWords; k++) a = max(a, w[k] & 0x7FFFFFFFu);
+    } else {
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int k = 0; k < kWords; k++) m2 = __vmaxu2(m2, w[k] & 0x7FFF7FFFu);
+        a = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+    }
+    const bool nonfinite = a >= 0x7F800000u;
+    const int e = nonfinite ? 0 : mx4_exp(__uint_as_float(a), sf);
+    const uint32_t sbyte = nonfinite ? 0xFFu : static_cast<uint32_t>(e + 127);
+    uint32_t nib[4];  // 8 nibbles each
+    const float inv = mx4_inv_scale(e);
+    const uint32_t t025 = static_cast<uint32_t>(e + 125) << 23;
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+        uint32_t v[8];  // fp32 bit patterns of elements 8g .. 8g + 7
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            v[k] = sizeof(InT) == 4 ? w[8 * g + k] : ((k & 1) ? (w[4 * g + (k >> 1)] & 0xFFFF0000u) : (w[4 * g + (k >> 1)] << 16));
+        if (nonfinite) {
+            uint32_t p = 0;
+#pragma unroll
+            for (int k = 0; k < 8; k++) p |= (((v[k] >> 28) & 8u) | 7u) << (4 * k);
+            nib[g] = p;
+        } else {
+            uint32_t b[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+                b[k] = cvt_e2m1x2(mx4_scaled(v[2 * k], t025, inv), mx4_scaled(v[2 * k + 1], t025, inv));
+            nib[g] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+        }
+    }
+    stg_v4(q + r * ldq + c / 2, make_uint4(nib[0], nib[1], nib[2], nib[3]));
+    // the row's 4 scale bytes, from lanes 4i .. 4i + 3
+    uint32_t word = sbyte << (8 * blk);
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    if (blk == 0)
+        *reinterpret_cast<uint32_t *>(s + ((r >> 7) * kb_tiles + blockIdx.x) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3)) =
+            word;
+    (void)lane;
 }
 
 // Clipped straight-through estimator, backward: gx = gy except +0.0 where the
@@ -1097,8 +1242,8 @@ __global__ void __launch_bounds__(kThreads) k_ste_backward_gen(const float *__re
 // CTAs for the windowed elementwise kernels: one window each, so the hardware
 // hands out short CTAs as SMs free up (no persistent loop whose last round
 // runs part-empty); capped, with the kernels looping past the cap.
-int grid_windows(int64_t nchunks) {
-    const int64_t g = (nchunks + kEwWindow - 1) / kEwWindow;
+int grid_windows(int64_t nchunks, int64_t window = kEwWindow) {
+    const int64_t g = (nchunks + window - 1) / window;
     return static_cast<int>(g < 1 ? 1 : (g > (1 << 20) ? (1 << 20) : g));
 }
 
@@ -1140,6 +1285,14 @@ cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, i
         k_quant_rows<uint16_t, 0><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf);
     } else if (fmt == 2) {
         k_quant_rows<uint16_t, 2><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf);
+    } else if (R % kTile == 0 && C % kTile == 0 &&
+               ((reinterpret_cast<uintptr_t>(x) | static_cast<uintptr_t>(ldx * (fp32_in ? 4 : 2))) & 31) == 0) {
+        // whole scale tiles: 64 x 128 blocks
+        const dim3 g2(static_cast<unsigned>(C / kTile), static_cast<unsigned>(R / 64));
+        if (fp32_in)
+            k_pack_mxfp4<float><<<g2, kThreads, 0, st>>>(static_cast<const float *>(x), ldx, q, C / 2, s, kb_tiles, sf);
+        else
+            k_pack_mxfp4<uint16_t><<<g2, kThreads, 0, st>>>(xb, ldx, q, C / 2, s, kb_tiles, sf);
     } else if (fp32_in) {
         k_quant_rows<float, 1><<<grid, kThreads, 0, st>>>(static_cast<const float *>(x), R, C, ldx, q, C / 2, s,
                                                           kb_tiles, sf);
@@ -1254,8 +1407,8 @@ cudaError_t launch_qdq_mxfp4(const float *x, float *y, uint32_t *mask, int64_t r
 
 cudaError_t launch_qdq_mxfp4_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols, float sf,
                                   cudaStream_t st) {
-    const int64_t nchunks = rows * cols / 8;
-    k_qdq_mxfp4_bf16<<<grid_windows(nchunks), kThreads, 0, st>>>(x, y, nchunks, sf);
+    const int64_t nblocks = rows * cols / 32;
+    k_qdq_mxfp4_bf16<<<grid_windows(nblocks, kBlkWindow), kThreads, 0, st>>>(x, y, nblocks, sf);
     return cudaGetLastError();
 }
 

@@ -152,3 +152,30 @@ def test_bf16_qdq_bit_exact(mxq, shape, sf):
     assert np.array_equal(torch.from_numpy(ref).to(torch.bfloat16).to(torch.float32).numpy().view(np.uint32),
                           ref.view(np.uint32))  # exact in bf16
     assert np.array_equal(y.view(torch.int16).numpy(), torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy())
+
+
+def test_bf16_qdq_every_bf16_pattern_under_six_scales(mxq):
+    """Every finite bf16 pattern p, each in its own block of 32 whose maximum
+    is an anchor 1.5 * 2^(E_p + j), j = 0..5, so that p / scale falls in every
+    codebook interval and on every midpoint of the MXFP4 rule ("AMCT FakeQuant
+    模拟伪量化工具包", section 2): the bf16 quant-dequant equals the fp32 oracle
+    on the widened values, bit for bit."""
+    pats = np.arange(1 << 16, dtype=np.uint32)
+    f = (pats << 16).view(np.float32)
+    p = f[np.isfinite(f) & (f != 0)]
+    e_p = np.floor(np.log2(np.abs(p).astype(np.float64))).astype(np.int64)
+    rows = []
+    for j in range(6):
+        blk = np.zeros((p.size, 32), np.float32)
+        blk[:, 0] = (1.5 * np.exp2(np.minimum(e_p + j, 127))).astype(np.float32)
+        blk[:, 1] = p
+        rows.append(blk)
+    a = np.concatenate(rows)
+    a = a[np.isfinite(a).all(axis=1)]
+    # keep the blocks whose anchor bf16 holds exactly (not the deepest subnormal ones)
+    a = a[torch.from_numpy(a[:, 0]).to(torch.bfloat16).to(torch.float32).numpy() == a[:, 0]]
+    xb = torch.from_numpy(a).to(torch.bfloat16)
+    assert torch.equal(xb.to(torch.float32), torch.from_numpy(a))
+    y = mxq.qdq_mxfp4(xb.to(DEV), 6.0).cpu()
+    ref = oracle.mxfp4_qdq(a, np.float32(6.0))
+    assert np.array_equal(y.view(torch.int16).numpy(), torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy())

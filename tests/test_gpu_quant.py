@@ -128,7 +128,7 @@ def test_qdq_mxfp4_in_place(mxq):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("R,C", [(48, 160), (128, 128), (300, 4096)])
+@pytest.mark.parametrize("R,C", [(48, 160), (128, 128), (300, 4096), (512, 4096), (4096, 4096)])
 def test_packed_mxfp4_bit_exact(mxq, dtype, R, C):
     a = mxq_inputs.mxfp4_large(R, C, seed=R)
     t = torch.from_numpy(a).to(dtype)
