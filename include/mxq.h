@@ -347,8 +347,11 @@ mxq_status mxq_linear_bwd_dx_wq(const void *dy, const void *wcache, int64_t M, i
  * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
  *
  * The first call on a device looks up the scratch's device address
- * (cudaGetSymbolAddress) with that device current: make that first call
- * before any stream capture.  All calls share the one scratch array, which
+ * (cudaGetSymbolAddress) with that device current and keeps it for the life
+ * of the process: make that first call before any stream capture.  A
+ * cudaDeviceReset (or anything else that destroys the device's primary
+ * context) invalidates the kept address: after one, do not call this entry
+ * point on that device again in the same process.  All calls share the one scratch array, which
  * keeps the last call's contents; each call rewrites everything it reads, so
  * nothing needs clearing.  Calls whose GPU work can overlap (on different
  * streams, or from different host threads) race on the array and corrupt
@@ -365,7 +368,9 @@ mxq_status mxq_linear_fwd_noalloc(const void *x, const void *w, int64_t M, int64
 const char *mxq_last_error_string(void);
 
 /* Synchronizes the current device, then reads and clears the device-side
- * error word that kernels set when they give up (bit 0: an mbarrier wait
+ * error word (a variable inside the library, whose device address is looked
+ * up once per device and kept, so it too is invalid after a cudaDeviceReset)
+ * that kernels set when they give up (bit 0: an mbarrier wait
  * timed out; bit 1: a tensor-memory allocation failed; bit 2: a grouped
  * kernel found its group offsets malformed and did no work).  Returns
  * MXQ_ERR_INVALID_ARG if bit 2 was set, else MXQ_ERR_TIMEOUT if any bit was

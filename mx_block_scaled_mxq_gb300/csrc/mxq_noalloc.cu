@@ -13,7 +13,10 @@
 //
 // The array's name is only a host-side stand-in for host code; its device
 // address is looked up once per device with cudaGetSymbolAddress (on the
-// first call made with that device current) and passed to the kernels.
+// first call made with that device current) and passed to the kernels.  The
+// kept address belongs to the device's primary context: a cudaDeviceReset
+// makes it stale (the header tells callers not to use this entry point on
+// that device afterwards).
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
