@@ -26,15 +26,17 @@
  *    magnitude), and per-row zero padding of a ragged last dimension
  *    (section 3.3, padding convention).
  *
- * Readings taken where the pages are silent (each listed in the design notes):
+ * Readings taken where the pages are silent:
  *  - round(log2 r) is evaluated in exact real arithmetic.  r = amax/sf is
  *    rational and log2 r is a half-integer only for irrational r, so no tie can
  *    occur and the rounding direction of "round" never matters.
  *  - non-finite blocks: an MXFP8 block whose amax is Inf or NaN gets scale byte
  *    0xFF and every code 0x7F | sign; an MXFP4 block with a non-finite amax
  *    yields NaN for every element (QDQ) and scale byte 0xFF with nibble 0x7|sign
- *    (packed).  Parity unpinned: the pages say nothing and no test feeds such
- *    inputs.
+ *    (packed).  Partly pinned by library casts and IEEE arithmetic (the scale
+ *    byte, the non-finite elements' E4M3 codes, NaN on dequantization, NaN for
+ *    the finite elements' QDQ); parity unpinned for the finite elements' code
+ *    bytes, the non-finite element's own QDQ result and the packed nibble.
  *  - negative inputs that round to zero keep their sign (E4M3 code 0x80, QDQ
  *    output -0.0, E2M1 nibble 0x8).
  */

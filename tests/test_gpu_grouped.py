@@ -115,7 +115,9 @@ def test_grouped_dirichlet_32_experts(mxq):
 def test_full_size_moe_sampled(mxq):
     """32 experts, 32768 routed rows (Dirichlet(0.5) sizes), K=7168, N=4096:
     forward and input gradient on sampled rows, weight gradient of the three
-    smallest non-empty experts in full and the empty ones exactly zero."""
+    smallest non-empty experts in full, of the two largest on sampled rows
+    (their contractions run over 4415 and 4740 rows: the most k-blocks and
+    stage-ring wraps of the launch), and the empty ones exactly zero."""
     E, T, K, N = 32, 32768, 7168, 4096
     off, x, w, dy = mxq_inputs.moe_inputs(E, T, K, N, seed=0)
     moe = MoE(mxq, off, x, w, dy)
@@ -152,6 +154,12 @@ def test_full_size_moe_sampled(mxq):
         a, sa = oracle.mxfp8_quant_cols(dy[r0:r1])
         b, sb = oracle.mxfp8_quant_cols(x[r0:r1])
         check_close(dw[e], oracle.gemm_ref(a, sa, b, sb))
+    for e in np.argsort(n)[-2:]:
+        r0, r1 = int(off[e]), int(off[e + 1])
+        a, sa = oracle.mxfp8_quant_cols(dy[r0:r1])
+        b, sb = oracle.mxfp8_quant_cols(x[r0:r1])
+        rows_n = np.unique(np.concatenate([rng.choice(N, 46, replace=False), [0, N - 1]]))
+        check_close(dw[int(e)][torch.from_numpy(rows_n).to(DEV)], oracle.gemm_ref(a[rows_n], sa[rows_n], b, sb))
     for e in np.nonzero(n == 0)[0]:
         assert not torch.any(dw[int(e)].float() != 0)
 
