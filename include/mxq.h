@@ -372,9 +372,12 @@ const char *mxq_last_error_string(void);
  * up once per device and kept, so it too is invalid after a cudaDeviceReset)
  * that kernels set when they give up (bit 0: an mbarrier wait
  * timed out; bit 1: a tensor-memory allocation failed; bit 2: a grouped
- * kernel found its group offsets malformed and did no work).  Returns
- * MXQ_ERR_INVALID_ARG if bit 2 was set, else MXQ_ERR_TIMEOUT if any bit was
- * set (*word receives the bits), MXQ_OK otherwise.  word may be NULL. */
+ * kernel found its group offsets malformed and did no work; bit 3: the debug
+ * build of the library, compiled with MXQ_DEBUG, found a computed address
+ * outside its buffer and skipped that access).  Returns MXQ_ERR_CUDA if bit 3
+ * was set, else MXQ_ERR_INVALID_ARG if bit 2 was set, else MXQ_ERR_TIMEOUT if
+ * any bit was set (*word receives the bits), MXQ_OK otherwise.  word may be
+ * NULL. */
 mxq_status mxq_poll_device_error(uint32_t *word);
 
 /* Failure-detection self-test (no counterpart on the pages): launches one

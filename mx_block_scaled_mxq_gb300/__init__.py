@@ -7,7 +7,9 @@ device addresses as ints); ``stream`` defaults to torch's current stream.  A
 non-OK status raises :class:`MXQError` with the library's reason.
 
 The compute path is the CUDA library only: if ``libmxq.so`` cannot be built or
-loaded, every call raises -- there is no fallback.
+loaded, every call raises -- there is no fallback.  With the environment
+variable ``MXQ_LIBRARY=debug`` the debug build ``libmxq_debug.so`` (bounds
+checks on every computed global access) is loaded instead.
 
 The ``alloc_*`` / ``quantize_*`` helpers at the bottom only size and allocate
 output tensors with the library's own size queries, then call the entry points.
@@ -86,19 +88,26 @@ _SIGNATURES = {
 }
 
 
+def _debug_requested() -> bool:
+    import os
+    return os.environ.get("MXQ_LIBRARY", "") == "debug"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.DEBUG_LIB if _debug_requested() else _build.LIB
 
 
 def load(build_if_needed: bool = True):
-    """Load libmxq.so (compiling it in-tree first if it is missing or stale)."""
+    """Load libmxq.so (compiling it in-tree first if it is missing or stale);
+    libmxq_debug.so under MXQ_LIBRARY=debug."""
     global _lib
     if _lib is None:
-        if not _build.up_to_date():
+        debug = _debug_requested()
+        if not _build.up_to_date(debug):
             if not build_if_needed:
-                raise MXQError(f"libmxq is not built at {_build.LIB}", -1)
-            _build.build()
-        lib = ctypes.CDLL(_build.LIB)
+                raise MXQError(f"libmxq is not built at {library_path()}", -1)
+            _build.build(debug=debug)
+        lib = ctypes.CDLL(library_path())
         for name, (res, args) in _SIGNATURES.items():
             fn = getattr(lib, name)
             fn.restype = res
@@ -248,10 +257,11 @@ def mxq_selftest_wait_timeout(timeout_ms, d_gave_up, stream=None):
 
 def mxq_poll_device_error():
     """Returns the device error bits (0 = none; bit 2 = malformed group
-    offsets); raises on a CUDA failure."""
+    offsets; bit 3 = an access outside its buffer, found by the debug build);
+    raises on a CUDA failure."""
     w = ctypes.c_uint32(0)
     st = load().mxq_poll_device_error(ctypes.byref(w))
-    if st not in (0, 1, 5) or (st == 1 and not w.value & 4):
+    if w.value == 0 and st != 0:
         _check(st, "mxq_poll_device_error")
     return int(w.value)
 

@@ -171,6 +171,11 @@ mxq_status mxq_poll_device_error(uint32_t *word) {
     e = mxq::read_and_clear_device_error(&w);
     if (e != cudaSuccess) return fail(MXQ_ERR_CUDA, "read device error word: %s", cudaGetErrorString(e));
     if (word) *word = w;
+    if (w & 8u)
+        return fail(MXQ_ERR_CUDA,
+                    "a bounds check of the debug build found an access outside its buffer and skipped it "
+                    "(device error bits 0x%x)",
+                    w);
     if (w & 4u)
         return fail(MXQ_ERR_INVALID_ARG,
                     "a grouped kernel found its group offsets malformed (they must rise from off[0] = 0 to "

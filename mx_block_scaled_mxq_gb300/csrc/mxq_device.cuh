@@ -12,9 +12,30 @@ namespace mxq {
 // Bits of the device-side error word a kernel sets when it gives up.
 // Bit 0: a bounded wait timed out.  Bit 1: a tensor-memory allocation failed.
 // Bit 2: a grouped kernel found its group offsets malformed and did no work.
+// Bit 3: a debug build (MXQ_DEBUG) found an access outside its buffer and
+// skipped it.
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrTmemAlloc = 2u;
 constexpr unsigned kErrBadOffsets = 4u;
+constexpr unsigned kErrBounds = 8u;
+
+// Debug builds (-DMXQ_DEBUG) check the address of every plain global load and
+// store that a kernel computes against the extent of the buffer it belongs
+// to: an access of n bytes at p outside [base, base + bytes) sets kErrBounds
+// and is skipped.  (TMA copies are clipped by their tensor maps.)  Release
+// builds compile the checks away.
+#ifdef MXQ_DEBUG
+__device__ __forceinline__ bool in_bounds(const void *p, uint64_t n, const void *base, uint64_t bytes,
+                                          unsigned int *err) {
+    const uint64_t a = reinterpret_cast<uint64_t>(p), b = reinterpret_cast<uint64_t>(base);
+    if (a >= b && a + n <= b + bytes) return true;
+    atomicOr(err, kErrBounds);
+    return false;
+}
+#define MXQ_IN_BOUNDS(p, n, base, bytes, err) ::mxq::in_bounds((p), (n), (base), (bytes), (err))
+#else
+#define MXQ_IN_BOUNDS(p, n, base, bytes, err) true
+#endif
 constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;  // 4 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

@@ -117,6 +117,7 @@ struct Params {
     int vec_store;         // rows of C are 16-byte aligned (coalesced 16-byte stores)
     const __nv_bfloat16 *bias;  // kDense: bf16 [N] added to every row in fp32, or null
     int64_t total_tiles;   // tile index space (an upper bound for grouped rows)
+    uint64_t sa_bytes, sb_bytes, c_bytes;  // buffer extents (checked by debug builds)
 };
 
 struct TileInfo {
@@ -642,10 +643,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + C::SFA_BYTES + 512u * ti.b_atoms);
                         tma_load_2d(sa_s, &tmA, fb, ka, static_cast<int>(ti.a_row0));
                         tma_load_2d(sb_s, &tmB, fb, kb_, static_cast<int>(ti.b_row0));
-                        bulk_load(sfa_s, p.sa + (ti.a_ratom * p.sa_kt + ti.a_katom0 + kb) * 512, 512, fb);
-                        for (int h = 0; h < ti.b_atoms; h++)
-                            bulk_load(sfb_s + 512 * h, p.sb + ((ti.b_ratom + h) * p.sb_kt + ti.b_katom0 + kb) * 512,
-                                      512, fb);
+                        const uint8_t *sa_src = p.sa + (ti.a_ratom * p.sa_kt + ti.a_katom0 + kb) * 512;
+                        // (a skipped copy leaves its bytes missing: the stage's wait times out)
+                        if (MXQ_IN_BOUNDS(sa_src, 512, p.sa, p.sa_bytes, &g_device_error)) bulk_load(sfa_s, sa_src, 512, fb);
+                        for (int h = 0; h < ti.b_atoms; h++) {
+                            const uint8_t *sb_src = p.sb + ((ti.b_ratom + h) * p.sb_kt + ti.b_katom0 + kb) * 512;
+                            if (MXQ_IN_BOUNDS(sb_src, 512, p.sb, p.sb_bytes, &g_device_error))
+                                bulk_load(sfb_s + 512 * h, sb_src, 512, fb);
+                        }
                     } else {
                         // both CTAs' loads complete on the even CTA's barrier, which
                         // expects the bytes of both (scale tiles past the buffer are
@@ -815,8 +820,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (row_ok) {
                     const int64_t pend = min(ti.col_hi, pcol0 + kEpiCols);
                     int64_t col = pcol0;
-                    for (; col + 8 <= pend; col += 8) *reinterpret_cast<uint4 *>(crow + col) = make_uint4(0, 0, 0, 0);
-                    for (; col < pend; col++) crow[col] = __float2bfloat16_rn(0.0f);
+                    for (; col + 8 <= pend; col += 8)
+                        if (MXQ_IN_BOUNDS(crow + col, 16, p.c, p.c_bytes, &g_device_error))
+                            *reinterpret_cast<uint4 *>(crow + col) = make_uint4(0, 0, 0, 0);
+                    for (; col < pend; col++)
+                        if (MXQ_IN_BOUNDS(crow + col, 2, p.c, p.c_bytes, &g_device_error))
+                            crow[col] = __float2bfloat16_rn(0.0f);
                 }
                 continue;
             }
@@ -872,7 +881,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         uint8_t *wp = reinterpret_cast<uint8_t *>(p.c + ti.c_off + r0 * p.ldc + col + 8 * c4);
 #pragma unroll
                         for (int k = 0; k < 4; k++)
-                            if (rmask & (1u << k))
+                            if ((rmask & (1u << k)) && MXQ_IN_BOUNDS(wp + k * p.ldc * 2, 16, p.c, p.c_bytes, &g_device_error))
                                 *reinterpret_cast<uint4 *>(wp + k * p.ldc * 2) =
                                     make_uint4(m[4 * k], m[4 * k + 1], m[4 * k + 2], m[4 * k + 3]);
                         return;
@@ -902,12 +911,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!row_ok) return;
                 if (col + 32 <= ti.col_hi) {
                     uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
+                    if (MXQ_IN_BOUNDS(dst, 64, p.c, p.c_bytes, &g_device_error)) {
 #pragma unroll
-                    for (int i = 0; i < 4; i++) dst[i] = make_uint4(m[4 * i], m[4 * i + 1], m[4 * i + 2], m[4 * i + 3]);
+                        for (int i = 0; i < 4; i++) dst[i] = make_uint4(m[4 * i], m[4 * i + 1], m[4 * i + 2], m[4 * i + 3]);
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; i++)
-                        if (col + i < ti.col_hi)
+                        if (col + i < ti.col_hi && MXQ_IN_BOUNDS(crow + col + i, 2, p.c, p.c_bytes, &g_device_error))
                             reinterpret_cast<uint16_t *>(crow)[col + i] = static_cast<uint16_t>(m[i >> 1] >> (16 * (i & 1)));
                 }
             };
@@ -1207,6 +1218,10 @@ cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
     p.bias = g.mode == kDense ? static_cast<const __nv_bfloat16 *>(g.bias) : nullptr;
     p.n_tiles = static_cast<int>((g.N + BN - 1) / BN);
     p.n_fastest = g.mode == kDense && g.a_rows > g.b_rows ? 1 : 0;
+    p.sa_bytes = g.kind == kBF16 ? 0 : static_cast<uint64_t>(scale_bytes_of(g.a_rows, g.a_k));
+    p.sb_bytes = g.kind == kBF16 ? 0 : static_cast<uint64_t>(scale_bytes_of(g.b_rows, g.b_k));
+    p.c_bytes = 2ull * static_cast<uint64_t>(g.mode == kGroupedK ? static_cast<int64_t>(g.E) * g.M : g.M) *
+                static_cast<uint64_t>(g.ldc);
     // bias (dense only) is a separate instance: a per-chunk test in the
     // epilogue measurably slows the launches that have none
     if (g.kind == kBF16) {

@@ -275,7 +275,12 @@ __device__ __forceinline__ uint2 mx4_as_e4m3_codes8(const uint32_t (&w)[4], cons
 template <typename InT, int FMT>
 __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__ x, int64_t R, int64_t C,
                                                          int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
-                                                         uint8_t *__restrict__ s, int64_t kb_tiles, float sf) {
+                                                         uint8_t *__restrict__ s, int64_t kb_tiles, float sf,
+                                                         unsigned int *err) {
+    // buffer extents in bytes (checked by debug builds)
+    const uint64_t x_bytes = static_cast<uint64_t>((R - 1) * ldx + C) * sizeof(InT);
+    const uint64_t q_bytes = static_cast<uint64_t>(R * ldq), s_bytes = static_cast<uint64_t>((R + 127) / 128 * kb_tiles * 512);
+    (void)x_bytes; (void)q_bytes; (void)s_bytes; (void)err;
     __shared__ __align__(16) uint8_t satom[512];
     const int tid = threadIdx.x, lane = tid & 31;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile, c0 = static_cast<int64_t>(blockIdx.x) * kTile;
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
         const int64_t gr = r0 + (id >> 4), gc = c0 + (id & 15) * 8;
 #pragma unroll
         for (int h = 0; h < kVec; h++) v[i][h] = make_uint4(0, 0, 0, 0);
-        if (gr < R && gc < C) {
+        if (gr < R && gc < C && MXQ_IN_BOUNDS(x + gr * ldx + gc, 8 * sizeof(InT), x, x_bytes, err)) {
             const InT *src = x + gr * ldx + gc;
             if (kVec == 2 && al32) {
                 ldg_nc_v8(src, v[i][0], v[i][kVec - 1]);
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
             a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
             const int X = mx8_exp_from_bf16(a);
             sbyte = mx8_scale_byte(X);
-            if (valid) {
+            if (valid && MXQ_IN_BOUNDS(q + gr * ldq + gc, 8, q, q_bytes, err)) {
                 const uint2 codes = e4m3_codes8(w4, X);
                 asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(q + gr * ldq + gc), "r"(codes.x), "r"(codes.y)
                              : "memory");
@@ -350,7 +355,7 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
                     const uint32_t nib = ((bits >> 28) & 8u) | idx;
                     packed |= nib << (4 * k);
                 }
-                if (valid) {
+                if (valid && MXQ_IN_BOUNDS(q + gr * ldq + gc / 2, 4, q, q_bytes, err)) {
                     asm volatile("st.global.u32 [%0], %1;" ::"l"(q + gr * ldq + gc / 2), "r"(packed) : "memory");
                 }
             } else {
@@ -365,7 +370,7 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
                     if (k < 4) lo |= code << (8 * k);
                     else hi |= code << (8 * (k - 4));
                 }
-                if (valid) {
+                if (valid && MXQ_IN_BOUNDS(q + gr * ldq + gc, 8, q, q_bytes, err)) {
                     asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(q + gr * ldq + gc), "r"(lo), "r"(hi)
                                  : "memory");
                 }
@@ -377,7 +382,8 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
     __syncthreads();
     if (tid < 32) {
         const uint4 v = *reinterpret_cast<const uint4 *>(satom + 16 * tid);
-        stg_v4(s + (static_cast<int64_t>(blockIdx.y) * kb_tiles + blockIdx.x) * 512 + 16 * tid, v);
+        uint8_t *dst = s + (static_cast<int64_t>(blockIdx.y) * kb_tiles + blockIdx.x) * 512 + 16 * tid;
+        if (MXQ_IN_BOUNDS(dst, 16, s, s_bytes, err)) stg_v4(dst, v);
     }
 }
 
@@ -403,8 +409,23 @@ struct ColParams {
     const int64_t *offsets;  // GROUPED: E+1 device offsets
     int E;
     float sf;                // MXFP4 scale factor (row pass in FMT 2)
-    unsigned int *err;       // GROUPED: device error word (malformed offsets)
+    unsigned int *err;       // device error word (malformed offsets; debug-build bounds checks)
 };
+
+// Extents in bytes of the buffers of a column (dual, grouped) quant, checked
+// by debug builds.
+struct ColExtents {
+    uint64_t x, q_row, s_row, qT, sT;
+};
+__device__ __forceinline__ ColExtents col_extents(const ColParams &P) {
+    ColExtents e;
+    e.x = P.R > 0 ? static_cast<uint64_t>((P.R - 1) * P.ldx + P.C) * 2 : 0;
+    e.q_row = static_cast<uint64_t>(P.R * P.C);
+    e.s_row = static_cast<uint64_t>((P.R + 127) / 128 * P.kb_row_tiles * 512);
+    e.qT = static_cast<uint64_t>(P.C * P.ldqT);
+    e.sT = static_cast<uint64_t>((P.C + 127) / 128 * P.kb_col_tiles * 512);
+    return e;
+}
 
 template <bool ROWS, bool GROUPED>
 __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
@@ -417,6 +438,8 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t rt = blockIdx.y, ct = blockIdx.x;
     const int64_t c0 = ct * kTile;
+    const ColExtents ext = col_extents(P);
+    (void)ext;
     int64_t src0 = rt * kTile;  // first source row of the tile
     int nvalid;                 // rows of the tile that hold data
     if (GROUPED) {
@@ -473,7 +496,8 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
         const int row = id >> 4;
         const int64_t gc = c0 + (id & 15) * 8;
         v[i] = make_uint4(0, 0, 0, 0);
-        if (row < nvalid && gc < P.C) v[i] = ldg_nc_v4(P.x + (src0 + row) * P.ldx + gc);
+        if (row < nvalid && gc < P.C && MXQ_IN_BOUNDS(P.x + (src0 + row) * P.ldx + gc, 16, P.x, ext.x, P.err))
+            v[i] = ldg_nc_v4(P.x + (src0 + row) * P.ldx + gc);
     }
 #pragma unroll
     for (int i = 0; i < 8; i++) {
@@ -487,7 +511,7 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
             a = max(a, __shfl_xor_sync(0xffffffffu, a, 1));
             a = max(a, __shfl_xor_sync(0xffffffffu, a, 2));
             const int X = mx8_exp_from_bf16(a);
-            if (valid) {
+            if (valid && MXQ_IN_BOUNDS(P.q_row + (src0 + row) * P.C + gc, 8, P.q_row, ext.q_row, P.err)) {
                 const uint2 codes = e4m3_codes8(w, X);
                 asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(P.q_row + (src0 + row) * P.C + gc),
                              "r"(codes.x), "r"(codes.y)
@@ -542,7 +566,9 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
             uint8_t *dlo = P.qT + gcol * P.ldqT + pos;
             uint8_t *dhi = dlo + P.ldqT;
             const int64_t limit = GROUPED ? P.ldqT : P.R;  // grouped tiles write padding zeros too
-            if (pos + 32 <= limit && (P.ldqT & 15) == 0) {
+            if (pos < limit && (!MXQ_IN_BOUNDS(dlo, limit - pos < 32 ? limit - pos : 32, P.qT, ext.qT, P.err) ||
+                                !MXQ_IN_BOUNDS(dhi, limit - pos < 32 ? limit - pos : 32, P.qT, ext.qT, P.err))) {
+            } else if (pos + 32 <= limit && (P.ldqT & 15) == 0) {
                 stg_v4(dlo, make_uint4(lo[0], lo[1], lo[2], lo[3]));
                 stg_v4(dlo + 16, make_uint4(lo[4], lo[5], lo[6], lo[7]));
                 stg_v4(dhi, make_uint4(hi[0], hi[1], hi[2], hi[3]));
@@ -561,11 +587,13 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
     __syncthreads();
     if (ROWS && tid < 32) {
         const uint4 v = *reinterpret_cast<const uint4 *>(srow_atom + 16 * tid);
-        stg_v4(P.s_row + (rt * P.kb_row_tiles + ct) * 512 + 16 * tid, v);
+        uint8_t *dst = P.s_row + (rt * P.kb_row_tiles + ct) * 512 + 16 * tid;
+        if (MXQ_IN_BOUNDS(dst, 16, P.s_row, ext.s_row, P.err)) stg_v4(dst, v);
     } else if (tid >= 32 && tid < 64) {
         const int l = tid - 32;
         const uint4 v = *reinterpret_cast<const uint4 *>(scol_atom + 16 * l);
-        stg_v4(P.sT + (ct * P.kb_col_tiles + rt) * 512 + 16 * l, v);
+        uint8_t *dst = P.sT + (ct * P.kb_col_tiles + rt) * 512 + 16 * l;
+        if (MXQ_IN_BOUNDS(dst, 16, P.sT, ext.sT, P.err)) stg_v4(dst, v);
     }
 }
 
@@ -670,6 +698,8 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t ring_s = smem_u32(ring), bar0 = smem_u32(&bars[0]);
+    const ColExtents ext = col_extents(P);
+    (void)ext;
     volatile int *abort_v = &abort_flag;
     if (tid == 0) {
         abort_flag = 0;
@@ -743,8 +773,8 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
         const int64_t npad = (P.R + 127) / 128 * 128 - P.R;
         for (int64_t i = tid; i < npad * P.kb_row_tiles; i += kThreads) {
             const int64_t r = P.R + i / P.kb_row_tiles, kt = i % P.kb_row_tiles;
-            *reinterpret_cast<uint32_t *>(P.s_row + ((r >> 7) * P.kb_row_tiles + kt) * 512 + 16 * (r & 31) +
-                                          4 * ((r >> 5) & 3)) = 0u;
+            uint8_t *dst = P.s_row + ((r >> 7) * P.kb_row_tiles + kt) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3);
+            if (MXQ_IN_BOUNDS(dst, 4, P.s_row, ext.s_row, err)) *reinterpret_cast<uint32_t *>(dst) = 0u;
         }
     }
 
@@ -821,7 +851,8 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
                         uint8_t *dst = P.q_row + (src0 + row) * P.C + gc;
                         const uint4 lo4 = make_uint4(cd[0].x, cd[0].y, cd[1].x, cd[1].y);
                         const uint4 hi4 = make_uint4(cd[2].x, cd[2].y, cd[3].x, cd[3].y);
-                        if (row_v8) {
+                        if (!MXQ_IN_BOUNDS(dst, 32, P.q_row, ext.q_row, err)) {
+                        } else if (row_v8) {
                             stg_v8(dst, lo4, hi4);
                         } else {
                             stg_v4(dst, lo4);
@@ -881,7 +912,9 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
                     uint8_t *dlo = P.qT + gcol * P.ldqT + pos;
                     uint8_t *dhi = dlo + P.ldqT;
                     const int64_t limit = GROUPED ? P.ldqT : P.R;  // grouped tiles write padding zeros too
-                    if (pos + 32 <= limit && col_v8) {
+                    if (pos < limit && (!MXQ_IN_BOUNDS(dlo, limit - pos < 32 ? limit - pos : 32, P.qT, ext.qT, err) ||
+                                        !MXQ_IN_BOUNDS(dhi, limit - pos < 32 ? limit - pos : 32, P.qT, ext.qT, err))) {
+                    } else if (pos + 32 <= limit && col_v8) {
                         stg_v8(dlo, make_uint4(lo[0], lo[1], lo[2], lo[3]), make_uint4(lo[4], lo[5], lo[6], lo[7]));
                         stg_v8(dhi, make_uint4(hi[0], hi[1], hi[2], hi[3]), make_uint4(hi[4], hi[5], hi[6], hi[7]));
                     } else if (pos + 32 <= limit && (P.ldqT & 15) == 0) {
@@ -911,16 +944,19 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
             // row's word goes to its own place, and only this tile's rows.
             const int row = tid - (kThreads - kTile);
             const int64_t r = src0 + row;
-            *reinterpret_cast<uint32_t *>(P.s_row + ((r >> 7) * P.kb_row_tiles + ct) * 512 + 16 * (r & 31) +
-                                          4 * ((r >> 5) & 3)) = *reinterpret_cast<const uint32_t *>(srow_atom + 4 * row);
+            uint8_t *dst = P.s_row + ((r >> 7) * P.kb_row_tiles + ct) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3);
+            if (MXQ_IN_BOUNDS(dst, 4, P.s_row, ext.s_row, err))
+                *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(srow_atom + 4 * row);
         }
         if (ROWS && !GROUPED && tid < 32) {
             const uint4 v = *reinterpret_cast<const uint4 *>(srow_atom + 16 * tid);
-            stg_v4(P.s_row + (rt * P.kb_row_tiles + ct) * 512 + 16 * tid, v);
+            uint8_t *dst = P.s_row + (rt * P.kb_row_tiles + ct) * 512 + 16 * tid;
+            if (MXQ_IN_BOUNDS(dst, 16, P.s_row, ext.s_row, err)) stg_v4(dst, v);
         } else if (COLS && tid >= 32 && tid < 64) {
             const int l = tid - 32;
             const uint4 v = *reinterpret_cast<const uint4 *>(scol_atom + 16 * l);
-            stg_v4(P.sT + (ct * P.kb_col_tiles + rt) * 512 + 16 * l, v);
+            uint8_t *dst = P.sT + (ct * P.kb_col_tiles + rt) * 512 + 16 * l;
+            if (MXQ_IN_BOUNDS(dst, 16, P.sT, ext.sT, err)) stg_v4(dst, v);
         }
     }
     // stopped early: let the loads still in flight (this tile's and the
@@ -954,8 +990,11 @@ constexpr int64_t kEwWindow = static_cast<int64_t>(kThreads) * kEwChunks;
 
 template <bool MASK>
 __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restrict__ x, float *y,
-                                                            uint32_t *__restrict__ mask, int64_t nchunks, float sf) {
+                                                            uint32_t *__restrict__ mask, int64_t nchunks, float sf,
+                                                            unsigned int *err) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t xy_bytes = static_cast<uint64_t>(nchunks) * 32, m_bytes = static_cast<uint64_t>(nchunks);  // extents
+    (void)xy_bytes; (void)m_bytes; (void)err;
     // one 32-byte access per chunk where both tensors are 32-byte aligned
     const bool al32 = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 31) == 0;
     for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kEwWindow; w0 < nchunks;
@@ -965,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restr
         for (int u = 0; u < kEwChunks; u++) {
             const int64_t g = w0 + u * kThreads + threadIdx.x;
             in[u][0] = in[u][1] = make_uint4(0, 0, 0, 0);
-            if (g < nchunks) {
+            if (g < nchunks && MXQ_IN_BOUNDS(x + 8 * g, 32, x, xy_bytes, err)) {
                 if (al32) {
                     ldg_nc_v8(x + 8 * g, in[u][0], in[u][1]);
                 } else {
@@ -1006,9 +1045,10 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restr
                 w |= __shfl_xor_sync(0xffffffffu, w, 1);
                 w |= __shfl_xor_sync(0xffffffffu, w, 2);
                 w = __shfl_sync(0xffffffffu, w, (4 * lane) & 31);
-                if (lane < 8 && wb + 4 * lane < nchunks) mask[wb / 4 + lane] = w;
+                if (lane < 8 && wb + 4 * lane < nchunks && MXQ_IN_BOUNDS(mask + wb / 4 + lane, 4, mask, m_bytes, err))
+                    mask[wb / 4 + lane] = w;
             }
-            if (g >= nchunks) continue;
+            if (g >= nchunks || !MXQ_IN_BOUNDS(y + 8 * g, 32, y, xy_bytes, err)) continue;
             const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]), o1 = make_uint4(o[4], o[5], o[6], o[7]);
             if (al32) {
                 stg_v8(y + 8 * g, o0, o1);
@@ -1023,7 +1063,9 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restr
 template <bool MASK>
 __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restrict__ x, float *y,
                                                             uint32_t *__restrict__ mask, int64_t rows, int64_t cols,
-                                                            float sf) {
+                                                            float sf, unsigned int *err) {
+    const uint64_t xy_bytes = static_cast<uint64_t>(rows * cols) * 4;  // extents (debug builds)
+    (void)xy_bytes; (void)err;
     const int lane = threadIdx.x & 31;
     const int64_t nb = (cols + 31) / 32;
     const int64_t nblocks = rows * nb;
@@ -1033,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restr
         const int64_t r = k / nb, b = k % nb;
         const int64_t c = 32 * b + lane;
         const bool valid = c < cols;
-        const uint32_t v = valid ? __float_as_uint(x[r * cols + c]) : 0u;
+        const uint32_t v = valid && MXQ_IN_BOUNDS(x + r * cols + c, 4, x, xy_bytes, err) ? __float_as_uint(x[r * cols + c]) : 0u;
         const uint32_t ax = v & 0x7FFFFFFFu;
         uint32_t a = ax;
 #pragma unroll
@@ -1049,9 +1091,9 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restr
         }
         if (MASK) {
             const uint32_t w = __ballot_sync(0xffffffffu, sat);
-            if (lane == 0) mask[k] = w;
+            if (lane == 0 && MXQ_IN_BOUNDS(mask + k, 4, mask, static_cast<uint64_t>(nblocks) * 4, err)) mask[k] = w;
         }
-        if (valid) y[r * cols + c] = __uint_as_float(out);
+        if (valid && MXQ_IN_BOUNDS(y + r * cols + c, 4, y, xy_bytes, err)) y[r * cols + c] = __uint_as_float(out);
     }
 }
 
@@ -1061,7 +1103,9 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restr
 // value x 2^e, or NaN for a non-finite block) is exact in bf16.
 constexpr int64_t kBlkWindow = static_cast<int64_t>(kThreads) * 2;
 __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_bf16(const uint16_t *__restrict__ x, uint16_t *y,
-                                                             int64_t nblocks, float sf) {
+                                                             int64_t nblocks, float sf, unsigned int *err) {
+    const uint64_t xy_bytes = static_cast<uint64_t>(nblocks) * 64;  // extent (debug builds)
+    (void)xy_bytes; (void)err;
     for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kBlkWindow; w0 < nblocks;
          w0 += static_cast<int64_t>(gridDim.x) * kBlkWindow) {
         uint4 in[2][4];
@@ -1069,12 +1113,14 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_bf16(const uint16_t *__r
         for (int u = 0; u < 2; u++) {
             const int64_t b = w0 + u * kThreads + threadIdx.x;
 #pragma unroll
-            for (int j = 0; j < 4; j++) in[u][j] = b < nblocks ? ldg_nc_v4(x + 32 * b + 8 * j) : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < 4; j++)
+                in[u][j] = b < nblocks && MXQ_IN_BOUNDS(x + 32 * b + 8 * j, 16, x, xy_bytes, err) ? ldg_nc_v4(x + 32 * b + 8 * j)
+                                                                                               : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < 2; u++) {
             const int64_t b = w0 + u * kThreads + threadIdx.x;
-            if (b >= nblocks) continue;
+            if (b >= nblocks || !MXQ_IN_BOUNDS(y + 32 * b, 64, y, xy_bytes, err)) continue;
             uint32_t w[16];
 #pragma unroll
             for (int j = 0; j < 4; j++) {
@@ -1114,17 +1160,24 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_bf16(const uint16_t *__r
 template <typename InT>
 __global__ void __launch_bounds__(kThreads) k_pack_mxfp4(const InT *__restrict__ x, int64_t ldx,
                                                          uint8_t *__restrict__ q, int64_t ldq,
-                                                         uint8_t *__restrict__ s, int64_t kb_tiles, float sf) {
+                                                         uint8_t *__restrict__ s, int64_t kb_tiles, float sf,
+                                                         unsigned int *err) {
+    // extents (debug builds): R = gridDim.y * 64 rows of C = gridDim.x * 128 columns
+    const int64_t R = static_cast<int64_t>(gridDim.y) * 64, C = static_cast<int64_t>(gridDim.x) * 128;
+    const uint64_t x_bytes = static_cast<uint64_t>((R - 1) * ldx + C) * sizeof(InT);
+    const uint64_t q_bytes = static_cast<uint64_t>(R * ldq), s_bytes = static_cast<uint64_t>(R / 128 * kb_tiles * 512);
+    (void)x_bytes; (void)q_bytes; (void)s_bytes; (void)err;
     constexpr int kWords = sizeof(InT) == 4 ? 32 : 16;  // 32-bit words of one block
     const int t = threadIdx.x, lane = t & 31, blk = t & 3;
     const int64_t r = static_cast<int64_t>(blockIdx.y) * 64 + (t >> 2);
     const int64_t c = static_cast<int64_t>(blockIdx.x) * 128 + 32 * blk;
     uint32_t w[kWords];
     const InT *src = x + r * ldx + c;
+    const bool src_ok = MXQ_IN_BOUNDS(src, 32 * sizeof(InT), x, x_bytes, err);
 #pragma unroll
     for (int j = 0; j < kWords / 8; j++) {
-        uint4 lo, hi;
-        ldg_nc_v8(reinterpret_cast<const uint32_t *>(src) + 8 * j, lo, hi);
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (src_ok) ldg_nc_v8(reinterpret_cast<const uint32_t *>(src) + 8 * j, lo, hi);
         w[8 * j] = lo.x; w[8 * j + 1] = lo.y; w[8 * j + 2] = lo.z; w[8 * j + 3] = lo.w;
         w[8 * j + 4] = hi.x; w[8 * j + 5] = hi.y; w[8 * j + 6] = hi.z; w[8 * j + 7] = hi.w;
     }
@@ -1163,14 +1216,14 @@ __global__ void __launch_bounds__(kThreads) k_pack_mxfp4(const InT *__restrict__
             nib[g] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
         }
     }
-    stg_v4(q + r * ldq + c / 2, make_uint4(nib[0], nib[1], nib[2], nib[3]));
+    if (MXQ_IN_BOUNDS(q + r * ldq + c / 2, 16, q, q_bytes, err))
+        stg_v4(q + r * ldq + c / 2, make_uint4(nib[0], nib[1], nib[2], nib[3]));
     // the row's 4 scale bytes, from lanes 4i .. 4i + 3
     uint32_t word = sbyte << (8 * blk);
     word |= __shfl_xor_sync(0xffffffffu, word, 1);
     word |= __shfl_xor_sync(0xffffffffu, word, 2);
-    if (blk == 0)
-        *reinterpret_cast<uint32_t *>(s + ((r >> 7) * kb_tiles + blockIdx.x) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3)) =
-            word;
+    uint8_t *sdst = s + ((r >> 7) * kb_tiles + blockIdx.x) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3);
+    if (blk == 0 && MXQ_IN_BOUNDS(sdst, 4, s, s_bytes, err)) *reinterpret_cast<uint32_t *>(sdst) = word;
     (void)lane;
 }
 
@@ -1180,7 +1233,9 @@ __global__ void __launch_bounds__(kThreads) k_pack_mxfp4(const InT *__restrict__
 // per thread before any store; general path: one warp per block.
 __global__ void __launch_bounds__(kThreads) k_ste_backward_vec(const float *__restrict__ gy,
                                                                const uint32_t *__restrict__ mask, float *gx,
-                                                               int64_t nchunks) {
+                                                               int64_t nchunks, unsigned int *err) {
+    const uint64_t g_bytes = static_cast<uint64_t>(nchunks) * 32, m_bytes = static_cast<uint64_t>(nchunks);  // extents
+    (void)g_bytes; (void)m_bytes; (void)err;
     const bool al32 = ((reinterpret_cast<uintptr_t>(gy) | reinterpret_cast<uintptr_t>(gx)) & 31) == 0;
     for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kEwWindow; w0 < nchunks;
          w0 += static_cast<int64_t>(gridDim.x) * kEwWindow) {
@@ -1191,7 +1246,8 @@ __global__ void __launch_bounds__(kThreads) k_ste_backward_vec(const float *__re
             const int64_t g = w0 + u * kThreads + threadIdx.x;
             in[u][0] = in[u][1] = make_uint4(0, 0, 0, 0);
             mw[u] = 0;
-            if (g < nchunks) {
+            if (g < nchunks && MXQ_IN_BOUNDS(gy + 8 * g, 32, gy, g_bytes, err) &&
+                MXQ_IN_BOUNDS(mask + g / 4, 4, mask, m_bytes, err)) {
                 mw[u] = __ldg(mask + g / 4);
                 if (al32) {
                     ldg_nc_v8(gy + 8 * g, in[u][0], in[u][1]);
@@ -1204,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads) k_ste_backward_vec(const float *__re
 #pragma unroll
         for (int u = 0; u < kEwChunks; u++) {
             const int64_t g = w0 + u * kThreads + threadIdx.x;
-            if (g >= nchunks) continue;
+            if (g >= nchunks || !MXQ_IN_BOUNDS(gx + 8 * g, 32, gx, g_bytes, err)) continue;
             const uint32_t bits = (mw[u] >> (8 * (g & 3))) & 0xFFu;
             uint4 a = in[u][0], b = in[u][1];
             if (bits) {
@@ -1225,7 +1281,9 @@ __global__ void __launch_bounds__(kThreads) k_ste_backward_vec(const float *__re
 
 __global__ void __launch_bounds__(kThreads) k_ste_backward_gen(const float *__restrict__ gy,
                                                                const uint32_t *__restrict__ mask, float *gx,
-                                                               int64_t rows, int64_t cols) {
+                                                               int64_t rows, int64_t cols, unsigned int *err) {
+    const uint64_t g_bytes = static_cast<uint64_t>(rows * cols) * 4;  // extent (debug builds)
+    (void)g_bytes; (void)err;
     const int lane = threadIdx.x & 31;
     const int64_t nb = (cols + 31) / 32;
     const int64_t nblocks = rows * nb;
@@ -1233,7 +1291,10 @@ __global__ void __launch_bounds__(kThreads) k_ste_backward_gen(const float *__re
     const int64_t wstride = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
     for (int64_t k = warp0; k < nblocks; k += wstride) {
         const int64_t r = k / nb, c = 32 * (k % nb) + lane;
-        if (c >= cols) continue;
+        if (c >= cols || !MXQ_IN_BOUNDS(gx + r * cols + c, 4, gx, g_bytes, err) ||
+            !MXQ_IN_BOUNDS(gy + r * cols + c, 4, gy, g_bytes, err) ||
+            !MXQ_IN_BOUNDS(mask + k, 4, mask, static_cast<uint64_t>(nblocks) * 4, err))
+            continue;
         const bool sat = (__ldg(mask + k) >> lane) & 1u;
         gx[r * cols + c] = sat ? 0.0f : gy[r * cols + c];
     }
@@ -1266,6 +1327,9 @@ bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cud
 
 cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, int64_t C, int64_t ldx, uint8_t *q,
                               uint8_t *s, cudaStream_t st, float sf) {
+    unsigned int *err = nullptr;
+    cudaError_t ee = device_error_word(&err);
+    if (ee != cudaSuccess) return ee;
     const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>((R + kTile - 1) / kTile));
     const int64_t kb_tiles = ((C / 32) + 3) / 4;
     const uint16_t *xb = static_cast<const uint16_t *>(x);
@@ -1275,6 +1339,7 @@ cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, i
         P.x = xb; P.R = R; P.C = C; P.ldx = ldx;
         P.q_row = q; P.s_row = s; P.kb_row_tiles = kb_tiles;
         P.sf = sf;
+        P.err = err;
         const int64_t row_tiles = (R + kTile - 1) / kTile;
         cudaError_t res = cudaSuccess;
         if (fmt == 0 ? launch_cols_tma<true, false, false, 0>(P, row_tiles, st, &res)
@@ -1282,22 +1347,23 @@ cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, i
             return res;
     }
     if (fmt == 0) {
-        k_quant_rows<uint16_t, 0><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf);
+        k_quant_rows<uint16_t, 0><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf, err);
     } else if (fmt == 2) {
-        k_quant_rows<uint16_t, 2><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf);
+        k_quant_rows<uint16_t, 2><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf, err);
     } else if (R % kTile == 0 && C % kTile == 0 &&
                ((reinterpret_cast<uintptr_t>(x) | static_cast<uintptr_t>(ldx * (fp32_in ? 4 : 2))) & 31) == 0) {
         // whole scale tiles: 64 x 128 blocks
         const dim3 g2(static_cast<unsigned>(C / kTile), static_cast<unsigned>(R / 64));
         if (fp32_in)
-            k_pack_mxfp4<float><<<g2, kThreads, 0, st>>>(static_cast<const float *>(x), ldx, q, C / 2, s, kb_tiles, sf);
+            k_pack_mxfp4<float><<<g2, kThreads, 0, st>>>(static_cast<const float *>(x), ldx, q, C / 2, s, kb_tiles, sf,
+                                                          err);
         else
-            k_pack_mxfp4<uint16_t><<<g2, kThreads, 0, st>>>(xb, ldx, q, C / 2, s, kb_tiles, sf);
+            k_pack_mxfp4<uint16_t><<<g2, kThreads, 0, st>>>(xb, ldx, q, C / 2, s, kb_tiles, sf, err);
     } else if (fp32_in) {
         k_quant_rows<float, 1><<<grid, kThreads, 0, st>>>(static_cast<const float *>(x), R, C, ldx, q, C / 2, s,
-                                                          kb_tiles, sf);
+                                                          kb_tiles, sf, err);
     } else {
-        k_quant_rows<uint16_t, 1><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C / 2, s, kb_tiles, sf);
+        k_quant_rows<uint16_t, 1><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C / 2, s, kb_tiles, sf, err);
     }
     return cudaGetLastError();
 }
@@ -1357,7 +1423,8 @@ cudaError_t launch_quant_cols(const uint16_t *x, int64_t R, int64_t C, int64_t l
     P.q_row = q_row; P.s_row = s_row; P.kb_row_tiles = ((C / 32) + 3) / 4;
     P.qT = qT; P.sT = sT; P.ldqT = R; P.kb_col_tiles = (((R + 31) / 32) + 3) / 4;
     const int64_t row_tiles = (R + kTile - 1) / kTile;
-    cudaError_t res = cudaSuccess;
+    cudaError_t res = device_error_word(&P.err);
+    if (res != cudaSuccess) return res;
     if (q_row ? launch_cols_tma<true, false>(P, row_tiles, st, &res) : launch_cols_tma<false, false>(P, row_tiles, st, &res))
         return res;
     const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>(row_tiles));
@@ -1390,37 +1457,46 @@ cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, c
 
 cudaError_t launch_qdq_mxfp4(const float *x, float *y, uint32_t *mask, int64_t rows, int64_t cols, float sf,
                              cudaStream_t st) {
+    unsigned int *err = nullptr;
+    cudaError_t ee = device_error_word(&err);
+    if (ee != cudaSuccess) return ee;
     const bool vec = (cols % 32 == 0) && ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15) == 0;
     if (vec) {
         const int64_t nchunks = rows * cols / 8;
         const int grid = grid_windows(nchunks);
-        if (mask) k_qdq_mxfp4_vec<true><<<grid, kThreads, 0, st>>>(x, y, mask, nchunks, sf);
-        else k_qdq_mxfp4_vec<false><<<grid, kThreads, 0, st>>>(x, y, nullptr, nchunks, sf);
+        if (mask) k_qdq_mxfp4_vec<true><<<grid, kThreads, 0, st>>>(x, y, mask, nchunks, sf, err);
+        else k_qdq_mxfp4_vec<false><<<grid, kThreads, 0, st>>>(x, y, nullptr, nchunks, sf, err);
     } else {
         const int64_t nblocks = rows * ((cols + 31) / 32);
         const int grid = grid_for(nblocks, kThreads / 32);
-        if (mask) k_qdq_mxfp4_gen<true><<<grid, kThreads, 0, st>>>(x, y, mask, rows, cols, sf);
-        else k_qdq_mxfp4_gen<false><<<grid, kThreads, 0, st>>>(x, y, nullptr, rows, cols, sf);
+        if (mask) k_qdq_mxfp4_gen<true><<<grid, kThreads, 0, st>>>(x, y, mask, rows, cols, sf, err);
+        else k_qdq_mxfp4_gen<false><<<grid, kThreads, 0, st>>>(x, y, nullptr, rows, cols, sf, err);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_qdq_mxfp4_bf16(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols, float sf,
                                   cudaStream_t st) {
+    unsigned int *err = nullptr;
+    cudaError_t ee = device_error_word(&err);
+    if (ee != cudaSuccess) return ee;
     const int64_t nblocks = rows * cols / 32;
-    k_qdq_mxfp4_bf16<<<grid_windows(nblocks, kBlkWindow), kThreads, 0, st>>>(x, y, nblocks, sf);
+    k_qdq_mxfp4_bf16<<<grid_windows(nblocks, kBlkWindow), kThreads, 0, st>>>(x, y, nblocks, sf, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_ste_backward(const float *gy, const uint32_t *mask, float *gx, int64_t rows, int64_t cols,
                                 cudaStream_t st) {
+    unsigned int *err = nullptr;
+    cudaError_t ee = device_error_word(&err);
+    if (ee != cudaSuccess) return ee;
     const bool vec = (cols % 32 == 0) && ((reinterpret_cast<uintptr_t>(gy) | reinterpret_cast<uintptr_t>(gx)) & 15) == 0;
     if (vec) {
         const int64_t nchunks = rows * cols / 8;
-        k_ste_backward_vec<<<grid_windows(nchunks), kThreads, 0, st>>>(gy, mask, gx, nchunks);
+        k_ste_backward_vec<<<grid_windows(nchunks), kThreads, 0, st>>>(gy, mask, gx, nchunks, err);
     } else {
         const int64_t nblocks = rows * ((cols + 31) / 32);
-        k_ste_backward_gen<<<grid_for(nblocks, kThreads / 32), kThreads, 0, st>>>(gy, mask, gx, rows, cols);
+        k_ste_backward_gen<<<grid_for(nblocks, kThreads / 32), kThreads, 0, st>>>(gy, mask, gx, rows, cols, err);
     }
     return cudaGetLastError();
 }

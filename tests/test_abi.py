@@ -150,3 +150,21 @@ def test_group_offsets_validated_on_the_host(lib):
     assert _status(m.mxq_check_group_offsets, None, 4, 300, 0) == INV
     assert _status(m.mxq_check_group_offsets, FAKE + 4, 4, 300, 0) == INV
     assert _status(m.mxq_check_group_offsets, FAKE, 0, 300, 0) == INV
+
+
+def test_debug_build_exports_every_symbol_and_loads_under_the_switch():
+    """libmxq_debug.so (MXQ_DEBUG: bounds checks on every computed global
+    access) builds, exports the same entry points, and is what the binding
+    loads when MXQ_LIBRARY=debug."""
+    import subprocess
+    import sys
+    from mx_block_scaled_mxq_gb300 import build as b
+    path = b.build(debug=True)
+    raw = ctypes.CDLL(path)
+    for n in _declared():
+        assert hasattr(raw, n), n
+    env = dict(os.environ, MXQ_LIBRARY="debug")
+    code = "import mx_block_scaled_mxq_gb300 as m; m.load(); import os; print(os.path.basename(m.library_path()))"
+    res = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    assert res.stdout.strip().endswith("libmxq_debug.so")
