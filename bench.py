@@ -49,11 +49,11 @@ PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f in ("mxq_gemm.cu", "mxq_device.cuh")]
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the GEMM
 # kernel for each launch the timed region brackets, from one ncu capture of the
-# full-size launches (profiles/k_gemm__bench_launches_dram.md), keyed by a
-# hash of the kernel source; when the source has changed since, traffic is null.
+# same full-size launches in the parity tests, keyed by a hash of the kernel
+# source; when the source has changed since, traffic is null.
 GEMM_DRAM_TRAFFIC = {
-    "320d26573fb1d5aa": {"linear_dw_gemm": 287821568, "moe_fwd_gemm": 1499957504,
-                         "moe_dx_gemm": 1531104768, "moe_dw_gemm": 2236594688},
+    "19f7fc9a28ec5004": {"linear_dw_gemm": 260626176, "moe_fwd_gemm": 1499859456,
+                         "moe_dx_gemm": 1534428672, "moe_dw_gemm": 2236278016},
 }
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
@@ -569,11 +569,16 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--quant-sweep", action="store_true",
                     help="instead of the step: dual-axis MXFP8 quant bandwidth over sizes (one JSON line each)")
+    ap.add_argument("--ncu-case", choices=["mxfp4", "dense", "moe_small"],
+                    help="instead of the step: run one small profiling case once (for ncu captures) and exit")
     args = ap.parse_args()
     world, rank, local = dist_init()
 
     if args.quant_sweep:
         quant_sweep()
+        return
+    if args.ncu_case:
+        ncu_case(args.ncu_case)
         return
     if args.impl == "reference":
         run_reference(args, world, rank)
@@ -647,7 +652,7 @@ def main():
                    "l2": "inputs larger than L2 (step touches > 8 GB); kernels alone rotate buffer sets > 2x L2",
                    "step_gemm_flop": STEP_FLOP},
         "roofline": {"bound": "tensor",
-                     "kernel": "k_gemm<1,MXF8,0> (tcgen05 kind::mxf8f6f4.block_scale, 128x256 tiles)",
+                     "kernel": "k_gemm<1,MXF8,0> (tcgen05 kind::mxf8f6f4.block_scale, 128x256 tiles, 8 epilogue warps)",
                      "achieved": round(achieved, 1) if achieved else None,
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / fp8_peak, 4) if achieved else None,
@@ -674,6 +679,64 @@ def main():
         line["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def ncu_case(case: str):
+    """One launch of each kernel of a small case, for profiler captures that
+    must end quickly (a few hundred MB on the device, no timing loop):
+      mxfp4      QDQ, clipped-STE forward and backward, packed quant of the
+                 4096 x 4096 fp32 tensor, then the W4A4 QAT forward
+                 (8192 x 14336 x 4096: its two operand quants and the GEMM) and
+                 the bf16 QDQ of its 14336 x 4096 weight;
+      dense      row quants and one forward GEMM, 8192 x 14336 x 4096;
+      moe_small  the MoE layer's GEMMs (fwd, dX, dW) at E=8, T=8192, K=7168,
+                 N=4096 (the bench's 1024 routed rows per expert on average)."""
+    import mxq_inputs
+    import mx_block_scaled_mxq_gb300 as m
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    m.load()
+    bf = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=dev)  # noqa: E731
+    u8 = lambda n: torch.empty(max(int(n), 1), dtype=torch.uint8, device=dev)  # noqa: E731
+    if case == "mxfp4":
+        R, C = FP4["R"], FP4["C"]
+        a4 = torch.from_numpy(mxq_inputs.mxfp4_large(R, C, seed=0)).to(dev)
+        y4, g4 = torch.empty_like(a4), torch.empty_like(a4)
+        mk = torch.empty((R, C // 32), dtype=torch.int32, device=dev)
+        m.mxq_qdq_mxfp4(a4, y4, R, C, 32, 6.0)
+        m.mxq_mxfp4_ste_forward(a4, y4, mk, R, C, 32, 6.0)
+        m.mxq_mxfp4_ste_backward(y4, mk, R, C, g4)
+        m.mxq_quantize(a4, m.F32, R, C, C, -1, m.E2M1, 0, u8(R * C // 2), u8(m.mxq_scale_bytes(R, C // 32)), None, None)
+        M, N, K = LIN["M"], LIN["N"], LIN["K"]
+        x, w, _ = mxq_inputs.linear_inputs(M, N, K, seed=0)
+        x, w = x.to(dev), w.to(dev)
+        wsb = m.mxq_qat_linear_workspace_bytes(M, N, K, 1)
+        m.mxq_qat_linear_fwd(x, w, None, M, N, K, 1, 6.0, bf(M, N), u8(wsb), wsb)
+        m.mxq_qdq_mxfp4_bf16(w, bf(N, K), N, K, 32, 6.0)
+    elif case == "dense":
+        M, N, K = LIN["M"], LIN["N"], LIN["K"]
+        x, w, _ = mxq_inputs.linear_inputs(M, N, K, seed=0)
+        xq, xs = m.quantize_mxfp8(x.to(dev))[:2]
+        wq, ws = m.quantize_mxfp8(w.to(dev))[:2]
+        m.mxq_gemm(xq, xs, wq, ws, M, N, K, bf(M, N), N)
+    else:
+        E, T, K, N = 8, 8192, MOE["K"], MOE["N"]
+        off, xm, wm, dym = mxq_inputs.moe_inputs(E, T, K, N, seed=0)
+        d_off = torch.from_numpy(off).to(dev)
+        tp = m.mxq_grouped_padded_rows(T, E)
+        xmd, dymd = xm.to(dev), dym.to(dev)
+        xq, xs = m.quantize_mxfp8(xmd)[:2]
+        wq, ws, wqT, wsT = m.quantize_mxfp8(wm.reshape(E * N, K).to(dev), dual=True)
+        dq, ds = m.quantize_mxfp8(dymd)[:2]
+        dqT, dsT, xqT, xsT = u8(N * tp), u8(m.mxq_scale_bytes(N, tp // 32)), u8(K * tp), u8(m.mxq_scale_bytes(K, tp // 32))
+        m.mxq_quantize_grouped_col(dymd, T, N, d_off, E, tp, dqT, dsT)
+        m.mxq_quantize_grouped_col(xmd, T, K, d_off, E, tp, xqT, xsT)
+        m.mxq_grouped_gemm(m.GG_FWD, xq, xs, wq, ws, d_off, E, T, N, K, 0, bf(T, N))
+        m.mxq_grouped_gemm(m.GG_DX, dq, ds, wqT, wsT, d_off, E, T, N, K, 0, bf(T, K))
+        m.mxq_grouped_gemm(m.GG_DW, dqT, dsT, xqT, xsT, d_off, E, T, N, K, tp, bf(E, N, K))
+    torch.cuda.synchronize()
+    assert m.mxq_poll_device_error() == 0
+    print(json.dumps({"ncu_case": case, "ok": True}), flush=True)
 
 
 def quant_sweep():
