@@ -342,12 +342,31 @@ def time_rotating(fns, reps=8, warm=2):
     """Mean device time (ms) of one call, over back-to-back calls that cycle
     through `fns` -- each on its own buffers, together larger than L2, so no
     call finds its inputs cached and every call pays the write-back of its
-    predecessor's output, as inside a running step.  Each call is bracketed by
-    its own CUDA events on the launching stream, so host launch overhead
-    between calls does not count."""
+    predecessor's output, as inside a running step.  The calls are captured
+    once in a CUDA graph and replayed, so the host's launch overhead between
+    short kernels does not count; if capture is refused, each call is
+    bracketed by its own events instead."""
     n = len(fns)
     for i in range(warm * n):
         fns[i % n]()
+    torch.cuda.synchronize()
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(reps * n):
+                fns[i % n]()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / (reps * n)
+        del g
+        return ms
+    except RuntimeError:
+        torch.cuda.synchronize()
     pairs = []
     for i in range(reps * n):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -193,17 +193,13 @@ __device__ __forceinline__ float mx4_scaled(uint32_t xb, uint32_t t025, float in
     const bool tie = (xb & 0x7FFFFFu) == 0x200000u || (xb & 0x7FFFFFFFu) == t025;
     return __uint_as_float(xb + (tie ? 1u : 0u)) * inv_s;
 }
-// Two bf16 at once, one per 16-bit half of w: each moved one bf16 ulp up in
-// magnitude where it sits on such a midpoint (mantissa pattern 1.25, or equal
-// to s/4, whose bf16 bits are t025x2 in both halves); one bf16 ulp moves no
-// value across a midpoint either.  A half h <= 0x7FFF is zero exactly when
-// h + 0x7FFF leaves bit 15 clear (no carry reaches the other half).
-__device__ __forceinline__ uint32_t mx4_untie2(uint32_t w, uint32_t t025x2) {
-    const uint32_t m = (w & 0x007F007Fu) ^ 0x00200020u;  // zero half: mantissa pattern 1.25
-    const uint32_t q = (w & 0x7FFF7FFFu) ^ t025x2;       // zero half: |x| = s/4
-    const uint32_t z = ~((m + 0x7FFF7FFFu) & (q + 0x7FFF7FFFu)) & 0x80008000u;
-    return w + (z >> 15);
-}
+// For bf16 inputs no tie fix-up is needed: a bf16 value has 8 significant
+// bits, so |x| * 2^-e * (1 + 2^-9) is exact in fp32 and lies strictly above y
+// exactly when y is a midpoint, and it never reaches the next midpoint from a
+// bf16 value below one (those are at least m * 2^-8 under the midpoint m, the
+// nudge is at most m * 2^-9).  One multiply per element takes the place of
+// mx4_untie2; the factor is exact too (a power of two times 1 + 2^-9).
+constexpr float kBf16Nudge = 1.001953125f;  // 1 + 2^-9
 // 2^-e for a block exponent e in [-30, 127] (2^-127 is a subnormal).
 __device__ __forceinline__ float mx4_inv_scale(int e) {
     return __uint_as_float(e <= 126 ? static_cast<uint32_t>(127 - e) << 23 : 0x00400000u);
@@ -230,18 +226,6 @@ __device__ __forceinline__ uint32_t e2m1_qdq_bf16x2(float lo, float hi, float s)
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f1 * s), "f"(f0 * s));
     return r;
 }
-// E4M3 codes (low byte: lo) of the E2M1 values of two scaled values lo, hi
-// (every E2M1 value is an E4M3 value: both decodings are exact).
-__device__ __forceinline__ uint32_t e2m1_as_e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("{\n\t.reg .b8 b;\n\t.reg .b32 h;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 h, b;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f16x2 %0, h;\n\t}"
-        : "=h"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
 // ============================================================================
 // Row quant: 128 x 128 tile per CTA, blocks along cols (cols % 32 == 0).
 //   FMT 0: bf16 -> E4M3 codes [R x C] (MXFP8)
@@ -256,20 +240,22 @@ __device__ __forceinline__ uint32_t e2m1_as_e4m3x2(float lo, float hi) {
 // low half of word k) under block B: sign | the E4M3 code of the E2M1 value;
 // the NaN code 0x7F | sign for a non-finite block.
 __device__ __forceinline__ uint2 mx4_as_e4m3_codes8(const uint32_t (&w)[4], const Mx4Blk &B, bool nonfinite) {
-    uint32_t c[4];
-    if (nonfinite) {
+    // the signs: bit 7 of byte k <- bit 15 of element k's bf16
+    const uint32_t sg0 = __byte_perm(w[0], w[1], 0x7531) & 0x80808080u;
+    const uint32_t sg1 = __byte_perm(w[2], w[3], 0x7531) & 0x80808080u;
+    if (nonfinite) return make_uint2(0x7F7F7F7Fu | sg0, 0x7F7F7F7Fu | sg1);
+    const float f = mx4_inv_scale(B.e) * kBf16Nudge;
+    uint32_t nb[4];  // E2M1 indices (no sign) of elements 2k, 2k + 1 in the low byte
 #pragma unroll
-        for (int k = 0; k < 4; k++) c[k] = 0x007F007Fu | ((w[k] >> 8) & 0x00800080u);
-    } else {
-        const float inv = mx4_inv_scale(B.e);
-        const uint32_t t2 = (B.t025 >> 16) * 0x10001u;
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const uint32_t u = mx4_untie2(w[k], t2);
-            c[k] = e2m1_as_e4m3x2(__uint_as_float(u << 16) * inv, __uint_as_float(u & 0xFFFF0000u) * inv);
-        }
-    }
-    return make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
+    for (int k = 0; k < 4; k++)
+        nb[k] = cvt_e2m1x2(__uint_as_float((w[k] & 0x7FFFu) << 16) * f, __uint_as_float(w[k] & 0x7FFF0000u) * f);
+    // E4M3 code of E2M1 index i (value 0, .5, 1, 1.5, 2, 3, 4, 6): byte i of
+    // the 8-byte table {kLo, kHi}, picked by a byte permute whose selector
+    // nibbles are the indices
+    constexpr uint32_t kLo = 0x3C383000u, kHi = 0x4C484440u;
+    const uint32_t c0 = __byte_perm(kLo, kHi, (nb[0] | (nb[1] << 8)) & 0x7777u);
+    const uint32_t c1 = __byte_perm(kLo, kHi, (nb[2] | (nb[3] << 8)) & 0x7777u);
+    return make_uint2(c0 | sg0, c1 | sg1);
 }
 
 template <typename InT, int FMT>
@@ -1136,13 +1122,10 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_bf16(const uint16_t *__r
                 for (int k = 0; k < 16; k++) o[k] = 0x7FC07FC0u;
             } else {
                 const int e = mx4_exp(__uint_as_float(a), sf);
-                const float inv = mx4_inv_scale(e), sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-                const uint32_t t2 = static_cast<uint32_t>(e + 125) * 0x800080u;  // s/4 as bf16, both halves
+                const float f = mx4_inv_scale(e) * kBf16Nudge, sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 #pragma unroll
-                for (int k = 0; k < 16; k++) {
-                    const uint32_t v = mx4_untie2(w[k], t2);
-                    o[k] = e2m1_qdq_bf16x2(__uint_as_float(v << 16) * inv, __uint_as_float(v & 0xFFFF0000u) * inv, sc);
-                }
+                for (int k = 0; k < 16; k++)
+                    o[k] = e2m1_qdq_bf16x2(__uint_as_float(w[k] << 16) * f, __uint_as_float(w[k] & 0xFFFF0000u) * f, sc);
             }
 #pragma unroll
             for (int j = 0; j < 4; j++) stg_v4(y + 32 * b + 8 * j, make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]));
@@ -1210,9 +1193,16 @@ __global__ void __launch_bounds__(kThreads) k_pack_mxfp4(const InT *__restrict__
             nib[g] = p;
         } else {
             uint32_t b[4];
+            if (sizeof(InT) == 2) {  // bf16: the one-multiply nudge
+                const float f = inv * kBf16Nudge;
 #pragma unroll
-            for (int k = 0; k < 4; k++)
-                b[k] = cvt_e2m1x2(mx4_scaled(v[2 * k], t025, inv), mx4_scaled(v[2 * k + 1], t025, inv));
+                for (int k = 0; k < 4; k++)
+                    b[k] = cvt_e2m1x2(__uint_as_float(v[2 * k]) * f, __uint_as_float(v[2 * k + 1]) * f);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    b[k] = cvt_e2m1x2(mx4_scaled(v[2 * k], t025, inv), mx4_scaled(v[2 * k + 1], t025, inv));
+            }
             nib[g] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
         }
     }
