@@ -189,6 +189,53 @@ def test_full_size_linear_operands_dual_quant(mxq):
         del q, s, qT, sT
 
 
+def _sweep_rows(C, p):
+    """The bandwidth sweep's row count for 2^p elements of width C."""
+    return ((1 << p) // C + 127) // 128 * 128
+
+
+@pytest.mark.parametrize("C", [2048, 7168, 14336])
+@pytest.mark.parametrize("p", [22, 24])
+def test_sweep_shapes_dual_quant_bit_exact(mxq, C, p):
+    """The dual-quant sweep's shapes up to 2^24 elements, heavy-tailed with
+    1000x outliers: all four outputs in full against the oracle."""
+    x = mxq_inputs.sweep_bf16(_sweep_rows(C, p), C, seed=p * C)
+    q, s, qT, sT = mxq.quantize_mxfp8(x.to(DEV), dual=True)
+    oq, os_ = oracle.mxfp8_quant_rows(x)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(s.cpu().numpy(), oracle.swizzle_scales(os_))
+    oqT, osT = oracle.mxfp8_quant_cols(x)
+    assert np.array_equal(qT.cpu().numpy(), oqT)
+    assert np.array_equal(sT.cpu().numpy(), oracle.swizzle_scales(osT))
+
+
+@pytest.mark.parametrize("C", [2048, 7168, 14336])
+def test_sweep_largest_size_dual_quant_sampled(mxq, C):
+    """The sweep's largest size, 2^30 elements drawn on the device as the
+    sweep draws them: three 128-row slabs of the row outputs and two
+    128-column slabs of the column outputs (every block of those columns)
+    against the oracle, scale tiles included (a slab of 128 rows or columns
+    starting at a multiple of 128 is one row of 512-byte scale tiles)."""
+    R = _sweep_rows(C, 30)
+    x = mxq_inputs.sweep_bf16_device(R, C, seed=C, device=DEV)
+    q, s, qT, sT = mxq.quantize_mxfp8(x, dual=True)
+    torch.cuda.synchronize()
+    kp = (C // 32 + 3) // 4 * 4                    # row-scale tile columns x 4
+    for r0 in (0, (R // 256) * 128, R - 128):
+        xs = x[r0:r0 + 128].cpu()
+        oq, os_ = oracle.mxfp8_quant_rows(xs)
+        assert np.array_equal(q[r0:r0 + 128].cpu().numpy(), oq), r0
+        tiles = s[r0 * kp:(r0 + 128) * kp].cpu().numpy()
+        assert np.array_equal(tiles, oracle.swizzle_scales(os_)), r0
+    kpT = (R // 32 + 3) // 4 * 4
+    for c0 in (0, C - 128):
+        xs = x[:, c0:c0 + 128].contiguous().cpu()
+        oqT, osT = oracle.mxfp8_quant_cols(xs)
+        assert np.array_equal(qT[c0:c0 + 128].cpu().numpy(), oqT), c0
+        tiles = sT[c0 * kpT:(c0 + 128) * kpT].cpu().numpy()
+        assert np.array_equal(tiles, oracle.swizzle_scales(osT)), c0
+
+
 @pytest.mark.parametrize("R,C,pad,shift", [(256, 64, 8, 0), (130, 96, 16, 8), (64, 128, 8, 24)])
 def test_dual_quant_strided_views(mxq, R, C, pad, shift):
     """A row stride larger than the row (ldx = C + pad + shift elements) and a
