@@ -588,7 +588,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--quant-sweep", action="store_true",
                     help="instead of the step: dual-axis MXFP8 quant bandwidth over sizes (one JSON line each)")
-    ap.add_argument("--ncu-case", choices=["mxfp4", "dense", "moe_small"],
+    ap.add_argument("--ncu-case", choices=["mxfp4", "dense", "moe_small", "dualquant"],
                     help="instead of the step: run one small profiling case once (for ncu captures) and exit")
     args = ap.parse_args()
     world, rank, local = dist_init()
@@ -709,7 +709,10 @@ def ncu_case(case: str):
                  the bf16 QDQ of its 14336 x 4096 weight;
       dense      row quants and one forward GEMM, 8192 x 14336 x 4096;
       moe_small  the MoE layer's GEMMs (fwd, dX, dW) at E=8, T=8192, K=7168,
-                 N=4096 (the bench's 1024 routed rows per expert on average)."""
+                 N=4096 (the bench's 1024 routed rows per expert on average);
+      dualquant  the dual quant of the dense layer's dY (8192 x 14336) and the
+                 per-group dual quant of the MoE layer's dY (32768 x 4096, 32
+                 Dirichlet(0.5) groups)."""
     import mxq_inputs
     import mx_block_scaled_mxq_gb300 as m
     dev = torch.device("cuda", 0)
@@ -732,6 +735,17 @@ def ncu_case(case: str):
         wsb = m.mxq_qat_linear_workspace_bytes(M, N, K, 1)
         m.mxq_qat_linear_fwd(x, w, None, M, N, K, 1, 6.0, bf(M, N), u8(wsb), wsb)
         m.mxq_qdq_mxfp4_bf16(w, bf(N, K), N, K, 32, 6.0)
+    elif case == "dualquant":
+        M, N, K = LIN["M"], LIN["N"], LIN["K"]
+        _, _, dy = mxq_inputs.linear_inputs(M, N, K, seed=0)
+        m.quantize_mxfp8(dy.to(dev), dual=True)
+        E, T, Nm = MOE["E"], MOE["T"], MOE["N"]
+        off = mxq_inputs.offsets_from_sizes(mxq_inputs.dirichlet_group_sizes(E, T, seed=0))
+        off_d = torch.from_numpy(np.asarray(off, dtype=np.int64)).to(dev)
+        dym = mxq_inputs.normal_bf16((T, Nm), 1e-3, seed=5).to(dev)
+        tp = m.mxq_grouped_padded_rows(T, E)
+        m.mxq_quantize_grouped_dual(dym, T, Nm, off_d, E, tp, u8(T * Nm), u8(m.mxq_scale_bytes(T, Nm // 32)),
+                                    u8(Nm * tp), u8(m.mxq_scale_bytes(Nm, tp // 32)))
     elif case == "dense":
         M, N, K = LIN["M"], LIN["N"], LIN["K"]
         x, w, _ = mxq_inputs.linear_inputs(M, N, K, seed=0)

@@ -1039,9 +1039,10 @@ bool make_out_tmap(CUtensorMap *m, void *base, int64_t rows, int64_t n, int64_t 
 int64_t scale_bytes_of(int64_t rows, int64_t k) { return (rows + 127) / 128 * 128 * ((k / 32 + 3) / 4 * 4); }
 
 // CTAs per tile.  Single-CTA tiles are the default: on GB300 the pair tile
-// moves a third less operand data per SM but measured slower (1440 vs 1493
-// TFLOP/s over the bench step), because the kernel is bound by the issue
-// chain of its single MMA thread, not by operand delivery.
+// moves a third less operand data per SM and, without its scale copies, runs
+// the dense 8192 x 14336 x 4096 product in 305 us against 325 us, but each
+// tcgen05.cp.cta_group::2 costs about 50 clocks of MMA issue while MMAs are in
+// flight, and its three copies per k-block bring it to 363 us.
 // MXQ_GEMM_CTA_GROUP=2 selects pair tiles (read once per process).
 int cta_group_for(const GemmProblem &) {
     static int forced = [] {
