@@ -173,10 +173,13 @@ class Workload:
         self.off_padded_total = int(((n_e + 127) // 128 * 128).sum())  # sum of the groups' padded lengths
         self.xm, self.wm, self.dym = xm.to(dev), wm.reshape(E * Nm, Km).to(dev), dym.to(dev)
         self.t_pad = m.mxq_grouped_padded_rows(T, E)
-        self.xmq, self.xms = u8(T * Km), u8(m.mxq_scale_bytes(T, Km // 32))
+        # row quants of X and dY with per-group padded row scales (each expert's
+        # rows start a scale tile, so the forward and dX tile each expert from its
+        # first row)
+        self.xmq, self.xms = u8(T * Km), u8(m.mxq_scale_bytes(self.t_pad, Km // 32))
         self.wmq, self.wms = u8(E * Nm * Km), u8(m.mxq_scale_bytes(E * Nm, Km // 32))
         self.wmqT, self.wmsT = u8(Km * E * Nm), u8(m.mxq_scale_bytes(Km, E * Nm // 32))
-        self.dymq, self.dyms = u8(T * Nm), u8(m.mxq_scale_bytes(T, Nm // 32))
+        self.dymq, self.dyms = u8(T * Nm), u8(m.mxq_scale_bytes(self.t_pad, Nm // 32))
         self.dymqT, self.dymsT = u8(Nm * self.t_pad), u8(m.mxq_scale_bytes(Nm, self.t_pad // 32))
         self.xmqT, self.xmsT = u8(Km * self.t_pad), u8(m.mxq_scale_bytes(Km, self.t_pad // 32))
         self.ym, self.dxm, self.dwm = bf(T, Nm), bf(T, Km), bf(E, Nm, Km)
@@ -218,15 +221,17 @@ class Workload:
             dw_call()
         # X and dY: row quant (fwd / dX operands) and per-group column quant (dW
         # operands) from one read each; W: row quant and column quant along N
-        m.mxq_quantize_grouped_dual(self.xm, T, Km, self.off, E, self.t_pad, self.xmq, self.xms, self.xmqT, self.xmsT)
+        m.mxq_quantize_grouped_dual_padded(self.xm, T, Km, self.off, E, self.t_pad, self.xmq, self.xms, self.xmqT,
+                                           self.xmsT)
         m.mxq_quantize(self.wm, m.BF16, E * Nm, Km, Km, -1, m.E4M3, 1, self.wmq, self.wms, self.wmqT, self.wmsT)
-        m.mxq_quantize_grouped_dual(self.dym, T, Nm, self.off, E, self.t_pad, self.dymq, self.dyms, self.dymqT,
-                                    self.dymsT)
+        m.mxq_quantize_grouped_dual_padded(self.dym, T, Nm, self.off, E, self.t_pad, self.dymq, self.dyms, self.dymqT,
+                                           self.dymsT)
         gf = 2 * T * Nm * Km
+        tp = self.t_pad
         timed("moe_fwd_gemm", gf, lambda: m.mxq_grouped_gemm(m.GG_FWD, self.xmq, self.xms, self.wmq, self.wms,
-                                                             self.off, E, T, Nm, Km, 0, self.ym))
+                                                             self.off, E, T, Nm, Km, tp, self.ym))
         timed("moe_dx_gemm", gf, lambda: m.mxq_grouped_gemm(m.GG_DX, self.dymq, self.dyms, self.wmqT, self.wmsT,
-                                                            self.off, E, T, Nm, Km, 0, self.dxm))
+                                                            self.off, E, T, Nm, Km, tp, self.dxm))
         timed("moe_dw_gemm", gf, lambda: m.mxq_grouped_gemm(m.GG_DW, self.dymqT, self.dymsT, self.xmqT, self.xmsT,
                                                             self.off, E, T, Nm, Km, self.t_pad, self.dwm))
         m.mxq_qdq_mxfp4(self.a4, self.y4, FP4["R"], FP4["C"], 32, 6.0)
@@ -758,14 +763,13 @@ def ncu_case(case: str):
         d_off = torch.from_numpy(off).to(dev)
         tp = m.mxq_grouped_padded_rows(T, E)
         xmd, dymd = xm.to(dev), dym.to(dev)
-        xq, xs = m.quantize_mxfp8(xmd)[:2]
         wq, ws, wqT, wsT = m.quantize_mxfp8(wm.reshape(E * N, K).to(dev), dual=True)
-        dq, ds = m.quantize_mxfp8(dymd)[:2]
-        dqT, dsT, xqT, xsT = u8(N * tp), u8(m.mxq_scale_bytes(N, tp // 32)), u8(K * tp), u8(m.mxq_scale_bytes(K, tp // 32))
-        m.mxq_quantize_grouped_col(dymd, T, N, d_off, E, tp, dqT, dsT)
-        m.mxq_quantize_grouped_col(xmd, T, K, d_off, E, tp, xqT, xsT)
-        m.mxq_grouped_gemm(m.GG_FWD, xq, xs, wq, ws, d_off, E, T, N, K, 0, bf(T, N))
-        m.mxq_grouped_gemm(m.GG_DX, dq, ds, wqT, wsT, d_off, E, T, N, K, 0, bf(T, K))
+        xq, xs, xqT, xsT = u8(T * K), u8(m.mxq_scale_bytes(tp, K // 32)), u8(K * tp), u8(m.mxq_scale_bytes(K, tp // 32))
+        dq, ds, dqT, dsT = u8(T * N), u8(m.mxq_scale_bytes(tp, N // 32)), u8(N * tp), u8(m.mxq_scale_bytes(N, tp // 32))
+        m.mxq_quantize_grouped_dual_padded(xmd, T, K, d_off, E, tp, xq, xs, xqT, xsT)
+        m.mxq_quantize_grouped_dual_padded(dymd, T, N, d_off, E, tp, dq, ds, dqT, dsT)
+        m.mxq_grouped_gemm(m.GG_FWD, xq, xs, wq, ws, d_off, E, T, N, K, tp, bf(T, N))
+        m.mxq_grouped_gemm(m.GG_DX, dq, ds, wqT, wsT, d_off, E, T, N, K, tp, bf(T, K))
         m.mxq_grouped_gemm(m.GG_DW, dqT, dsT, xqT, xsT, d_off, E, T, N, K, tp, bf(E, N, K))
     torch.cuda.synchronize()
     assert m.mxq_poll_device_error() == 0
@@ -868,16 +872,16 @@ def component_timings(wl, peaks):
     tp = wl.t_pad
 
     def gdual_set(x, C):
-        q, sc = u8(T * C), u8(m.mxq_scale_bytes(T, C // 32))
+        q, sc = u8(T * C), u8(m.mxq_scale_bytes(tp, C // 32))
         qT, sT = u8(C * tp), u8(m.mxq_scale_bytes(C, tp // 32))
-        return lambda: m.mxq_quantize_grouped_dual(x, T, C, wl.off, E, tp, q, sc, qT, sT)
+        return lambda: m.mxq_quantize_grouped_dual_padded(x, T, C, wl.off, E, tp, q, sc, qT, sT)
 
     padded = int(wl.off_padded_total)
     for name, x, C in (("grouped_dual_quant_moe_X", wl.xm, Km), ("grouped_dual_quant_moe_dY", wl.dym, Nm)):
         ms = time_rotating([gdual_set(x, C)])
-        nbytes = T * C * (2 + 1 + 1 / 32) + C * padded * (1 + 1 / 32)
+        nbytes = T * C * (2 + 1) + padded * C / 32 + C * padded * (1 + 1 / 32)
         hbm_entry(name, "k_quant_cols_tma<1,1,1,0>", nbytes, ms,
-                  note="column output counted over the groups' padded length")
+                  note="row scales and column output counted over the groups' padded length")
 
     # ---- MXFP4 kernels on the 4096 x 4096 fp32 tensor
     nset = copies_past_l2(R4 * C4 * 8)
@@ -928,11 +932,11 @@ def component_timings(wl, peaks):
     tensor_entry("dense_dw_gemm", "k_gemm<1,MXF8,0>", fl, ms)
     del ops, y2, dx2, dw2
     gf = 2 * T * Nm * Km
-    ms = time_rotating([lambda: m.mxq_grouped_gemm(m.GG_FWD, wl.xmq, wl.xms, wl.wmq, wl.wms, wl.off, E, T, Nm, Km, 0,
-                                                   wl.ym)])
+    ms = time_rotating([lambda: m.mxq_grouped_gemm(m.GG_FWD, wl.xmq, wl.xms, wl.wmq, wl.wms, wl.off, E, T, Nm, Km,
+                                                   wl.t_pad, wl.ym)])
     tensor_entry("moe_fwd_gemm", "k_gemm<1,MXF8,0> grouped rows", gf, ms)
     ms = time_rotating([lambda: m.mxq_grouped_gemm(m.GG_DX, wl.dymq, wl.dyms, wl.wmqT, wl.wmsT, wl.off, E, T, Nm, Km,
-                                                   0, wl.dxm)])
+                                                   wl.t_pad, wl.dxm)])
     tensor_entry("moe_dx_gemm", "k_gemm<1,MXF8,0> grouped rows", gf, ms)
     ms = time_rotating([lambda: m.mxq_grouped_gemm(m.GG_DW, wl.dymqT, wl.dymsT, wl.xmqT, wl.xmsT, wl.off, E, T, Nm,
                                                    Km, wl.t_pad, wl.dwm)])

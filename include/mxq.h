@@ -162,6 +162,21 @@ mxq_status mxq_quantize_grouped_dual(const void *x_bf16, int64_t rows, int64_t c
                                      void *q_row, void *s_row, void *q_colT, void *s_colT,
                                      mxq_stream_t stream);
 
+/* The same quant with the row scales in the per-group padded layout:
+ * s_row is swz(t_pad, cols/32) (DEVICE, written in full), and the row scales
+ * of row r of group e sit at scale row P_e + (r - off[e]), where
+ * P_e = sum over e' < e of ceil128(off[e'+1] - off[e']) is the group's padded
+ * start, the same as in the column quant; every other scale row is zero.
+ * q_row is the plain [rows x cols] row quant as above, and q_colT/s_colT as
+ * above.  Each group's scale rows start a 512-byte scale tile, so the grouped
+ * forward / dX GEMM given this layout (t_pad > 0) tiles each group from its
+ * first row and computes no row twice.  q_row and s_row are required;
+ * other arguments and errors as for mxq_quantize_grouped_dual. */
+mxq_status mxq_quantize_grouped_dual_padded(const void *x_bf16, int64_t rows, int64_t cols,
+                                            const int64_t *d_offsets, int E, int64_t t_pad,
+                                            void *q_row, void *s_row, void *q_colT, void *s_colT,
+                                            mxq_stream_t stream);
+
 /* MXFP4 quant-dequant ([AMCT] sections 2, 3.2-3.3): fp32 x viewed as
  * [rows x cols] with cols the tensor's last dim; blocks of 32 along each row,
  * the last block of a row zero-padded (never spanning two rows);
@@ -258,7 +273,16 @@ mxq_status mxq_gemm(const uint8_t *a, const uint8_t *sa, const uint8_t *b, const
  *      [N x t_pad], swz(N, t_pad/32)), B = per-group column quant of X (codes
  *      [K x t_pad], swz(K, t_pad/32)); a group with no rows gives zeros.
  * K % 32 == 0 (FWD/DX), ldc is the output's row length (N for FWD/DW, K for
- * DX). */
+ * DX).
+ * t_pad: for MXQ_GG_DW the padded length of the column quants (a multiple of
+ * 128, >= mxq_grouped_padded_rows(T, E)).  For MXQ_GG_FWD / MXQ_GG_DX, 0
+ * means A's scales are swz(T, .) as written by mxq_quantize or
+ * mxq_quantize_grouped_dual: the row tiles are the matrix's 128-row tiles,
+ * and one that straddles a group boundary is computed once per group it
+ * touches; t_pad > 0 (same rule as for DW) means A's scales are in the
+ * per-group padded layout of mxq_quantize_grouped_dual_padded (swz(t_pad, .)):
+ * each group is tiled from its own first row.  Both give the same output bit
+ * for bit. */
 mxq_status mxq_grouped_gemm(mxq_gg_kind kind, const uint8_t *a, const uint8_t *sa,
                             const uint8_t *b, const uint8_t *sb, const int64_t *d_offsets, int E,
                             int64_t T, int64_t N, int64_t K, int64_t t_pad, void *out_bf16,

@@ -26,7 +26,7 @@ from . import build as _build
 __all__ = [
     "MXQError", "load", "BF16", "F32", "E4M3", "E2M1", "SAVE_QUANT", "RECOMPUTE", "GG_FWD", "GG_DX", "GG_DW",
     "mxq_scale_bytes", "mxq_grouped_padded_rows", "mxq_quantize", "mxq_quantize_grouped_col",
-    "mxq_quantize_grouped_dual", "mxq_qdq_mxfp4",
+    "mxq_quantize_grouped_dual", "mxq_quantize_grouped_dual_padded", "mxq_qdq_mxfp4",
     "mxq_gemm", "mxq_grouped_gemm", "mxq_linear_ctx_bytes", "mxq_linear_saved_bytes",
     "mxq_linear_workspace_bytes", "mxq_linear_fwd", "mxq_linear_bwd_dx", "mxq_linear_bwd_dw",
     "mxq_last_error_string", "mxq_poll_device_error", "mxq_linear_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
@@ -60,6 +60,7 @@ _SIGNATURES = {
     "mxq_quantize": (_I32, [_P, _I32, _I64, _I64, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "mxq_quantize_grouped_col": (_I32, [_P, _I64, _I64, _P, _I32, _I64, _P, _P, _P]),
     "mxq_quantize_grouped_dual": (_I32, [_P, _I64, _I64, _P, _I32, _I64, _P, _P, _P, _P, _P]),
+    "mxq_quantize_grouped_dual_padded": (_I32, [_P, _I64, _I64, _P, _I32, _I64, _P, _P, _P, _P, _P]),
     "mxq_qdq_mxfp4": (_I32, [_P, _P, _I64, _I64, _I32, _F32, _P]),
     "mxq_qdq_mxfp4_bf16": (_I32, [_P, _P, _I64, _I64, _I32, _F32, _P]),
     "mxq_mxfp4_ste_forward": (_I32, [_P, _P, _P, _I64, _I64, _I32, _F32, _P]),
@@ -161,6 +162,13 @@ def mxq_quantize_grouped_col(x, rows, cols, d_offsets, E, t_pad, q_colT, s_colT,
 def mxq_quantize_grouped_dual(x, rows, cols, d_offsets, E, t_pad, q_row, s_row, q_colT, s_colT, stream=None):
     _check(load().mxq_quantize_grouped_dual(_p(x), rows, cols, _p(d_offsets), E, t_pad, _p(q_row), _p(s_row),
                                             _p(q_colT), _p(s_colT), _s(stream)), "mxq_quantize_grouped_dual")
+
+
+def mxq_quantize_grouped_dual_padded(x, rows, cols, d_offsets, E, t_pad, q_row, s_row, q_colT, s_colT,
+                                     stream=None):
+    _check(load().mxq_quantize_grouped_dual_padded(_p(x), rows, cols, _p(d_offsets), E, t_pad, _p(q_row),
+                                                   _p(s_row), _p(q_colT), _p(s_colT), _s(stream)),
+           "mxq_quantize_grouped_dual_padded")
 
 
 def mxq_qdq_mxfp4(x, y, rows, cols, block_size=32, scale_factor=6.0, stream=None):

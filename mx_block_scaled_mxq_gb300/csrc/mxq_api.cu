@@ -248,9 +248,10 @@ mxq_status mxq_quantize(const void *x, mxq_dtype dtype, int64_t rows, int64_t co
     return cuda_result(e, "mxq_quantize launch");
 }
 
-mxq_status mxq_quantize_grouped_dual(const void *x_bf16, int64_t rows, int64_t cols, const int64_t *d_offsets,
-                                     int E, int64_t t_pad, void *q_row, void *s_row, void *q_colT, void *s_colT,
-                                     mxq_stream_t stream) {
+namespace {
+mxq_status grouped_dual(const void *x_bf16, int64_t rows, int64_t cols, const int64_t *d_offsets, int E,
+                        int64_t t_pad, void *q_row, void *s_row, void *q_colT, void *s_colT, mxq_stream_t stream,
+                        bool row_pad) {
     if (rows < 0 || cols < 0) return fail(MXQ_ERR_INVALID_ARG, "negative size");
     if (E < 1 || E > 4096) return fail(MXQ_ERR_INVALID_ARG, "E must be in [1, 4096]");
     if (cols % 8) return fail(MXQ_ERR_INVALID_ARG, "cols must be a multiple of 8");
@@ -273,8 +274,22 @@ mxq_status mxq_quantize_grouped_dual(const void *x_bf16, int64_t rows, int64_t c
                                                       t_pad, static_cast<uint8_t *>(q_row),
                                                       static_cast<uint8_t *>(s_row), static_cast<uint8_t *>(q_colT),
                                                       static_cast<uint8_t *>(s_colT),
-                                                      reinterpret_cast<cudaStream_t>(stream)),
+                                                      reinterpret_cast<cudaStream_t>(stream), row_pad),
                        "mxq_quantize_grouped_dual launch");
+}
+}  // namespace
+
+mxq_status mxq_quantize_grouped_dual(const void *x_bf16, int64_t rows, int64_t cols, const int64_t *d_offsets,
+                                     int E, int64_t t_pad, void *q_row, void *s_row, void *q_colT, void *s_colT,
+                                     mxq_stream_t stream) {
+    return grouped_dual(x_bf16, rows, cols, d_offsets, E, t_pad, q_row, s_row, q_colT, s_colT, stream, false);
+}
+
+mxq_status mxq_quantize_grouped_dual_padded(const void *x_bf16, int64_t rows, int64_t cols,
+                                            const int64_t *d_offsets, int E, int64_t t_pad, void *q_row,
+                                            void *s_row, void *q_colT, void *s_colT, mxq_stream_t stream) {
+    if (!q_row || !s_row) return fail(MXQ_ERR_INVALID_ARG, "q_row and s_row are required");
+    return grouped_dual(x_bf16, rows, cols, d_offsets, E, t_pad, q_row, s_row, q_colT, s_colT, stream, true);
 }
 
 mxq_status mxq_quantize_grouped_col(const void *x_bf16, int64_t rows, int64_t cols, const int64_t *d_offsets, int E,
@@ -386,9 +401,15 @@ mxq_status mxq_grouped_gemm(mxq_gg_kind kind, const uint8_t *a, const uint8_t *s
     if (kind == MXQ_GG_FWD || kind == MXQ_GG_DX) {
         if (N % 128) return fail(MXQ_ERR_INVALID_ARG, "N must be a multiple of 128 for the grouped forward/dX");
         if (K % 32) return fail(MXQ_ERR_INVALID_ARG, "K must be a multiple of 32");
+        if (t_pad != 0 && (t_pad < 0 || t_pad % 128 || t_pad < mxq_grouped_padded_rows(T, E)))
+            return fail(MXQ_ERR_INVALID_ARG,
+                        "t_pad must be 0 or a multiple of 128 and >= mxq_grouped_padded_rows(T, E) = %lld",
+                        (long long)mxq_grouped_padded_rows(T, E));
+        if (t_pad > (1ll << 31)) return fail(MXQ_ERR_UNSUPPORTED, "t_pad above 2^31");
         if (T == 0) return ok();
         g.mode = mxq::kGroupedRows;
         g.T = T;
+        g.a_row_pad = t_pad;
         g.a = a; g.sa = sa; g.b = b; g.sb = sb;
         if (kind == MXQ_GG_FWD) {  // out[T x N] = X[T x K] . W_e[N x K]^T
             g.a_rows = T; g.a_k = K;

@@ -94,7 +94,7 @@ struct Cfg {
     static constexpr uint32_t OFF_MISC = OFF_BAR + 256;
     static constexpr uint32_t OFF_GRP = OFF_MISC + 256;  // group tables (grouped modes, E <= kMaxTableE)
     // epilogue store staging: kEpiWarps x kStoreSlots x (32 rows x 64 bytes), 1024-aligned
-    static constexpr uint32_t OFF_STORE = (OFF_GRP + 2 * 8 * (kMaxTableE + 1) + 1023) / 1024 * 1024;
+    static constexpr uint32_t OFF_STORE = (OFF_GRP + 3 * 8 * (kMaxTableE + 1) + 1023) / 1024 * 1024;
     static constexpr uint32_t SMEM_ALLOC = OFF_STORE + kEpiWarps * kStoreSlots * 2048 + 1024;  // + slack to align the base
     static_assert(NUM_BARS * 8 <= 256, "barrier area");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
@@ -110,6 +110,7 @@ struct Params {
     const int64_t *offsets;
     int E;
     int64_t T;                         // grouped modes: token rows, the value off[E] must hold
+    int64_t a_row_pad;                 // kGroupedRows: A's scales in the per-group padded layout (t_pad rows), or 0
     int64_t b_row_per_expert, b_k_per_expert, c_expert_stride;
     int m_tiles, n_tiles;  // tile counts (m in units of 128 * CG rows)
     int n_fastest;         // kDense tile order: 1 = n fastest (A is the larger operand)
@@ -171,34 +172,47 @@ __device__ __forceinline__ void add_bias32(uint32_t (&acc)[32], const __nv_bfloa
 // Group tables a CTA builds once in shared memory (grouped modes with
 // E <= kMaxTableE): off[e] = group offsets, pre[e] = exclusive prefix of the
 // per-expert tile counts (kGroupedRows) or of the padded group lengths
-// (kGroupedK).  Tiles are then decoded without touching global memory.
+// (kGroupedK), pst[e] = exclusive prefix of the padded group lengths
+// (kGroupedRows with A's scales in the per-group padded layout: group e's
+// first scale row).  Tiles are then decoded without touching global memory.
 struct GroupTables {
-    const int64_t *off, *pre;
+    const int64_t *off, *pre, *pst;
 };
 
+// Row tiles of expert e in the grouped forward / dX, rows [o0, o1): with A's
+// scales in the per-group padded layout the tiles start at the group's first
+// row, so no row is computed twice; otherwise they are the TM-row tiles of
+// the matrix that overlap the group.
+template <int TM>
+__device__ __forceinline__ int64_t expert_row_tiles(const Params &p, int64_t o0, int64_t o1) {
+    if (o1 <= o0) return 0;
+    return p.a_row_pad ? (o1 - o0 + TM - 1) / TM : (o1 - 1) / TM - o0 / TM + 1;
+}
+
 template <int CG>
-__device__ void build_group_tables(const Params &p, int64_t *off, int64_t *pre, int warp, int lane) {
+__device__ void build_group_tables(const Params &p, int64_t *off, int64_t *pre, int64_t *pst, int warp, int lane) {
     constexpr int TM = Cfg<CG>::TILE_M;
     if (warp != 0) return;
-    int64_t run = 0;
+    int64_t run = 0, run_p = 0;
     for (int base = 0; base <= p.E; base += 32) {
         const int e = base + lane;
         int64_t o0 = 0, o1 = 0;
         if (e <= p.E) { o0 = p.offsets[e]; off[e] = o0; }
         if (e < p.E) o1 = p.offsets[e + 1];
-        int64_t v = 0;
+        int64_t v = 0, w = 0;
         if (e < p.E) {
-            if (p.mode == kGroupedRows) v = (o1 > o0) ? ((o1 - 1) / TM - o0 / TM + 1) * p.n_tiles : 0;
-            else v = (o1 - o0 + 127) / 128 * 128;
+            w = (o1 - o0 + 127) / 128 * 128;
+            v = p.mode == kGroupedRows ? expert_row_tiles<TM>(p, o0, o1) * p.n_tiles : w;
         }
-        int64_t incl = v;
+        int64_t incl = v, incl_p = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int64_t u = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += u;
+            const int64_t u = __shfl_up_sync(0xffffffffu, incl, o), up = __shfl_up_sync(0xffffffffu, incl_p, o);
+            if (lane >= o) { incl += u; incl_p += up; }
         }
-        if (e <= p.E) pre[e] = run + incl - v;
+        if (e <= p.E) { pre[e] = run + incl - v; pst[e] = run_p + incl_p - w; }
         run += __shfl_sync(0xffffffffu, incl, 31);
+        run_p += __shfl_sync(0xffffffffu, incl_p, 31);
     }
 }
 
@@ -208,6 +222,7 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
     TileInfo t{};
     t.k_last = 4;
     int64_t tile_row0 = 0, bn0 = 0;  // first row of the tile; first row of B for the tile
+    int64_t srow0 = -1;              // first scale row of the tile, where it differs from tile_row0
     if (p.mode == kGroupedRows && gt.off != nullptr) {
         // the expert whose tile range [pre[e], pre[e+1]) holds bid (binary search)
         if (bid >= gt.pre[p.E]) { t.valid = 0; return t; }
@@ -218,11 +233,12 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
         }
         const int fe = lo;
         const int64_t fo0 = gt.off[fe], fo1 = gt.off[fe + 1];
-        const int64_t mtiles_e = (fo1 - 1) / TM - fo0 / TM + 1;
+        const int64_t mtiles_e = expert_row_tiles<TM>(p, fo0, fo1);
         const int64_t local = bid - gt.pre[fe];
-        const int64_t nt = local / mtiles_e, mt = fo0 / TM + local % mtiles_e;
+        const int64_t nt = local / mtiles_e, j = local % mtiles_e;
         t.valid = 1;
-        tile_row0 = mt * TM;
+        tile_row0 = p.a_row_pad ? fo0 + j * TM : (fo0 / TM + j) * TM;
+        if (p.a_row_pad) srow0 = gt.pst[fe] + j * TM;
         bn0 = fe * p.b_row_per_expert + nt * BN;
         t.b_k0 = fe * p.b_k_per_expert; t.b_katom0 = t.b_k0 / BK;
         t.col0 = nt * BN;
@@ -254,22 +270,23 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
         t.row_lo = tile_row0 + 128 * rank;
         t.row_hi = min(p.M, t.row_lo + 128);
     } else if (p.mode == kGroupedRows) {
-        // tiles of expert e: every TM-row tile overlapping [o_e, o_e+1), times n_tiles
-        int64_t run = 0;
+        // tiles of expert e (expert_row_tiles), times n_tiles; the padded
+        // starts P_e of the groups are summed alongside
+        int64_t run = 0, run_p = 0;
         int fe = -1;
-        int64_t fstart = 0, fo0 = 0, fo1 = 0;
+        int64_t fstart = 0, fo0 = 0, fo1 = 0, fpst = 0;
         for (int base = 0; base < p.E; base += 32) {
             const int e = base + lane;
             int64_t o0 = 0, o1 = 0;
             if (e < p.E) { o0 = p.offsets[e]; o1 = p.offsets[e + 1]; }
-            const int64_t cnt = (o1 > o0) ? ((o1 - 1) / TM - o0 / TM + 1) * p.n_tiles : 0;
-            int64_t incl = cnt;
+            const int64_t cnt = expert_row_tiles<TM>(p, o0, o1) * p.n_tiles, w = (o1 - o0 + 127) / 128 * 128;
+            int64_t incl = cnt, incl_p = w;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
+                const int64_t v = __shfl_up_sync(0xffffffffu, incl, o), vp = __shfl_up_sync(0xffffffffu, incl_p, o);
+                if (lane >= o) { incl += v; incl_p += vp; }
             }
-            const int64_t start = run + incl - cnt;
+            const int64_t start = run + incl - cnt, pstart = run_p + incl_p - w;
             const bool mine = cnt > 0 && bid >= start && bid < start + cnt;
             const unsigned bal = __ballot_sync(0xffffffffu, mine);
             if (bal) {
@@ -278,16 +295,19 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
                 fstart = __shfl_sync(0xffffffffu, start, src);
                 fo0 = __shfl_sync(0xffffffffu, o0, src);
                 fo1 = __shfl_sync(0xffffffffu, o1, src);
+                fpst = __shfl_sync(0xffffffffu, pstart, src);
                 break;
             }
             run += __shfl_sync(0xffffffffu, incl, 31);
+            run_p += __shfl_sync(0xffffffffu, incl_p, 31);
         }
         if (fe < 0) { t.valid = 0; return t; }
-        const int64_t mtiles_e = (fo1 - 1) / TM - fo0 / TM + 1;
+        const int64_t mtiles_e = expert_row_tiles<TM>(p, fo0, fo1);
         const int64_t local = bid - fstart;
-        const int64_t nt = local / mtiles_e, mt = fo0 / TM + local % mtiles_e;
+        const int64_t nt = local / mtiles_e, j = local % mtiles_e;
         t.valid = 1;
-        tile_row0 = mt * TM;
+        tile_row0 = p.a_row_pad ? fo0 + j * TM : (fo0 / TM + j) * TM;
+        if (p.a_row_pad) srow0 = fpst + j * TM;
         bn0 = fe * p.b_row_per_expert + nt * BN;
         t.b_k0 = fe * p.b_k_per_expert; t.b_katom0 = t.b_k0 / BK;
         t.col0 = nt * BN;
@@ -316,7 +336,7 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
         t.c_off = static_cast<int64_t>(e) * p.c_expert_stride;
     }
     t.a_row0 = tile_row0 + 128 * rank;  // this CTA's 128 rows of A (and of the output)
-    t.a_ratom = t.a_row0 / 128;
+    t.a_ratom = (srow0 >= 0 ? srow0 + 128 * rank : t.a_row0) / 128;
     t.out_row0 = t.a_row0;
     t.b_row0 = bn0 + BR * rank;         // this CTA's share of B's rows
     t.b_ratom = bn0 / 128;              // the tile's B scale tiles (all of them)
@@ -591,7 +611,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if constexpr (CLUSTER) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    GroupTables gt{nullptr, nullptr};
+    GroupTables gt{nullptr, nullptr, nullptr};
     if (p.mode != kDense) {
         // malformed offsets: no tile is decoded from them, no load or store is issued
         if (warp == 0 && !group_offsets_valid(p.offsets, p.E, p.T, lane) && lane == 0) {
@@ -602,10 +622,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (p.mode != kDense && p.E <= kMaxTableE && !*abort_flag) {
         int64_t *off = reinterpret_cast<int64_t *>(smem + C::OFF_GRP), *pre = off + kMaxTableE + 1;
-        build_group_tables<CG>(p, off, pre, warp, lane);
+        int64_t *pst = pre + kMaxTableE + 1;
+        build_group_tables<CG>(p, off, pre, pst, warp, lane);
         __syncthreads();
         gt.off = off;
         gt.pre = pre;
+        gt.pst = pst;
     }
     // stage barriers and the accumulator-release barriers of the even CTA
     uint32_t lead_full = bar_full, lead_acce = bar_acce, lead_headf0 = bar_headf0;
@@ -1068,7 +1090,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         !make_tmap(&tmB, g.b, g.b_rows, esz * g.b_k, C::B_ROWS))
         return cudaErrorInvalidValue;
     if (CG == 2) {
-        if (!make_scale_tmap(&tmSA, g.sa, scale_bytes_of(g.a_rows, g.a_k)) ||
+        if (!make_scale_tmap(&tmSA, g.sa, scale_bytes_of(p.a_row_pad ? p.a_row_pad : g.a_rows, g.a_k)) ||
             !make_scale_tmap(&tmSB, g.sb, scale_bytes_of(g.b_rows, g.b_k)))
             return cudaErrorInvalidValue;
     } else {
@@ -1213,13 +1235,14 @@ cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
     p.M = g.M; p.N = g.N; p.ldc = g.ldc;
     p.K = g.kind == kBF16 ? 2 * g.K : g.K;  // the mainloop counts contraction bytes
     p.offsets = g.offsets; p.E = g.E; p.T = g.T;
+    p.a_row_pad = g.mode == kGroupedRows ? g.a_row_pad : 0;
     p.b_row_per_expert = g.b_row_per_expert;
     p.b_k_per_expert = g.b_k_per_expert;
     p.c_expert_stride = g.c_expert_stride;
     p.bias = g.mode == kDense ? static_cast<const __nv_bfloat16 *>(g.bias) : nullptr;
     p.n_tiles = static_cast<int>((g.N + BN - 1) / BN);
     p.n_fastest = g.mode == kDense && g.a_rows > g.b_rows ? 1 : 0;
-    p.sa_bytes = g.kind == kBF16 ? 0 : static_cast<uint64_t>(scale_bytes_of(g.a_rows, g.a_k));
+    p.sa_bytes = g.kind == kBF16 ? 0 : static_cast<uint64_t>(scale_bytes_of(p.a_row_pad ? p.a_row_pad : g.a_rows, g.a_k));
     p.sb_bytes = g.kind == kBF16 ? 0 : static_cast<uint64_t>(scale_bytes_of(g.b_rows, g.b_k));
     p.c_bytes = 2ull * static_cast<uint64_t>(g.mode == kGroupedK ? static_cast<int64_t>(g.E) * g.M : g.M) *
                 static_cast<uint64_t>(g.ldc);

@@ -17,10 +17,11 @@ cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, i
 cudaError_t launch_quant_cols(const uint16_t *x, int64_t R, int64_t C, int64_t ldx, uint8_t *q_row,
                               uint8_t *s_row, uint8_t *qT, uint8_t *sT, cudaStream_t st);
 // Per-group column MXFP8 quant of bf16 x [T x C]; q_row/s_row non-null adds the
-// plain row quant of x from the same read (cols % 32 == 0).
+// plain row quant of x from the same read (cols % 32 == 0), its scales in
+// swz(T, C/32) or, with row_pad, in the per-group padded layout swz(t_pad, C/32).
 cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, const int64_t *d_off, int E,
                                       int64_t t_pad, uint8_t *q_row, uint8_t *s_row, uint8_t *qT, uint8_t *sT,
-                                      cudaStream_t st);
+                                      cudaStream_t st, bool row_pad);
 cudaError_t launch_qdq_mxfp4(const float *x, float *y, uint32_t *mask, int64_t rows, int64_t cols, float sf,
                              cudaStream_t st);
 // MXFP4 quant-dequant bf16 -> bf16, blocks of 32 along rows; cols % 32 == 0, 16-byte aligned.
@@ -55,6 +56,9 @@ struct GemmProblem {
     int64_t b_k_per_expert;   // kGroupedRows: B contraction offset of expert e = e * this
     int64_t c_expert_stride;  // kGroupedK: elements between experts' outputs
     int64_t T;                // kGroupedRows: token rows (= off[E])
+    int64_t a_row_pad;        // kGroupedRows: 0, or t_pad when A's scales are in the per-group
+                              // padded layout swz(t_pad, a_k/32) (row r of group e at scale row
+                              // P_e + r - off[e], P_e = sum over e' < e of ceil128(n_e'))
     const void *bias;         // kDense: optional bf16 [N] added in fp32 before rounding (16-byte aligned)
 };
 cudaError_t launch_gemm(const GemmProblem &p, cudaStream_t st);

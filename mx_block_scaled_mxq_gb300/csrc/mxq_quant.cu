@@ -394,6 +394,7 @@ struct ColParams {
     int64_t kb_col_tiles;
     const int64_t *offsets;  // GROUPED: E+1 device offsets
     int E;
+    int row_pad;             // GROUPED with ROWS: row scales in the per-group padded layout swz(ldqT, C/32)
     float sf;                // MXFP4 scale factor (row pass in FMT 2)
     unsigned int *err;       // device error word (malformed offsets; debug-build bounds checks)
 };
@@ -407,7 +408,7 @@ __device__ __forceinline__ ColExtents col_extents(const ColParams &P) {
     ColExtents e;
     e.x = P.R > 0 ? static_cast<uint64_t>((P.R - 1) * P.ldx + P.C) * 2 : 0;
     e.q_row = static_cast<uint64_t>(P.R * P.C);
-    e.s_row = static_cast<uint64_t>((P.R + 127) / 128 * P.kb_row_tiles * 512);
+    e.s_row = static_cast<uint64_t>(((P.row_pad ? P.ldqT : P.R) + 127) / 128 * P.kb_row_tiles * 512);
     e.qT = static_cast<uint64_t>(P.C * P.ldqT);
     e.sT = static_cast<uint64_t>((P.C + 127) / 128 * P.kb_col_tiles * 512);
     return e;
@@ -753,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
         }
     };
 
-    if (ROWS && GROUPED && blockIdx.x == 0) {
+    if (ROWS && GROUPED && !P.row_pad && blockIdx.x == 0) {
         // row scales of the padding rows [R, ceil128(R)) of the last scale tile:
         // no tile owns them
         const int64_t npad = (P.R + 127) / 128 * 128 - P.R;
@@ -845,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
                             stg_v4(dst + 16, hi4);
                         }
                     }
-                    if (GROUPED)  // row-major staging: row r's four blocks form word r
+                    if (GROUPED && !P.row_pad)  // row-major staging: row r's four blocks form word r
                         srow_atom[4 * row + blk] = gc < P.C ? sbyte : 0;
                     else
                         srow_atom[16 * (row & 31) + 4 * (row >> 5) + blk] = valid ? sbyte : 0;
@@ -925,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
             const int64_t tn = t + kRing * static_cast<int64_t>(gridDim.x);
             if (warp == 0 && tn < n_tiles) issue(tn, buf);
         }
-        if (ROWS && GROUPED && tid >= kThreads - kTile && tid - (kThreads - kTile) < nvalid) {
+        if (ROWS && GROUPED && !P.row_pad && tid >= kThreads - kTile && tid - (kThreads - kTile) < nvalid) {
             // A group's rows start anywhere inside a 128-row scale tile: each
             // row's word goes to its own place, and only this tile's rows.
             const int row = tid - (kThreads - kTile);
@@ -934,7 +935,9 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
             if (MXQ_IN_BOUNDS(dst, 4, P.s_row, ext.s_row, err))
                 *reinterpret_cast<uint32_t *>(dst) = *reinterpret_cast<const uint32_t *>(srow_atom + 4 * row);
         }
-        if (ROWS && !GROUPED && tid < 32) {
+        if (ROWS && (!GROUPED || P.row_pad) && tid < 32) {
+            // (per-group padded layout: padded tile rt is scale tile rt, its
+            // padding rows zero)
             const uint4 v = *reinterpret_cast<const uint4 *>(srow_atom + 16 * tid);
             uint8_t *dst = P.s_row + (rt * P.kb_row_tiles + ct) * 512 + 16 * tid;
             if (MXQ_IN_BOUNDS(dst, 16, P.s_row, ext.s_row, err)) stg_v4(dst, v);
@@ -1425,17 +1428,28 @@ cudaError_t launch_quant_cols(const uint16_t *x, int64_t R, int64_t C, int64_t l
 
 cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, const int64_t *d_off, int E,
                                       int64_t t_pad, uint8_t *q_row, uint8_t *s_row, uint8_t *qT, uint8_t *sT,
-                                      cudaStream_t st) {
+                                      cudaStream_t st, bool row_pad) {
     ColParams P{};
     P.x = x; P.R = T; P.C = C; P.ldx = C;
     P.q_row = q_row; P.s_row = s_row; P.kb_row_tiles = ((C / 32) + 3) / 4;
     P.qT = qT; P.sT = sT; P.ldqT = t_pad; P.kb_col_tiles = (t_pad / 32 + 3) / 4;
     P.offsets = d_off; P.E = E;
+    P.row_pad = row_pad && q_row ? 1 : 0;
     cudaError_t res = device_error_word(&P.err);
     if (res != cudaSuccess) return res;
+    if (P.row_pad && T == 0) {
+        // no rows: every padded row scale is zero
+        if ((res = cudaMemsetAsync(s_row, 0, static_cast<size_t>(t_pad / 128 * P.kb_row_tiles * 512), st)) !=
+            cudaSuccess)
+            return res;
+    }
     if (q_row && T > 0) {
         if (launch_cols_tma<true, true>(P, t_pad / kTile, st, &res)) return res;
-        // no tensor map for x: the row quant on its own, then the column quant
+        // no tensor map for x (only a row count of 2^31 or more gets here, as
+        // the entry points check x's alignment): the row quant on its own,
+        // then the column quant; the padded row-scale layout needs the
+        // combined kernel
+        if (P.row_pad) return cudaErrorNotSupported;
         if ((res = launch_quant_rows(x, false, 0, T, C, C, q_row, s_row, st)) != cudaSuccess) return res;
     } else if (launch_cols_tma<false, true>(P, t_pad / kTile, st, &res)) {
         return res;

@@ -119,6 +119,15 @@ def test_host_validation_rejects_before_launch(lib):
     assert "t_pad" in m.mxq_last_error_string()
     assert _status(m.mxq_grouped_gemm, m.GG_FWD, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 192, 64, 0, FAKE, 0) == INV
     assert _status(m.mxq_grouped_gemm, m.GG_DW, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 128, 64, 100, FAKE, 0) == INV
+    # the per-group padded row scales: the row outputs are required, and the
+    # forward / dX take t_pad = 0 or a valid padded length
+    assert _status(m.mxq_quantize_grouped_dual_padded, FAKE, 100, 64, FAKE, 2, 512, None, None, FAKE, FAKE,
+                   0) == INV
+    assert _status(m.mxq_quantize_grouped_dual_padded, FAKE, 100, 64, FAKE, 2, 128, FAKE, FAKE, FAKE, FAKE,
+                   0) == INV
+    assert _status(m.mxq_grouped_gemm, m.GG_FWD, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 128, 64, 200, FAKE, 0) == INV
+    assert "t_pad" in m.mxq_last_error_string()
+    assert _status(m.mxq_grouped_gemm, m.GG_DX, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 128, 64, -128, FAKE, 0) == INV
     # linear: dimensions multiple of 32, workspace large enough
     assert _status(m.mxq_linear_fwd, FAKE, FAKE, 100, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 1 << 30, 0) == INV
     assert _status(m.mxq_linear_fwd, FAKE, FAKE, 64, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 16, 0) == INV

@@ -13,9 +13,11 @@ DEV = "cuda"
 
 
 class MoE:
-    """Quantized operands of one MoE expert layer, built through the C ABI."""
+    """Quantized operands of one MoE expert layer, built through the C ABI.
+    padded=True takes X's and dY's row quants from the grouped dual quant with
+    per-group padded row scales, and passes t_pad to the forward and dX."""
 
-    def __init__(self, mxq, off, x, w, dy):
+    def __init__(self, mxq, off, x, w, dy, padded=False):
         self.mxq = mxq
         self.off = off
         self.E = len(off) - 1
@@ -24,12 +26,24 @@ class MoE:
         E, T, K, N = self.E, self.T, self.K, self.N
         self.d_off = torch.from_numpy(off).to(DEV)
         xg, wg, dyg = x.to(DEV), w.reshape(E * N, K).to(DEV), dy.to(DEV)
-        self.xq, self.xs, _, _ = mxq.quantize_mxfp8(xg)                   # forward A
         self.wq, self.ws, self.wqT, self.wsT = mxq.quantize_mxfp8(wg, dual=True)  # forward B, dX B
-        self.dyq, self.dys, _, _ = mxq.quantize_mxfp8(dyg)                # dX A
         self.t_pad = mxq.mxq_grouped_padded_rows(T, E)
-        self.dyqT, self.dysT = self._gcol(dyg, N)                         # dW A
-        self.xqT, self.xsT = self._gcol(xg, K)                            # dW B
+        self.row_pad = self.t_pad if padded else 0
+        if padded:
+            self.xq, self.xs, self.xqT, self.xsT = self._gdual_padded(xg, K)     # forward A, dW B
+            self.dyq, self.dys, self.dyqT, self.dysT = self._gdual_padded(dyg, N)  # dX A, dW A
+        else:
+            self.xq, self.xs, _, _ = mxq.quantize_mxfp8(xg)                   # forward A
+            self.dyq, self.dys, _, _ = mxq.quantize_mxfp8(dyg)                # dX A
+            self.dyqT, self.dysT = self._gcol(dyg, N)                         # dW A
+            self.xqT, self.xsT = self._gcol(xg, K)                            # dW B
+
+    def _gdual_padded(self, t, C):
+        u8 = lambda n: torch.empty((n,), dtype=torch.uint8, device=DEV)  # noqa: E731
+        q, s = u8(max(self.T, 1) * C), u8(self.mxq.mxq_scale_bytes(self.t_pad, C // 32))
+        qT, sT = u8(C * self.t_pad), u8(self.mxq.mxq_scale_bytes(C, self.t_pad // 32))
+        self.mxq.mxq_quantize_grouped_dual_padded(t, self.T, C, self.d_off, self.E, self.t_pad, q, s, qT, sT)
+        return q, s, qT, sT
 
     def _gcol(self, t, C):
         qT = torch.empty((C, self.t_pad), dtype=torch.uint8, device=DEV)
@@ -40,13 +54,13 @@ class MoE:
     def fwd(self):
         y = torch.full((self.T, self.N), float("nan"), dtype=torch.bfloat16, device=DEV)
         self.mxq.mxq_grouped_gemm(self.mxq.GG_FWD, self.xq, self.xs, self.wq, self.ws, self.d_off, self.E, self.T,
-                                  self.N, self.K, 0, y)
+                                  self.N, self.K, self.row_pad, y)
         return y
 
     def dx(self):
         dx = torch.full((self.T, self.K), float("nan"), dtype=torch.bfloat16, device=DEV)
         self.mxq.mxq_grouped_gemm(self.mxq.GG_DX, self.dyq, self.dys, self.wqT, self.wsT, self.d_off, self.E,
-                                  self.T, self.N, self.K, 0, dx)
+                                  self.T, self.N, self.K, self.row_pad, dx)
         return dx
 
     def dw(self):
@@ -124,6 +138,11 @@ def test_full_size_moe_sampled(mxq):
     y, dx, dw = moe.fwd(), moe.dx(), moe.dw()
     torch.cuda.synchronize()
     assert mxq.mxq_poll_device_error() == 0
+    # the per-group padded row scales give the same forward and dX bit for bit
+    pm = MoE(mxq, off, x, w, dy, padded=True)
+    assert torch.equal(pm.fwd().view(torch.int16), y.view(torch.int16))
+    assert torch.equal(pm.dx().view(torch.int16), dx.view(torch.int16))
+    del pm
     n = np.diff(off)
     rng = np.random.default_rng(0)
     # six non-empty experts (the oracle re-quantizes each one's full weight):
@@ -190,3 +209,38 @@ def test_grouped_many_experts_decode_without_tables(mxq):
             assert not np.any(got_dw[e])
         else:
             check_close(dw[e], ref_dw[e])
+
+
+@pytest.mark.parametrize("sizes,K,N", [([3, 0, 200, 0, 97], 256, 256), ([128, 128], 160, 384), ([0, 0, 1], 1024, 1024),
+                                       ([129, 127, 0, 3, 255, 1], 224, 256), ([1] * 40, 64, 128)])
+def test_grouped_padded_row_scales(mxq, sizes, K, N):
+    """Forward and dX from the per-group padded row scales (tiles start at
+    each group's first row): bit for bit the result of the matrix-aligned row
+    tiles, and within tolerance of the oracle; the weight gradient from the
+    same padded quant's column outputs likewise."""
+    off, x, w, dy = mxq_inputs.moe_inputs(len(sizes), sum(sizes), K, N, seed=len(sizes) + K + 7, sizes=sizes)
+    ref, pad = MoE(mxq, off, x, w, dy), MoE(mxq, off, x, w, dy, padded=True)
+    y, dx, dw = pad.fwd(), pad.dx(), pad.dw()
+    torch.cuda.synchronize()
+    assert mxq.mxq_poll_device_error() == 0
+    assert torch.equal(y.view(torch.int16), ref.fwd().view(torch.int16))
+    assert torch.equal(dx.view(torch.int16), ref.dx().view(torch.int16))
+    assert torch.equal(dw.view(torch.int16), ref.dw().view(torch.int16))
+    qx, sx = oracle.mxfp8_quant_rows(x)
+    qw, sw, qwT, swT = _oracle_w(w)
+    qdy, sdy = oracle.mxfp8_quant_rows(dy)
+    check_close(y, oracle.grouped_fwd_ref(qx, sx, qw, sw, off))
+    check_close(dx, oracle.grouped_fwd_ref(qdy, sdy, qwT, swT, off))
+
+
+def test_grouped_padded_row_scales_many_experts(mxq):
+    """300 experts (tiles decoded from the device offsets, no shared-memory
+    tables): padded and matrix-aligned row tiles agree bit for bit."""
+    E, T, K, N = 300, 1200, 64, 128
+    sizes = mxq_inputs.dirichlet_group_sizes(E, T, alpha=0.5, seed=3)
+    off, x, w, dy = mxq_inputs.moe_inputs(E, T, K, N, seed=5, sizes=sizes)
+    ref, pad = MoE(mxq, off, x, w, dy), MoE(mxq, off, x, w, dy, padded=True)
+    assert torch.equal(pad.fwd().view(torch.int16), ref.fwd().view(torch.int16))
+    assert torch.equal(pad.dx().view(torch.int16), ref.dx().view(torch.int16))
+    torch.cuda.synchronize()
+    assert mxq.mxq_poll_device_error() == 0

@@ -328,6 +328,48 @@ def test_grouped_dual_quant_300_groups(mxq):
     assert np.array_equal(sT, oracle.swizzle_scales(osT))
 
 
+def _grouped_dual_padded(mxq, x, off):
+    T, C = x.shape
+    E = len(off) - 1
+    t_pad = mxq.mxq_grouped_padded_rows(T, E)
+    poison = lambda *shape: torch.full(shape, 0xAB, dtype=torch.uint8, device=DEV)  # noqa: E731
+    q, s = poison(max(T, 1), C), poison(mxq.mxq_scale_bytes(t_pad, C // 32))
+    qT, sT = poison(C, t_pad), poison(mxq.mxq_scale_bytes(C, t_pad // 32))
+    mxq.mxq_quantize_grouped_dual_padded(x.to(DEV), T, C, torch.from_numpy(off).to(DEV), E, t_pad, q, s, qT, sT)
+    return q.cpu().numpy()[:T], s.cpu().numpy(), qT.cpu().numpy(), sT.cpu().numpy(), t_pad
+
+
+def _padded_row_scales(os_, off, t_pad):
+    """The oracle's row scales laid out per group: group e's rows from padded
+    row P_e = sum of ceil128 of the earlier groups' lengths, zeros elsewhere."""
+    L = np.zeros((t_pad, os_.shape[1]), np.uint8)
+    p = 0
+    for e in range(len(off) - 1):
+        n = int(off[e + 1] - off[e])
+        L[p:p + n] = os_[int(off[e]):int(off[e + 1])]
+        p += (n + 127) // 128 * 128
+    return oracle.swizzle_scales(L)
+
+
+@pytest.mark.parametrize("sizes", [[0, 5, 128, 33, 0, 200, 1], [300], [0, 0, 64], [1] * 40, [129, 127, 0, 3],
+                                   [0, 0]])
+@pytest.mark.parametrize("C", [160, 256])
+def test_grouped_dual_quant_padded_row_scales(mxq, sizes, C):
+    """The per-group padded row-scale layout: row codes as the plain row
+    quant, row scales placed per group (every padding byte zero, outputs
+    poisoned first), column outputs as the per-group column quant."""
+    off = mxq_inputs.offsets_from_sizes(sizes)
+    T = int(off[-1])
+    x = _inputs(T, C, "heavy", seed=len(sizes) + C + 1) if T else torch.zeros((0, C), dtype=torch.bfloat16)
+    q, s, qT, sT, t_pad = _grouped_dual_padded(mxq, x, off)
+    oq, os_ = oracle.mxfp8_quant_rows(x) if T else (np.zeros((0, C), np.uint8), np.zeros((0, C // 32), np.uint8))
+    assert np.array_equal(q, oq)
+    assert np.array_equal(s, _padded_row_scales(os_, off, t_pad))
+    oqT, osT = oracle.mxfp8_quant_cols_grouped(x, off, t_pad)
+    assert np.array_equal(qT, oqT)
+    assert np.array_equal(sT, oracle.swizzle_scales(osT))
+
+
 def test_grouped_dual_quant_full_size_moe_dy(mxq):
     """The MoE layer's dY, 32768 x 4096 bf16 in 32 Dirichlet(0.5) groups: every
     byte of the four outputs against the oracle."""
@@ -341,6 +383,11 @@ def test_grouped_dual_quant_full_size_moe_dy(mxq):
     oqT, osT = oracle.mxfp8_quant_cols_grouped(x, off, t_pad)
     assert np.array_equal(qT, oqT)
     assert np.array_equal(sT, oracle.swizzle_scales(osT))
+    # the per-group padded row scales of the same tensor
+    qp, sp, qTp, sTp, _ = _grouped_dual_padded(mxq, x, off)
+    assert np.array_equal(qp, oq)
+    assert np.array_equal(sp, _padded_row_scales(os_, off, t_pad))
+    assert np.array_equal(qTp, oqT) and np.array_equal(sTp, sT)
 
 
 def test_grouped_dual_quant_without_row_outputs_is_the_column_quant(mxq):
