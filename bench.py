@@ -998,6 +998,16 @@ def component_timings(wl, peaks):
     out["linear_saved_bytes"] = {"save": m.mxq_linear_saved_bytes(M, N, K, m.SAVE_QUANT),
                                  "recompute": m.mxq_linear_saved_bytes(M, N, K, m.RECOMPUTE)}
     del ctx, ws, qat_ws, wcache
+    # the MXFP4 QAT forward of the MoE layer (32 experts, 32768 routed rows)
+    E, T, Km, Nm = MOE["E"], MOE["T"], MOE["K"], MOE["N"]
+    for qi, tag in ((1, "w4a4"), (0, "w4a16")):
+        gq_bytes = m.mxq_qat_grouped_fwd_workspace_bytes(T, E, Nm, Km, qi)
+        gq_ws = u8(gq_bytes)
+        ms = time_rotating([lambda: m.mxq_qat_grouped_fwd(wl.xm, wl.wm, wl.off, E, T, Nm, Km, qi, 6.0, wl.ym, gq_ws,
+                                                          gq_bytes)], reps=5)
+        out[f"qat_grouped_fwd_{tag}_ms"] = round(ms, 4)
+        out[f"qat_grouped_fwd_{tag}_tflops"] = round(2 * T * Nm * Km / (ms / 1e3) / 1e12, 1)
+        del gq_ws
     torch.cuda.empty_cache()
     return out, entries
 

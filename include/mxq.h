@@ -245,6 +245,26 @@ mxq_status mxq_qat_linear_fwd(const void *x_bf16, const void *w_bf16, const void
                               float scale_factor, void *y_bf16, void *workspace,
                               size_t ws_bytes, mxq_stream_t stream);
 
+/* The MXFP4 QAT forward of an MoE expert layer ([AMCT] section 4.3 applies
+ * the fake-quant linear to each expert's matmul): for each group e of the
+ * routed rows (d_offsets as for mxq_grouped_gemm),
+ *   y[off[e]:off[e+1]] = Q(x[off[e]:off[e+1]]) Q(W_e)^T    (quantize_input = 1, W4A4)
+ *   y[off[e]:off[e+1]] = x[off[e]:off[e+1]] Q(W_e)^T       (quantize_input = 0, W4A16)
+ * with Q the MXFP4 quant-dequant of mxq_qdq_mxfp4 along K.  x bf16 [T x K],
+ * w bf16 [E x N x K] (expert e's weight is rows [e*N, (e+1)*N) of the
+ * stacked [E*N x K]), y bf16 [T x N], all DEVICE and 16-byte aligned.
+ * W4A4 holds both operands' MXFP4 values exactly as E4M3 codes under their
+ * E8M0 scales and runs the block-scaled grouped GEMM; W4A16 forms Q(W) in
+ * bf16 (exact) and runs the grouped GEMM on the bf16 tensor cores.  An empty
+ * group has no rows to write; T = 0 is a no-op.  N % 128 == 0, K % 32 == 0;
+ * workspace >= mxq_qat_grouped_fwd_workspace_bytes(T, E, N, K,
+ * quantize_input), 16-byte aligned.  Malformed offsets as for the grouped
+ * GEMM. */
+size_t mxq_qat_grouped_fwd_workspace_bytes(int64_t T, int E, int64_t N, int64_t K, int quantize_input);
+mxq_status mxq_qat_grouped_fwd(const void *x_bf16, const void *w_bf16, const int64_t *d_offsets, int E,
+                               int64_t T, int64_t N, int64_t K, int quantize_input, float scale_factor,
+                               void *y_bf16, void *workspace, size_t ws_bytes, mxq_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* Block-scaled MXFP8 GEMMs ([TT] MXFP8 mode; output in bf16, fp32 accumulate) */
 /* ------------------------------------------------------------------ */

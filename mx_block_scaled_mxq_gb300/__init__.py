@@ -31,7 +31,8 @@ __all__ = [
     "mxq_linear_workspace_bytes", "mxq_linear_fwd", "mxq_linear_bwd_dx", "mxq_linear_bwd_dw",
     "mxq_last_error_string", "mxq_poll_device_error", "mxq_linear_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "mxq_mxfp4_ste_forward", "mxq_mxfp4_ste_backward", "mxfp4_ste_forward", "mxfp4_ste_backward",
-    "mxq_qat_linear_workspace_bytes", "mxq_qat_linear_fwd", "qat_linear_fwd", "mxq_qdq_mxfp4_bf16",
+    "mxq_qat_linear_workspace_bytes", "mxq_qat_linear_fwd", "qat_linear_fwd",
+    "mxq_qat_grouped_fwd_workspace_bytes", "mxq_qat_grouped_fwd", "qat_grouped_fwd", "mxq_qdq_mxfp4_bf16",
     "mxq_linear_weight_cache_bytes", "mxq_linear_wq_ctx_bytes", "mxq_linear_quantize_weight", "mxq_linear_fwd_wq",
     "mxq_linear_bwd_dx_wq", "mxq_selftest_wait_timeout", "mxq_validate_group_offsets", "mxq_check_group_offsets",
 ]
@@ -67,6 +68,8 @@ _SIGNATURES = {
     "mxq_mxfp4_ste_backward": (_I32, [_P, _P, _I64, _I64, _P, _P]),
     "mxq_qat_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
     "mxq_qat_linear_fwd": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I32, _F32, _P, _P, _SZ, _P]),
+    "mxq_qat_grouped_fwd_workspace_bytes": (_SZ, [_I64, _I32, _I64, _I64, _I32]),
+    "mxq_qat_grouped_fwd": (_I32, [_P, _P, _P, _I32, _I64, _I64, _I64, _I32, _F32, _P, _P, _SZ, _P]),
     "mxq_gemm": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P]),
     "mxq_grouped_gemm": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I64, _P, _P]),
     "mxq_linear_ctx_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
@@ -339,6 +342,30 @@ def qat_linear_fwd(x: torch.Tensor, w: torch.Tensor, bias=None, quantize_input: 
     ws = _u8(ws_bytes, x.device)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     mxq_qat_linear_fwd(x, w, bias, M, N, K, int(quantize_input), scale_factor, y, ws, ws_bytes, stream)
+    return y
+
+
+def mxq_qat_grouped_fwd_workspace_bytes(T, E, N, K, quantize_input=1):
+    return load().mxq_qat_grouped_fwd_workspace_bytes(T, E, N, K, quantize_input)
+
+
+def mxq_qat_grouped_fwd(x, w, d_offsets, E, T, N, K, quantize_input, scale_factor, y, workspace, ws_bytes,
+                        stream=None):
+    _check(load().mxq_qat_grouped_fwd(_p(x), _p(w), _p(d_offsets), E, T, N, K, quantize_input, scale_factor, _p(y),
+                                      _p(workspace), ws_bytes, _s(stream)), "mxq_qat_grouped_fwd")
+
+
+def qat_grouped_fwd(x: torch.Tensor, w: torch.Tensor, d_offsets: torch.Tensor, quantize_input: bool = True,
+                    scale_factor: float = 6.0, stream=None) -> torch.Tensor:
+    """MXFP4 QAT forward of an MoE expert layer: x bf16 [T x K] routed rows,
+    w bf16 [E x N x K], d_offsets int64 [E+1] on the device: returns bf16
+    [T x N]."""
+    T, K = x.shape
+    E, N = w.shape[0], w.shape[1]
+    ws_bytes = mxq_qat_grouped_fwd_workspace_bytes(T, E, N, K, int(quantize_input))
+    ws = _u8(max(ws_bytes, 1), x.device)
+    y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    mxq_qat_grouped_fwd(x, w, d_offsets, E, T, N, K, int(quantize_input), scale_factor, y, ws, ws_bytes, stream)
     return y
 
 

@@ -641,4 +641,67 @@ mxq_status mxq_qat_linear_fwd(const void *x, const void *w, const void *bias, in
     return dense_gemm(xq, wq, M, N, K, y, N, st, bias);
 }
 
+size_t mxq_qat_grouped_fwd_workspace_bytes(int64_t T, int E, int64_t N, int64_t K, int quantize_input) {
+    if (T < 0 || E <= 0 || N <= 0 || K <= 0) return 0;
+    const int64_t wrows = static_cast<int64_t>(E) * N;
+    return quantize_input ? (T > 0 ? operand_bytes(T, K) : 0) + operand_bytes(wrows, K)
+                          : round256(2 * static_cast<size_t>(wrows) * static_cast<size_t>(K));
+}
+
+mxq_status mxq_qat_grouped_fwd(const void *x, const void *w, const int64_t *d_offsets, int E, int64_t T, int64_t N,
+                               int64_t K, int quantize_input, float scale_factor, void *y, void *workspace,
+                               size_t ws_bytes, mxq_stream_t stream) {
+    if (E < 1 || E > 4096) return fail(MXQ_ERR_INVALID_ARG, "E must be in [1, 4096]");
+    if (T < 0 || N <= 0 || K <= 0 || N % 128 || K % 32)
+        return fail(MXQ_ERR_INVALID_ARG, "T >= 0, N a positive multiple of 128, K of 32 (got %lld, %lld, %lld)",
+                    (long long)T, (long long)N, (long long)K);
+    if (!(scale_factor > 0.0f) || !(scale_factor <= 3.402823466e38f))
+        return fail(MXQ_ERR_INVALID_ARG, "scale_factor must be finite and > 0");
+    if (K > (1ll << 31) || T > (1ll << 31) || static_cast<int64_t>(E) * N > (1ll << 31))
+        return fail(MXQ_ERR_UNSUPPORTED, "dimension above 2^31");
+    if (!w || !al16(w) || (T > 0 && (!x || !y || !al16(x) || !al16(y))))
+        return fail(MXQ_ERR_INVALID_ARG, "tensor pointers must be non-null and 16-byte aligned");
+    if (!d_offsets || (reinterpret_cast<uintptr_t>(d_offsets) & 7))
+        return fail(MXQ_ERR_INVALID_ARG, "d_offsets must be a non-null 8-byte aligned device pointer");
+    const size_t need = mxq_qat_grouped_fwd_workspace_bytes(T, E, N, K, quantize_input);
+    if (!workspace || !al16(workspace) || ws_bytes < need)
+        return fail(MXQ_ERR_INVALID_ARG, "workspace too small or unaligned: need %zu bytes, got %zu", need,
+                    workspace ? ws_bytes : 0);
+    if (T == 0) return ok();
+    mxq_status s = check_arch();
+    if (s != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t wrows = static_cast<int64_t>(E) * N;
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    mxq::GemmProblem g{};
+    g.mode = mxq::kGroupedRows;
+    g.offsets = d_offsets; g.E = E; g.T = T;
+    g.M = T; g.N = N; g.ldc = N; g.K = K;
+    g.a_rows = T; g.a_k = K;
+    g.b_rows = wrows; g.b_k = K;
+    g.b_row_per_expert = N; g.b_k_per_expert = 0;
+    g.c = y;
+    if (!quantize_input) {
+        // W4A16: Q(W_e) in bf16 (exact), then the bf16 grouped tensor-core product
+        uint16_t *qw = reinterpret_cast<uint16_t *>(wp);
+        cudaError_t e = mxq::launch_qdq_mxfp4_bf16(static_cast<const uint16_t *>(w), qw, wrows, K, scale_factor, st);
+        if (e != cudaSuccess) return cuda_result(e, "mxq_qat_grouped_fwd quant launch");
+        g.kind = mxq::kBF16;
+        g.a = static_cast<const uint8_t *>(x);
+        g.b = reinterpret_cast<const uint8_t *>(qw);
+        return cuda_result(mxq::launch_gemm(g, st), "mxq_qat_grouped_fwd gemm launch");
+    }
+    // W4A4: both operands' MXFP4 quant-dequant held exactly as E4M3 codes under
+    // their E8M0 scales (rows of x are independent, so one row quant of all T
+    // rows serves every group), then the block-scaled grouped product
+    const Operand xq = carve(wp, T, K), wq = carve(wp, wrows, K);
+    cudaError_t e = mxq::launch_quant_rows(x, false, 2, T, K, K, xq.q, xq.s, st, scale_factor);
+    if (e == cudaSuccess) e = mxq::launch_quant_rows(w, false, 2, wrows, K, K, wq.q, wq.s, st, scale_factor);
+    if (e != cudaSuccess) return cuda_result(e, "mxq_qat_grouped_fwd quant launch");
+    g.kind = mxq::kMXF8;
+    g.a = xq.q; g.sa = xq.s;
+    g.b = wq.q; g.sb = wq.s;
+    return cuda_result(mxq::launch_gemm(g, st), "mxq_qat_grouped_fwd gemm launch");
+}
+
 }  // extern "C"

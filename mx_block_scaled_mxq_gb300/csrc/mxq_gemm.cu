@@ -1249,7 +1249,9 @@ cudaError_t launch_gemm(const GemmProblem &g, cudaStream_t st) {
     // bias (dense only) is a separate instance: a per-chunk test in the
     // epilogue measurably slows the launches that have none
     if (g.kind == kBF16) {
-        if (g.mode != kDense) return cudaErrorInvalidValue;
+        // dense, or the grouped forward (experts' B rows stacked; no contraction offsets)
+        if (g.mode == kGroupedK || (g.mode == kGroupedRows && (g.b_k_per_expert != 0 || p.a_row_pad || p.bias)))
+            return cudaErrorInvalidValue;
         return p.bias ? launch_cg<1, kBF16, true>(g, p, st) : launch_cg<1, kBF16, false>(g, p, st);
     }
     if (p.bias) return launch_cg<1, kMXF8, true>(g, p, st);

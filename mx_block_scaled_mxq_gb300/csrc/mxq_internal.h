@@ -33,7 +33,8 @@ cudaError_t launch_ste_backward(const float *gy, const uint32_t *mask, float *gx
 // ---- GEMM (mxq_gemm.cu) ----
 enum GemmMode { kDense = 0, kGroupedRows = 1, kGroupedK = 2 };
 // Operand kind: kMXF8 = E4M3 codes with E8M0 block scales (all modes);
-// kBF16 = plain bf16 operands, no scales (kDense only).
+// kBF16 = plain bf16 operands, no scales (kDense, and kGroupedRows without
+// contraction offsets: the grouped forward).
 enum GemmKind { kMXF8 = 0, kBF16 = 1 };
 
 struct GemmProblem {

@@ -128,6 +128,14 @@ def test_host_validation_rejects_before_launch(lib):
     assert _status(m.mxq_grouped_gemm, m.GG_FWD, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 128, 64, 200, FAKE, 0) == INV
     assert "t_pad" in m.mxq_last_error_string()
     assert _status(m.mxq_grouped_gemm, m.GG_DX, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, 128, 64, -128, FAKE, 0) == INV
+    # grouped QAT forward: N multiple of 128, finite positive scale factor, workspace size
+    ws = m.mxq_qat_grouped_fwd_workspace_bytes(100, 4, 128, 64, 1)
+    assert ws > 0 and m.mxq_qat_grouped_fwd_workspace_bytes(100, 4, 128, 64, 0) == 2 * 4 * 128 * 64
+    assert _status(m.mxq_qat_grouped_fwd, FAKE, FAKE, FAKE, 4, 100, 96, 64, 1, 6.0, FAKE, FAKE, ws, 0) == INV
+    assert _status(m.mxq_qat_grouped_fwd, FAKE, FAKE, FAKE, 4, 100, 128, 64, 1, 0.0, FAKE, FAKE, ws, 0) == INV
+    assert _status(m.mxq_qat_grouped_fwd, FAKE, FAKE, FAKE, 4, 100, 128, 64, 1, 6.0, FAKE, FAKE, ws - 1, 0) == INV
+    assert "workspace" in m.mxq_last_error_string()
+    assert _status(m.mxq_qat_grouped_fwd, None, FAKE, FAKE, 4, 0, 128, 64, 1, 6.0, None, FAKE, ws, 0) == 0
     # linear: dimensions multiple of 32, workspace large enough
     assert _status(m.mxq_linear_fwd, FAKE, FAKE, 100, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 1 << 30, 0) == INV
     assert _status(m.mxq_linear_fwd, FAKE, FAKE, 64, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 16, 0) == INV

@@ -179,3 +179,83 @@ def test_bf16_qdq_every_bf16_pattern_under_six_scales(mxq):
     y = mxq.qdq_mxfp4(xb.to(DEV), 6.0).cpu()
     ref = oracle.mxfp4_qdq(a, np.float32(6.0))
     assert np.array_equal(y.view(torch.int16).numpy(), torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy())
+
+
+# ------------------------------------------------------------------ MoE experts
+
+def _grouped_ref(x, w, off, quantize_input, sf=6.0):
+    """The oracle's QAT forward applied to each group's rows and its expert's
+    weight (rows of x are independent, so this is the layer's definition)."""
+    T, N = x.shape[0], w.shape[1]
+    ref = np.zeros((T, N))
+    for e in range(len(off) - 1):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 > r0:
+            ref[r0:r1] = oracle.qat_linear_ref(x[r0:r1], w[e], None, scale_factor=sf, quantize_input=quantize_input)
+    return ref
+
+
+def _grouped_run(mxq, x, w, off, quantize_input, sf=6.0):
+    d_off = torch.from_numpy(np.asarray(off, dtype=np.int64)).to(DEV)
+    y = mxq.qat_grouped_fwd(x.to(DEV), w.to(DEV), d_off, quantize_input=quantize_input, scale_factor=sf)
+    torch.cuda.synchronize()
+    assert mxq.mxq_poll_device_error() == 0
+    return y
+
+
+@pytest.mark.parametrize("quantize_input", [True, False])
+@pytest.mark.parametrize("sizes,N,K", [([3, 0, 200, 0, 97], 256, 128), ([128, 128], 384, 96), ([0, 0, 1], 128, 512)])
+def test_grouped_exact_sums_bit_exact(mxq, quantize_input, sizes, N, K):
+    """Each expert's rows against its own weight, operands chosen so that
+    every partial sum is exact in fp32 (W on the MXFP4 grid; x on the grid for
+    W4A4, on a 2^-4 grid for W4A16): y = bf16(exact), empty groups included."""
+    off = mxq_inputs.offsets_from_sizes(sizes)
+    T, E = int(off[-1]), len(sizes)
+    if quantize_input:
+        x = _on_grid(T, K, 11)
+    else:
+        x = np.random.default_rng(T + K).integers(-128, 129, size=(T, K)) / 16.0
+    w = np.stack([_on_grid(N, K, 20 + e) for e in range(E)])
+    y = _grouped_run(mxq, _bf16(x), _bf16(w), off, quantize_input)
+    ref = _grouped_ref(_bf16(x), _bf16(w), off, quantize_input)
+    exact = np.zeros((T, N))
+    for e in range(E):
+        exact[off[e]:off[e + 1]] = x[off[e]:off[e + 1]] @ w[e].T
+    assert np.array_equal(ref, exact)
+    assert np.array_equal(y.cpu().view(torch.int16).numpy(), _rne_bits(ref))
+
+
+@pytest.mark.parametrize("quantize_input", [True, False])
+@pytest.mark.parametrize("sf", [6.0, 7.5])
+def test_grouped_random_within_tolerance(mxq, quantize_input, sf):
+    sizes = [37, 0, 300, 129, 0, 1, 211]
+    off, x, w, _ = mxq_inputs.moe_inputs(len(sizes), sum(sizes), 256, 384, seed=17, sizes=sizes)
+    y = _grouped_run(mxq, x, w, off, quantize_input, sf)
+    check_close(y, _grouped_ref(x, w, off, quantize_input, sf))
+
+
+def test_grouped_many_experts(mxq):
+    """300 experts, more than the GEMM's shared-memory group tables hold."""
+    E, T, K, N = 300, 1200, 64, 128
+    sizes = mxq_inputs.dirichlet_group_sizes(E, T, alpha=0.5, seed=3)
+    off, x, w, _ = mxq_inputs.moe_inputs(E, T, K, N, seed=5, sizes=sizes)
+    for qi in (True, False):
+        check_close(_grouped_run(mxq, x, w, off, qi), _grouped_ref(x, w, off, qi))
+
+
+def test_grouped_full_size_sampled_rows(mxq):
+    """The MoE layer's shape (32 experts, 32768 Dirichlet-routed rows,
+    K = 7168, N = 4096), both modes, on sampled rows of six experts."""
+    E, T, K, N = 32, 32768, 7168, 4096
+    off, x, w, _ = mxq_inputs.moe_inputs(E, T, K, N, seed=0, need_dy=False)
+    n = np.diff(off)
+    rng = np.random.default_rng(4)
+    experts = rng.choice(np.nonzero(n > 0)[0], 6, replace=False)
+    for qi in (True, False):
+        y = _grouped_run(mxq, x, w, off, qi)
+        for e in experts:
+            r0, r1 = int(off[e]), int(off[e + 1])
+            rows = np.unique(np.concatenate([[r0, r1 - 1], rng.integers(r0, r1, size=6)]))
+            ref = oracle.qat_linear_ref(x[torch.from_numpy(rows)], w[int(e)], None, quantize_input=qi)
+            check_close(y[torch.from_numpy(rows).to(DEV)], ref)
+        del y
