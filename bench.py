@@ -52,8 +52,8 @@ GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f
 # same full-size launches in the parity tests, keyed by a hash of the kernel
 # source; when the source has changed since, traffic is null.
 GEMM_DRAM_TRAFFIC = {
-    "ed54a1d37fde4372": {"linear_dw_gemm": 262502144, "moe_fwd_gemm": 1502192128,
-                         "moe_dx_gemm": 1534883584, "moe_dw_gemm": 2236919040},
+    "7cc3faf3066712ef": {"linear_dw_gemm": 260606464, "moe_fwd_gemm": 1495538432,
+                         "moe_dx_gemm": 1533581568, "moe_dw_gemm": 2236005888},
 }
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
