@@ -998,8 +998,24 @@ def component_timings(wl, peaks):
     out["linear_saved_bytes"] = {"save": m.mxq_linear_saved_bytes(M, N, K, m.SAVE_QUANT),
                                  "recompute": m.mxq_linear_saved_bytes(M, N, K, m.RECOMPUTE)}
     del ctx, ws, qat_ws, wcache
-    # the MXFP4 QAT forward of the MoE layer (32 experts, 32768 routed rows)
+    # the MoE layer through its orchestration entry points, both modes
     E, T, Km, Nm = MOE["E"], MOE["T"], MOE["K"], MOE["N"]
+    for gmode, tag in ((m.SAVE_QUANT, "save"), (m.RECOMPUTE, "recompute")):
+        gctx = u8(m.mxq_grouped_linear_ctx_bytes(T, E, Nm, Km, gmode))
+        gwsb = m.mxq_grouped_linear_workspace_bytes(T, E, Nm, Km, gmode)
+        gws = u8(gwsb)
+
+        def moe_layer(gmode=gmode, gctx=gctx, gws=gws, gwsb=gwsb):
+            m.mxq_grouped_linear_fwd(wl.xm, wl.wm, wl.off, E, T, Nm, Km, gmode, gctx, wl.ym, gws, gwsb)
+            m.mxq_grouped_linear_bwd_dx(wl.dym, wl.wm, wl.off, E, T, Nm, Km, gmode, gctx, wl.dxm, gws, gwsb)
+            m.mxq_grouped_linear_bwd_dw(wl.dym, wl.xm, wl.off, E, T, Nm, Km, gmode, gctx, wl.dwm, gws, gwsb)
+        ms = time_rotating([moe_layer], reps=3)
+        out[f"moe_layer_{tag}_ms"] = round(ms, 4)
+        out[f"moe_layer_{tag}_tflops"] = round(3 * 2 * T * Nm * Km / (ms / 1e3) / 1e12, 1)
+        del gctx, gws
+    out["moe_layer_saved_bytes"] = {"save": m.mxq_grouped_linear_saved_bytes(T, E, Nm, Km, m.SAVE_QUANT),
+                                    "recompute": m.mxq_grouped_linear_saved_bytes(T, E, Nm, Km, m.RECOMPUTE)}
+    # the MXFP4 QAT forward of the MoE layer (32 experts, 32768 routed rows)
     for qi, tag in ((1, "w4a4"), (0, "w4a16")):
         gq_bytes = m.mxq_qat_grouped_fwd_workspace_bytes(T, E, Nm, Km, qi)
         gq_ws = u8(gq_bytes)

@@ -340,6 +340,44 @@ mxq_status mxq_linear_bwd_dw(const void *dy, const void *x, int64_t M, int64_t N
                              mxq_mode mode, void *ctx, void *dw, void *workspace, size_t ws_bytes,
                              mxq_stream_t stream);
 
+/* ---- MoE expert layer, the same two modes ([TT] MoE MXFP8 mode; [FB]'s
+ * weights are the experts' [E,K,N], so its forward weight quant along axis
+ * -2 and its dX recompute along axis -1 are our row and column quants of the
+ * stacked [E*N x K]).  x bf16 [T x K] routed rows grouped by d_offsets
+ * (DEVICE, E+1, as for mxq_grouped_gemm), w bf16 [E x N x K] (expert e's
+ * weight is rows [e*N, (e+1)*N) of the stacked [E*N x K]), dy bf16 [T x N];
+ * y [T x N], dx [T x K], dw [E x N x K] bf16.  For group e:
+ *   y_e = X_e W_e^T,  dX_e = dY_e W_e,  dW_e = dY_e^T X_e (zero for an empty group),
+ * all MXFP8 with fp32 accumulation (the grouped GEMM kinds FWD, DX, DW).
+ *  MXQ_SAVE_QUANT: the forward quantizes X (row quant and per-group column
+ *      quant from one read) and W (row and column quant from one read) and
+ *      keeps the column quants in ctx for the backward.
+ *  MXQ_RECOMPUTE: the forward row-quantizes only and keeps nothing; the
+ *      backward re-quantizes W along E*N and X per group from the bf16
+ *      originals.
+ * In both, bwd_dx quantizes dY once (row quant and per-group column quant)
+ * and leaves the column quant in ctx for bwd_dw.  The two modes give
+ * bitwise-identical y, dx and dw.  T > 0, 1 <= E <= 4096, N a positive
+ * multiple of 128, K of 32; ctx (mxq_grouped_linear_ctx_bytes) carries state
+ * from fwd to bwd_dx to bwd_dw of one step; workspace
+ * (mxq_grouped_linear_workspace_bytes) is scratch for one call; all DEVICE,
+ * 16-byte aligned.  Malformed offsets as for mxq_grouped_gemm. */
+size_t mxq_grouped_linear_ctx_bytes(int64_t T, int E, int64_t N, int64_t K, mxq_mode mode);
+/* Bytes of ctx that live from the forward to the backward: the column quants
+ * of X (per group, [K x t_pad]) and of W ([K x E*N]) with their scales for
+ * SAVE, 0 for RECOMPUTE. */
+size_t mxq_grouped_linear_saved_bytes(int64_t T, int E, int64_t N, int64_t K, mxq_mode mode);
+size_t mxq_grouped_linear_workspace_bytes(int64_t T, int E, int64_t N, int64_t K, mxq_mode mode);
+mxq_status mxq_grouped_linear_fwd(const void *x, const void *w, const int64_t *d_offsets, int E,
+                                  int64_t T, int64_t N, int64_t K, mxq_mode mode, void *ctx, void *y,
+                                  void *workspace, size_t ws_bytes, mxq_stream_t stream);
+mxq_status mxq_grouped_linear_bwd_dx(const void *dy, const void *w, const int64_t *d_offsets, int E,
+                                     int64_t T, int64_t N, int64_t K, mxq_mode mode, void *ctx, void *dx,
+                                     void *workspace, size_t ws_bytes, mxq_stream_t stream);
+mxq_status mxq_grouped_linear_bwd_dw(const void *dy, const void *x, const int64_t *d_offsets, int E,
+                                     int64_t T, int64_t N, int64_t K, mxq_mode mode, void *ctx, void *dw,
+                                     void *workspace, size_t ws_bytes, mxq_stream_t stream);
+
 /* ---- Quantized-weight reuse ([FB]: the reuse flags of the MXFP8 matmul
  * path) ----
  * Within one optimizer step W does not change, so its quantization can be

@@ -32,7 +32,9 @@ __all__ = [
     "mxq_last_error_string", "mxq_poll_device_error", "mxq_linear_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "mxq_mxfp4_ste_forward", "mxq_mxfp4_ste_backward", "mxfp4_ste_forward", "mxfp4_ste_backward",
     "mxq_qat_linear_workspace_bytes", "mxq_qat_linear_fwd", "qat_linear_fwd",
-    "mxq_qat_grouped_fwd_workspace_bytes", "mxq_qat_grouped_fwd", "qat_grouped_fwd", "mxq_qdq_mxfp4_bf16",
+    "mxq_qat_grouped_fwd_workspace_bytes", "mxq_qat_grouped_fwd", "qat_grouped_fwd",
+    "mxq_grouped_linear_ctx_bytes", "mxq_grouped_linear_saved_bytes", "mxq_grouped_linear_workspace_bytes",
+    "mxq_grouped_linear_fwd", "mxq_grouped_linear_bwd_dx", "mxq_grouped_linear_bwd_dw", "mxq_qdq_mxfp4_bf16",
     "mxq_linear_weight_cache_bytes", "mxq_linear_wq_ctx_bytes", "mxq_linear_quantize_weight", "mxq_linear_fwd_wq",
     "mxq_linear_bwd_dx_wq", "mxq_selftest_wait_timeout", "mxq_validate_group_offsets", "mxq_check_group_offsets",
 ]
@@ -69,6 +71,12 @@ _SIGNATURES = {
     "mxq_qat_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32]),
     "mxq_qat_linear_fwd": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I32, _F32, _P, _P, _SZ, _P]),
     "mxq_qat_grouped_fwd_workspace_bytes": (_SZ, [_I64, _I32, _I64, _I64, _I32]),
+    "mxq_grouped_linear_ctx_bytes": (_SZ, [_I64, _I32, _I64, _I64, _I32]),
+    "mxq_grouped_linear_saved_bytes": (_SZ, [_I64, _I32, _I64, _I64, _I32]),
+    "mxq_grouped_linear_workspace_bytes": (_SZ, [_I64, _I32, _I64, _I64, _I32]),
+    "mxq_grouped_linear_fwd": (_I32, [_P, _P, _P, _I32, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
+    "mxq_grouped_linear_bwd_dx": (_I32, [_P, _P, _P, _I32, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
+    "mxq_grouped_linear_bwd_dw": (_I32, [_P, _P, _P, _I32, _I64, _I64, _I64, _I32, _P, _P, _P, _SZ, _P]),
     "mxq_qat_grouped_fwd": (_I32, [_P, _P, _P, _I32, _I64, _I64, _I64, _I32, _F32, _P, _P, _SZ, _P]),
     "mxq_gemm": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P]),
     "mxq_grouped_gemm": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I64, _I64, _P, _P]),
@@ -343,6 +351,33 @@ def qat_linear_fwd(x: torch.Tensor, w: torch.Tensor, bias=None, quantize_input: 
     y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     mxq_qat_linear_fwd(x, w, bias, M, N, K, int(quantize_input), scale_factor, y, ws, ws_bytes, stream)
     return y
+
+
+def mxq_grouped_linear_ctx_bytes(T, E, N, K, mode):
+    return load().mxq_grouped_linear_ctx_bytes(T, E, N, K, mode)
+
+
+def mxq_grouped_linear_saved_bytes(T, E, N, K, mode):
+    return load().mxq_grouped_linear_saved_bytes(T, E, N, K, mode)
+
+
+def mxq_grouped_linear_workspace_bytes(T, E, N, K, mode):
+    return load().mxq_grouped_linear_workspace_bytes(T, E, N, K, mode)
+
+
+def mxq_grouped_linear_fwd(x, w, d_offsets, E, T, N, K, mode, ctx, y, workspace, ws_bytes, stream=None):
+    _check(load().mxq_grouped_linear_fwd(_p(x), _p(w), _p(d_offsets), E, T, N, K, mode, _p(ctx), _p(y),
+                                         _p(workspace), ws_bytes, _s(stream)), "mxq_grouped_linear_fwd")
+
+
+def mxq_grouped_linear_bwd_dx(dy, w, d_offsets, E, T, N, K, mode, ctx, dx, workspace, ws_bytes, stream=None):
+    _check(load().mxq_grouped_linear_bwd_dx(_p(dy), _p(w), _p(d_offsets), E, T, N, K, mode, _p(ctx), _p(dx),
+                                            _p(workspace), ws_bytes, _s(stream)), "mxq_grouped_linear_bwd_dx")
+
+
+def mxq_grouped_linear_bwd_dw(dy, x, d_offsets, E, T, N, K, mode, ctx, dw, workspace, ws_bytes, stream=None):
+    _check(load().mxq_grouped_linear_bwd_dw(_p(dy), _p(x), _p(d_offsets), E, T, N, K, mode, _p(ctx), _p(dw),
+                                            _p(workspace), ws_bytes, _s(stream)), "mxq_grouped_linear_bwd_dw")
 
 
 def mxq_qat_grouped_fwd_workspace_bytes(T, E, N, K, quantize_input=1):

@@ -113,6 +113,101 @@ size_t ws_dw(int64_t M, int64_t N, int64_t K, mxq_mode mode) {
     return mode == MXQ_RECOMPUTE ? operand_bytes(K, M) : 0;
 }
 
+// ---- grouped (MoE expert) linear-layer memory plan ----
+// x [T x K] routed rows grouped by the offsets, the stacked expert weights
+// w [E*N x K], dy [T x N]; t_pad = mxq_grouped_padded_rows(T, E); gcolT = the
+// per-group column quant [C x t_pad]; prow = a row quant whose scales are in
+// the per-group padded layout ([T x C] codes, swz(t_pad, C/32) scales).
+// ctx:  SAVE: [gcolT(X): K x t_pad][gcolT(dY): N x t_pad][colT(W): K x E*N];  RECOMPUTE: [gcolT(dY)]
+// ws :  fwd [prow(X)][row(W)];  bwd_dx [prow(dY)][colT(W) if RECOMPUTE];  bwd_dw [gcolT(X) if RECOMPUTE]
+inline size_t prow_bytes(int64_t T, int64_t t_pad, int64_t k) {
+    return round256(static_cast<size_t>(T) * static_cast<size_t>(k)) + round256(scale_bytes(t_pad, ceil_div(k, 32)));
+}
+inline Operand carve_prow(uint8_t *&p, int64_t T, int64_t t_pad, int64_t k) {
+    Operand o;
+    o.q = p;
+    p += round256(static_cast<size_t>(T) * static_cast<size_t>(k));
+    o.s = p;
+    p += round256(scale_bytes(t_pad, ceil_div(k, 32)));
+    return o;
+}
+size_t g_saved_bytes(int64_t T, int E, int64_t N, int64_t K, mxq_mode mode) {
+    const int64_t tp = mxq_grouped_padded_rows(T, E);
+    return mode == MXQ_SAVE_QUANT ? operand_bytes(K, tp) + operand_bytes(K, static_cast<int64_t>(E) * N) : 0;
+}
+size_t g_ctx_bytes(int64_t T, int E, int64_t N, int64_t K, mxq_mode mode) {
+    return g_saved_bytes(T, E, N, K, mode) + operand_bytes(N, mxq_grouped_padded_rows(T, E));
+}
+size_t g_ws_fwd(int64_t T, int E, int64_t N, int64_t K) {
+    return prow_bytes(T, mxq_grouped_padded_rows(T, E), K) + operand_bytes(static_cast<int64_t>(E) * N, K);
+}
+size_t g_ws_dx(int64_t T, int E, int64_t N, int64_t K, mxq_mode mode) {
+    return prow_bytes(T, mxq_grouped_padded_rows(T, E), N) +
+           (mode == MXQ_RECOMPUTE ? operand_bytes(K, static_cast<int64_t>(E) * N) : 0);
+}
+size_t g_ws_dw(int64_t T, int E, int64_t N, int64_t K, mxq_mode mode) {
+    return mode == MXQ_RECOMPUTE ? operand_bytes(K, mxq_grouped_padded_rows(T, E)) : 0;
+}
+
+mxq_status check_grouped_linear(const void *a, const void *b, const int64_t *d_offsets, int E, int64_t T, int64_t N,
+                                int64_t K, mxq_mode mode, void *ctx, void *out, void *ws, size_t ws_bytes,
+                                size_t ws_need) {
+    if (!a || !b || !ctx || !out) return fail(MXQ_ERR_INVALID_ARG, "null tensor pointer");
+    if (!al16(a) || !al16(b) || !al16(ctx) || !al16(out) || (ws && !al16(ws)))
+        return fail(MXQ_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (!d_offsets || (reinterpret_cast<uintptr_t>(d_offsets) & 7))
+        return fail(MXQ_ERR_INVALID_ARG, "d_offsets must be a non-null 8-byte aligned device pointer");
+    if (mode != MXQ_SAVE_QUANT && mode != MXQ_RECOMPUTE) return fail(MXQ_ERR_INVALID_ARG, "bad mode %d", (int)mode);
+    if (E < 1 || E > 4096) return fail(MXQ_ERR_INVALID_ARG, "E must be in [1, 4096]");
+    if (T <= 0 || N <= 0 || K <= 0 || N % 128 || K % 32)
+        return fail(MXQ_ERR_INVALID_ARG, "T > 0, N a positive multiple of 128, K of 32 (got %lld, %lld, %lld)",
+                    (long long)T, (long long)N, (long long)K);
+    if (T > (1ll << 31) || K > (1ll << 31) || static_cast<int64_t>(E) * N > (1ll << 31) ||
+        mxq_grouped_padded_rows(T, E) / 128 > 65535)
+        return fail(MXQ_ERR_UNSUPPORTED, "dimension above the supported range");
+    if (ws_need > 0 && (!ws || ws_bytes < ws_need))
+        return fail(MXQ_ERR_INVALID_ARG, "workspace too small: need %zu bytes, got %zu", ws_need, ws ? ws_bytes : 0);
+    return MXQ_OK;
+}
+
+// The grouped GEMM problem of one MoE matmul (arguments already checked).
+//  FWD: out[T x N] rows of group e = A rows . B_e^T, A [T x K], B [E*N x K] (expert e's rows [eN, (e+1)N)).
+//  DX:  out[T x K] rows of group e = A rows . B_e^T, A [T x N], B = colT(W) [K x E*N] (expert e's columns).
+//  DW:  out[E x N x K], per-group contraction over the padded column quants [N x t_pad], [K x t_pad].
+//  t_pad for FWD/DX: 0 = A's scales swz(T, .), else the per-group padded layout swz(t_pad, .).
+mxq::GemmProblem grouped_problem(mxq_gg_kind kind, const uint8_t *a, const uint8_t *sa, const uint8_t *b,
+                                 const uint8_t *sb, const int64_t *d_offsets, int E, int64_t T, int64_t N, int64_t K,
+                                 int64_t t_pad, void *out_bf16) {
+    mxq::GemmProblem g{};
+    g.offsets = d_offsets;
+    g.E = E;
+    g.c = out_bf16;
+    g.T = T;
+    g.a = a; g.sa = sa; g.b = b; g.sb = sb;
+    if (kind == MXQ_GG_FWD || kind == MXQ_GG_DX) {
+        g.mode = mxq::kGroupedRows;
+        g.a_row_pad = t_pad;
+        if (kind == MXQ_GG_FWD) {  // out[T x N] = X[T x K] . W_e[N x K]^T
+            g.a_rows = T; g.a_k = K;
+            g.b_rows = static_cast<int64_t>(E) * N; g.b_k = K;
+            g.M = T; g.N = N; g.ldc = N; g.K = K;
+            g.b_row_per_expert = N; g.b_k_per_expert = 0;
+        } else {  // out[T x K] = dY[T x N] . colT(W)_e[K x N]^T
+            g.a_rows = T; g.a_k = N;
+            g.b_rows = K; g.b_k = static_cast<int64_t>(E) * N;
+            g.M = T; g.N = K; g.ldc = K; g.K = N;
+            g.b_row_per_expert = 0; g.b_k_per_expert = N;
+        }
+    } else {
+        g.mode = mxq::kGroupedK;
+        g.a_rows = N; g.a_k = t_pad;
+        g.b_rows = K; g.b_k = t_pad;
+        g.M = N; g.N = K; g.ldc = K;
+        g.c_expert_stride = N * K;
+    }
+    return g;
+}
+
 mxq_status check_linear(const void *a, const void *b, int64_t M, int64_t N, int64_t K, mxq_mode mode, void *ctx,
                         void *out, void *ws, size_t ws_bytes, size_t ws_need) {
     if (!a || !b || !ctx || !out) return fail(MXQ_ERR_INVALID_ARG, "null tensor pointer");
@@ -394,10 +489,6 @@ mxq_status mxq_grouped_gemm(mxq_gg_kind kind, const uint8_t *a, const uint8_t *s
         return fail(MXQ_ERR_INVALID_ARG, "d_offsets must be a non-null 8-byte aligned device pointer");
     if (!a || !sa || !b || !sb || !out_bf16 || !al16(a) || !al16(sa) || !al16(b) || !al16(sb) || !al16(out_bf16))
         return fail(MXQ_ERR_INVALID_ARG, "tensor pointers must be non-null and 16-byte aligned");
-    mxq::GemmProblem g{};
-    g.offsets = d_offsets;
-    g.E = E;
-    g.c = out_bf16;
     if (kind == MXQ_GG_FWD || kind == MXQ_GG_DX) {
         if (N % 128) return fail(MXQ_ERR_INVALID_ARG, "N must be a multiple of 128 for the grouped forward/dX");
         if (K % 32) return fail(MXQ_ERR_INVALID_ARG, "K must be a multiple of 32");
@@ -407,32 +498,12 @@ mxq_status mxq_grouped_gemm(mxq_gg_kind kind, const uint8_t *a, const uint8_t *s
                         (long long)mxq_grouped_padded_rows(T, E));
         if (t_pad > (1ll << 31)) return fail(MXQ_ERR_UNSUPPORTED, "t_pad above 2^31");
         if (T == 0) return ok();
-        g.mode = mxq::kGroupedRows;
-        g.T = T;
-        g.a_row_pad = t_pad;
-        g.a = a; g.sa = sa; g.b = b; g.sb = sb;
-        if (kind == MXQ_GG_FWD) {  // out[T x N] = X[T x K] . W_e[N x K]^T
-            g.a_rows = T; g.a_k = K;
-            g.b_rows = static_cast<int64_t>(E) * N; g.b_k = K;
-            g.M = T; g.N = N; g.ldc = N; g.K = K;
-            g.b_row_per_expert = N; g.b_k_per_expert = 0;
-        } else {  // out[T x K] = dY[T x N] . colT(W)_e[K x N]^T
-            g.a_rows = T; g.a_k = N;
-            g.b_rows = K; g.b_k = static_cast<int64_t>(E) * N;
-            g.M = T; g.N = K; g.ldc = K; g.K = N;
-            g.b_row_per_expert = 0; g.b_k_per_expert = N;
-        }
     } else {
         if (t_pad <= 0 || t_pad % 128 || t_pad < mxq_grouped_padded_rows(T, E))
             return fail(MXQ_ERR_INVALID_ARG, "t_pad must be a multiple of 128 and >= mxq_grouped_padded_rows(T, E)");
         if (t_pad > (1ll << 31)) return fail(MXQ_ERR_UNSUPPORTED, "t_pad above 2^31");
-        g.mode = mxq::kGroupedK;
-        g.T = T;
-        g.a = a; g.sa = sa; g.a_rows = N; g.a_k = t_pad;
-        g.b = b; g.sb = sb; g.b_rows = K; g.b_k = t_pad;
-        g.M = N; g.N = K; g.ldc = K;
-        g.c_expert_stride = N * K;
     }
+    const mxq::GemmProblem g = grouped_problem(kind, a, sa, b, sb, d_offsets, E, T, N, K, t_pad, out_bf16);
     mxq_status s = check_arch();
     if (s != MXQ_OK) return s;
     return cuda_result(mxq::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)), "mxq_grouped_gemm launch");
@@ -702,6 +773,111 @@ mxq_status mxq_qat_grouped_fwd(const void *x, const void *w, const int64_t *d_of
     g.a = xq.q; g.sa = xq.s;
     g.b = wq.q; g.sb = wq.s;
     return cuda_result(mxq::launch_gemm(g, st), "mxq_qat_grouped_fwd gemm launch");
+}
+
+
+// ---- grouped (MoE expert) linear layer, SAVE vs RECOMPUTE ----
+size_t mxq_grouped_linear_ctx_bytes(int64_t T, int E, int64_t N, int64_t K, mxq_mode mode) {
+    if (T <= 0 || E <= 0 || N <= 0 || K <= 0) return 0;
+    return g_ctx_bytes(T, E, N, K, mode);
+}
+size_t mxq_grouped_linear_saved_bytes(int64_t T, int E, int64_t N, int64_t K, mxq_mode mode) {
+    if (T <= 0 || E <= 0 || N <= 0 || K <= 0) return 0;
+    return g_saved_bytes(T, E, N, K, mode);
+}
+size_t mxq_grouped_linear_workspace_bytes(int64_t T, int E, int64_t N, int64_t K, mxq_mode mode) {
+    if (T <= 0 || E <= 0 || N <= 0 || K <= 0) return 0;
+    size_t w = g_ws_fwd(T, E, N, K);
+    if (g_ws_dx(T, E, N, K, mode) > w) w = g_ws_dx(T, E, N, K, mode);
+    if (g_ws_dw(T, E, N, K, mode) > w) w = g_ws_dw(T, E, N, K, mode);
+    return w;
+}
+
+mxq_status mxq_grouped_linear_fwd(const void *x, const void *w, const int64_t *d_offsets, int E, int64_t T, int64_t N,
+                                  int64_t K, mxq_mode mode, void *ctx, void *y, void *workspace, size_t ws_bytes,
+                                  mxq_stream_t stream) {
+    mxq_status s = check_grouped_linear(x, w, d_offsets, E, T, N, K, mode, ctx, y, workspace, ws_bytes,
+                                        g_ws_fwd(T, E, N, K));
+    if (s != MXQ_OK) return s;
+    if ((s = check_arch()) != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t tp = mxq_grouped_padded_rows(T, E), wrows = static_cast<int64_t>(E) * N;
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    const Operand xq = carve_prow(wp, T, tp, K), wq = carve(wp, wrows, K);
+    cudaError_t e;
+    int64_t a_pad = 0;
+    if (mode == MXQ_SAVE_QUANT) {
+        // X: row quant (padded row scales) and per-group column quant from one
+        // read; W: row quant and column quant along E*N from one read
+        uint8_t *cp = static_cast<uint8_t *>(ctx);
+        const Operand xT = carve(cp, K, tp);
+        (void)carve(cp, N, tp);  // gcolT(dY), written by bwd_dx
+        const Operand wT = carve(cp, K, wrows);
+        e = mxq::launch_quant_cols_grouped(static_cast<const uint16_t *>(x), T, K, d_offsets, E, tp, xq.q, xq.s, xT.q,
+                                           xT.s, st, true);
+        if (e == cudaSuccess)
+            e = mxq::launch_quant_cols(static_cast<const uint16_t *>(w), wrows, K, K, wq.q, wq.s, wT.q, wT.s, st);
+        a_pad = tp;
+    } else {
+        e = mxq::launch_quant_rows(x, false, 0, T, K, K, xq.q, xq.s, st);
+        if (e == cudaSuccess) e = mxq::launch_quant_rows(w, false, 0, wrows, K, K, wq.q, wq.s, st);
+    }
+    if (e != cudaSuccess) return cuda_result(e, "mxq_grouped_linear_fwd quant launch");
+    const mxq::GemmProblem g = grouped_problem(MXQ_GG_FWD, xq.q, xq.s, wq.q, wq.s, d_offsets, E, T, N, K, a_pad, y);
+    return cuda_result(mxq::launch_gemm(g, st), "mxq_grouped_linear_fwd gemm launch");
+}
+
+mxq_status mxq_grouped_linear_bwd_dx(const void *dy, const void *w, const int64_t *d_offsets, int E, int64_t T,
+                                     int64_t N, int64_t K, mxq_mode mode, void *ctx, void *dx, void *workspace,
+                                     size_t ws_bytes, mxq_stream_t stream) {
+    mxq_status s = check_grouped_linear(dy, w, d_offsets, E, T, N, K, mode, ctx, dx, workspace, ws_bytes,
+                                        g_ws_dx(T, E, N, K, mode));
+    if (s != MXQ_OK) return s;
+    if ((s = check_arch()) != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t tp = mxq_grouped_padded_rows(T, E), wrows = static_cast<int64_t>(E) * N;
+    uint8_t *cp = static_cast<uint8_t *>(ctx);
+    if (mode == MXQ_SAVE_QUANT) (void)carve(cp, K, tp);
+    const Operand dyT = carve(cp, N, tp);
+    Operand wT{};
+    if (mode == MXQ_SAVE_QUANT) wT = carve(cp, K, wrows);
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    const Operand dyq = carve_prow(wp, T, tp, N);
+    // dY: row quant (padded row scales, this call's A) and per-group column
+    // quant (bwd_dw's A, kept in ctx) from one read
+    cudaError_t e = mxq::launch_quant_cols_grouped(static_cast<const uint16_t *>(dy), T, N, d_offsets, E, tp, dyq.q,
+                                                   dyq.s, dyT.q, dyT.s, st, true);
+    if (e == cudaSuccess && mode == MXQ_RECOMPUTE) {
+        wT = carve(wp, K, wrows);
+        e = mxq::launch_quant_cols(static_cast<const uint16_t *>(w), wrows, K, K, nullptr, nullptr, wT.q, wT.s, st);
+    }
+    if (e != cudaSuccess) return cuda_result(e, "mxq_grouped_linear_bwd_dx quant launch");
+    const mxq::GemmProblem g = grouped_problem(MXQ_GG_DX, dyq.q, dyq.s, wT.q, wT.s, d_offsets, E, T, N, K, tp, dx);
+    return cuda_result(mxq::launch_gemm(g, st), "mxq_grouped_linear_bwd_dx gemm launch");
+}
+
+mxq_status mxq_grouped_linear_bwd_dw(const void *dy, const void *x, const int64_t *d_offsets, int E, int64_t T,
+                                     int64_t N, int64_t K, mxq_mode mode, void *ctx, void *dw, void *workspace,
+                                     size_t ws_bytes, mxq_stream_t stream) {
+    mxq_status s = check_grouped_linear(dy, x, d_offsets, E, T, N, K, mode, ctx, dw, workspace, ws_bytes,
+                                        g_ws_dw(T, E, N, K, mode));
+    if (s != MXQ_OK) return s;
+    if ((s = check_arch()) != MXQ_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t tp = mxq_grouped_padded_rows(T, E);
+    uint8_t *cp = static_cast<uint8_t *>(ctx);
+    Operand xT{};
+    if (mode == MXQ_SAVE_QUANT) xT = carve(cp, K, tp);
+    const Operand dyT = carve(cp, N, tp);
+    if (mode == MXQ_RECOMPUTE) {
+        uint8_t *wp = static_cast<uint8_t *>(workspace);
+        xT = carve(wp, K, tp);
+        const cudaError_t e = mxq::launch_quant_cols_grouped(static_cast<const uint16_t *>(x), T, K, d_offsets, E, tp,
+                                                             nullptr, nullptr, xT.q, xT.s, st, false);
+        if (e != cudaSuccess) return cuda_result(e, "mxq_grouped_linear_bwd_dw quant launch");
+    }
+    const mxq::GemmProblem g = grouped_problem(MXQ_GG_DW, dyT.q, dyT.s, xT.q, xT.s, d_offsets, E, T, N, K, tp, dw);
+    return cuda_result(mxq::launch_gemm(g, st), "mxq_grouped_linear_bwd_dw gemm launch");
 }
 
 }  // extern "C"

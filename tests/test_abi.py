@@ -136,6 +136,18 @@ def test_host_validation_rejects_before_launch(lib):
     assert _status(m.mxq_qat_grouped_fwd, FAKE, FAKE, FAKE, 4, 100, 128, 64, 1, 6.0, FAKE, FAKE, ws - 1, 0) == INV
     assert "workspace" in m.mxq_last_error_string()
     assert _status(m.mxq_qat_grouped_fwd, None, FAKE, FAKE, 4, 0, 128, 64, 1, 6.0, None, FAKE, ws, 0) == 0
+    # grouped linear layer: N multiple of 128, T > 0, mode, workspace
+    gws = m.mxq_grouped_linear_workspace_bytes(100, 4, 128, 64, m.RECOMPUTE)
+    assert gws >= m.mxq_grouped_linear_workspace_bytes(100, 4, 128, 64, m.SAVE_QUANT) > 0
+    assert _status(m.mxq_grouped_linear_fwd, FAKE, FAKE, FAKE, 4, 100, 96, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, gws,
+                   0) == INV
+    assert _status(m.mxq_grouped_linear_fwd, FAKE, FAKE, FAKE, 4, 0, 128, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, gws,
+                   0) == INV
+    assert _status(m.mxq_grouped_linear_bwd_dx, FAKE, FAKE, FAKE, 4, 100, 128, 64, 7, FAKE, FAKE, FAKE, gws, 0) == INV
+    assert _status(m.mxq_grouped_linear_bwd_dw, FAKE, FAKE, FAKE, 4, 100, 128, 64, m.RECOMPUTE, FAKE, FAKE, FAKE, 16,
+                   0) == INV
+    assert "workspace" in m.mxq_last_error_string()
+    assert m.mxq_grouped_linear_saved_bytes(100, 4, 128, 64, m.RECOMPUTE) == 0
     # linear: dimensions multiple of 32, workspace large enough
     assert _status(m.mxq_linear_fwd, FAKE, FAKE, 100, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 1 << 30, 0) == INV
     assert _status(m.mxq_linear_fwd, FAKE, FAKE, 64, 64, 64, m.SAVE_QUANT, FAKE, FAKE, FAKE, 16, 0) == INV

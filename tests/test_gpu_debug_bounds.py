@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_gpu_quant.py", "tests/test_gpu_gemm.py", "tests/test_gpu_grouped.py", "tests/test_gpu_ste.py",
           "tests/test_gpu_qat.py", "tests/test_gpu_linear.py", "tests/test_gpu_weight_reuse.py",
-          "tests/test_gpu_group_offsets.py"]
+          "tests/test_gpu_group_offsets.py", "tests/test_gpu_grouped_linear.py"]
 
 
 def test_parity_suites_pass_on_the_bounds_checking_build(mxq):
