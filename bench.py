@@ -716,8 +716,8 @@ def ncu_case(case: str):
       moe_small  the MoE layer's GEMMs (fwd, dX, dW) at E=8, T=8192, K=7168,
                  N=4096 (the bench's 1024 routed rows per expert on average);
       dualquant  the dual quant of the dense layer's dY (8192 x 14336) and the
-                 per-group dual quant of the MoE layer's dY (32768 x 4096, 32
-                 Dirichlet(0.5) groups)."""
+                 per-group dual quant, with per-group padded row scales, of the
+                 MoE layer's dY (32768 x 4096, 32 Dirichlet(0.5) groups)."""
     import mxq_inputs
     import mx_block_scaled_mxq_gb300 as m
     dev = torch.device("cuda", 0)
@@ -749,8 +749,8 @@ def ncu_case(case: str):
         off_d = torch.from_numpy(np.asarray(off, dtype=np.int64)).to(dev)
         dym = mxq_inputs.normal_bf16((T, Nm), 1e-3, seed=5).to(dev)
         tp = m.mxq_grouped_padded_rows(T, E)
-        m.mxq_quantize_grouped_dual(dym, T, Nm, off_d, E, tp, u8(T * Nm), u8(m.mxq_scale_bytes(T, Nm // 32)),
-                                    u8(Nm * tp), u8(m.mxq_scale_bytes(Nm, tp // 32)))
+        m.mxq_quantize_grouped_dual_padded(dym, T, Nm, off_d, E, tp, u8(T * Nm), u8(m.mxq_scale_bytes(tp, Nm // 32)),
+                                           u8(Nm * tp), u8(m.mxq_scale_bytes(Nm, tp // 32)))
     elif case == "dense":
         M, N, K = LIN["M"], LIN["N"], LIN["K"]
         x, w, _ = mxq_inputs.linear_inputs(M, N, K, seed=0)
