@@ -1,6 +1,7 @@
 // mxq_api.cu -- the C ABI of libmxq (declared in include/mxq.h): argument
 // validation, arch check, dispatch to the kernels, and the linear layer's
 // saved-quant / recompute orchestration.
+#include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -37,17 +38,19 @@ mxq_status check_arch() {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(MXQ_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    static int cc[kMaxDevices] = {0};  // major*10+minor, 0 = unknown
+    static std::atomic<int> cc[kMaxDevices] = {};  // major*10+minor, 0 = unknown (racing threads store the same value)
     if (dev < 0 || dev >= kMaxDevices) return fail(MXQ_ERR_CUDA, "device index %d out of range", dev);
-    if (cc[dev] == 0) {
+    int v = cc[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
             return fail(MXQ_ERR_CUDA, "cannot query compute capability of device %d", dev);
-        cc[dev] = major * 10 + minor;
+        v = major * 10 + minor;
+        cc[dev].store(v, std::memory_order_relaxed);
     }
-    if (cc[dev] != 103)
-        return fail(MXQ_ERR_ARCH, "libmxq is built for sm_103a (GB300); device %d is sm_%d", dev, cc[dev]);
+    if (v != 103)
+        return fail(MXQ_ERR_ARCH, "libmxq is built for sm_103a (GB300); device %d is sm_%d", dev, v);
     return MXQ_OK;
 }
 

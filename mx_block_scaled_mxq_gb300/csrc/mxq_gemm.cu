@@ -1077,13 +1077,6 @@ int cta_group_for(const GemmProblem &) {
 template <int CG, int KIND, bool BIAS>
 cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     using C = Cfg<CG>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(k_gemm<CG, KIND, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
-
     CUtensorMap tmA, tmB, tmSA, tmSB, tmC;
     const int64_t esz = KIND == kBF16 ? 2 : 1;  // operand bytes per element (tensor maps run over bytes)
     if (!make_tmap(&tmA, g.a, g.a_rows, esz * g.a_k, C::BM) ||
@@ -1113,7 +1106,10 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     if (p.total_tiles <= 0) return cudaSuccess;
 
     // persistent grid: as many CTAs (CTA pairs) as can be resident at once, one
-    // per SM (a CTA needs ~200 KB of shared memory)
+    // per SM (a CTA needs ~200 KB of shared memory).  Per device, once, under a
+    // lock (host threads may launch concurrently): the kernel's shared-memory
+    // attribute, which is a per-device setting, then the residency.
+    static std::mutex init_mu;
     static int resident[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1132,19 +1128,25 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    if (resident[dev] == 0) {
-        if (CG == 2) {
-            cfg.gridDim = dim3(2);
-            int clusters = 0;
-            e = cudaOccupancyMaxActiveClusters(&clusters, k_gemm<CG, KIND, BIAS>, &cfg);
+    int units_max = 0;
+    {
+        std::lock_guard<std::mutex> lock(init_mu);
+        if (resident[dev] == 0) {
+            e = cudaFuncSetAttribute(k_gemm<CG, KIND, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
             if (e != cudaSuccess) return e;
-            resident[dev] = clusters > 0 ? clusters : 1;
-        } else {
-            e = cudaDeviceGetAttribute(&resident[dev], cudaDevAttrMultiProcessorCount, dev);
+            int n = 0;
+            if (CG == 2) {
+                cfg.gridDim = dim3(2);
+                e = cudaOccupancyMaxActiveClusters(&n, k_gemm<CG, KIND, BIAS>, &cfg);
+            } else {
+                e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+            }
             if (e != cudaSuccess) return e;
+            resident[dev] = n > 0 ? n : 1;
         }
+        units_max = resident[dev];
     }
-    const int64_t units = p.total_tiles < resident[dev] ? p.total_tiles : resident[dev];
+    const int64_t units = p.total_tiles < units_max ? p.total_tiles : units_max;
     cfg.gridDim = dim3(static_cast<unsigned>(units * CG));
     return cudaLaunchKernelEx(&cfg, k_gemm<CG, KIND, BIAS>, tmA, tmB, tmSA, tmSB, tmC, p);
 }

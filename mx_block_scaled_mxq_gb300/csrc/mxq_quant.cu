@@ -16,6 +16,7 @@
 // read back as 32-bit column pairs (conflict-free).
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <mutex>
 
 #include "mxq_device.cuh"
 #include "mxq_internal.h"
@@ -1382,26 +1383,33 @@ bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cud
     cudaError_t e = device_error_word(&err);
     if (e != cudaSuccess) { *res = e; return true; }
     const int smem = QuantRing<GROUPED>::kSlots * static_cast<int>(kTileBytes);
-    static int per_sm[64] = {0}, sms[64] = {0};
+    // per device, once, under a lock (host threads may launch concurrently): the
+    // shared-memory attribute (a per-device setting) and the resident CTAs
+    static std::mutex init_mu;
+    static int64_t resident[64] = {0};
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) { *res = e; return true; }
     if (dev < 0 || dev >= 64) { *res = cudaErrorInvalidDevice; return true; }
-    if (per_sm[dev] == 0) {
-        if ((e = cudaFuncSetAttribute(k_quant_cols_tma<ROWS, GROUPED, COLS, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      smem)) != cudaSuccess ||
-            (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev], k_quant_cols_tma<ROWS, GROUPED, COLS, FMT>, kThreads,
-                                                               smem)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
-            per_sm[dev] = 0;
-            *res = e;
-            return true;
+    int64_t ctas = 0;
+    {
+        std::lock_guard<std::mutex> lock(init_mu);
+        if (resident[dev] == 0) {
+            int per_sm = 0, sms = 0;
+            if ((e = cudaFuncSetAttribute(k_quant_cols_tma<ROWS, GROUPED, COLS, FMT>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
+                (e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant_cols_tma<ROWS, GROUPED, COLS, FMT>,
+                                                                   kThreads, smem)) != cudaSuccess ||
+                (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+                *res = e;
+                return true;
+            }
+            resident[dev] = static_cast<int64_t>(per_sm < 1 ? 1 : per_sm) * (sms < 1 ? 1 : sms);
         }
-        if (per_sm[dev] < 1) per_sm[dev] = 1;
+        ctas = resident[dev];
     }
     const int64_t ct_tiles = (P.C + kTile - 1) / kTile;
     const int64_t n_tiles = row_tiles * ct_tiles;
-    const int64_t grid = n_tiles < static_cast<int64_t>(per_sm[dev]) * sms[dev] ? n_tiles
-                                                                                 : static_cast<int64_t>(per_sm[dev]) * sms[dev];
+    const int64_t grid = n_tiles < ctas ? n_tiles : ctas;
     k_quant_cols_tma<ROWS, GROUPED, COLS, FMT><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tm, P, n_tiles, ct_tiles, err);
     *res = cudaGetLastError();
     return true;
