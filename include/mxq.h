@@ -43,6 +43,14 @@
  *  - Errors: the return value; mxq_last_error_string() gives the reason
  *    (thread-local).  No exception crosses the ABI.  MXQ_ERR_ARCH when the
  *    current device is not compute capability 10.3.
+ *  - Host threads: entry points may be called from several host threads at
+ *    once, each on its own stream (mxq_linear_fwd_noalloc's shared scratch is
+ *    the exception; see there).  The first launch of each kernel on a device
+ *    does a one-time setup under a lock: its shared-memory attribute and its
+ *    resident-CTA count.  That setup, like every per-device value the library
+ *    keeps, belongs to the device's primary context.  After a
+ *    cudaDeviceReset, do not call the library on that device again in the
+ *    same process.
  */
 #ifndef MXQ_H
 #define MXQ_H
