@@ -95,3 +95,22 @@ def test_full_size_gemm_sampled_rows(mxq):
     wq_o, ws_o = oracle.mxfp8_quant_rows(w)
     ref = oracle.gemm_ref(oq, os_, wq_o, ws_o)
     check_close(c[torch.from_numpy(rows).to(DEV)], ref)
+
+
+@pytest.mark.parametrize("M,N,K,ldc", [(300, 384, 256, 448), (517, 1000, 96, 1008), (128, 256, 512, 4096),
+                                       (1, 8, 32, 16)])
+def test_strided_output(mxq, M, N, K, ldc):
+    """C written with a row pitch ldc > N: the [M x N] block equals the
+    exact product bit for bit, and the columns [N, ldc) keep their contents."""
+    rng = np.random.default_rng(M + N + K + ldc)
+    qa, la = _exact_operands(M, K, rng)
+    qb, lb = _exact_operands(N, K, rng)
+    big = torch.full((M, ldc), float("nan"), dtype=torch.bfloat16, device=DEV)
+    mxq.mxq_gemm(torch.from_numpy(qa).to(DEV), torch.from_numpy(oracle.swizzle_scales(la)).to(DEV),
+                 torch.from_numpy(qb).to(DEV), torch.from_numpy(oracle.swizzle_scales(lb)).to(DEV), M, N, K, big, ldc)
+    torch.cuda.synchronize()
+    assert mxq.mxq_poll_device_error() == 0
+    ref = oracle.gemm_ref(qa, la, qb, lb)
+    got = big.cpu().view(torch.int16).numpy()
+    assert np.array_equal(got[:, :N], _bf16_rne(ref))
+    assert torch.isnan(big[:, N:].float()).all()
