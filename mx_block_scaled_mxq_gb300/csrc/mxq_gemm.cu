@@ -100,6 +100,26 @@ struct Cfg {
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
+// Division of n < 2^31 by a divisor d fixed for the launch, by a multiply-high
+// and a shift (division by invariant integers using multiplication, Granlund
+// and Montgomery, 1994).  With l = ceil(log2 d) and m = ceil(2^(31+l) / d):
+// m < 2^32, and n * m / 2^(31+l) exceeds n / d by less than n * d / 2^(31+l)
+// < 1 / d, so its floor is floor(n / d) for every n < 2^31.  The tile decode
+// runs once per tile in three warps; a 64-bit division there costs hundreds of
+// cycles.
+struct FastDiv {
+    uint32_t d, m, s;  // divisor, multiplier, shift l - 1 (unused for d = 1)
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) l++;
+    const uint64_t m = ((1ull << (31 + l)) + d - 1) / d;
+    return FastDiv{d, static_cast<uint32_t>(m), l > 0 ? l - 1 : 0};
+}
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
+    return f.d == 1 ? n : __umulhi(n, f.m) >> f.s;
+}
+
 struct Params {
     GemmMode mode;
     const uint8_t *sa, *sb;
@@ -113,6 +133,8 @@ struct Params {
     int64_t a_row_pad;                 // kGroupedRows: A's scales in the per-group padded layout (t_pad rows), or 0
     int64_t b_row_per_expert, b_k_per_expert, c_expert_stride;
     int m_tiles, n_tiles;  // tile counts (m in units of 128 * CG rows)
+    FastDiv fd_m, fd_n, fd_mn;  // division by m_tiles, n_tiles, m_tiles * n_tiles
+    int64_t c_expert_rows;      // kGroupedK: output rows per expert (c_expert_stride / ldc)
     int n_fastest;         // kDense tile order: 1 = n fastest (A is the larger operand)
     int tma_store;         // an output tensor map exists: unmasked 32-row boxes are stored with TMA
     int vec_store;         // rows of C are 16-byte aligned (coalesced 16-byte stores)
@@ -126,6 +148,7 @@ struct TileInfo {
     int64_t a_row0, b_row0, a_k0, b_k0;   // this CTA's TMA coordinates of k-block 0
     int64_t a_ratom, b_ratom, a_katom0, b_katom0;
     int64_t row_lo, row_hi, out_row0, col0, col_hi, c_off;
+    int64_t c_row0;  // first row of this expert's output block in the stacked output (kGroupedK), else 0
 };
 
 // Instruction descriptors, both operands K-major, N = 256, M = 128 * CG.
@@ -235,7 +258,8 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
         const int64_t fo0 = gt.off[fe], fo1 = gt.off[fe + 1];
         const int64_t mtiles_e = expert_row_tiles<TM>(p, fo0, fo1);
         const int64_t local = bid - gt.pre[fe];
-        const int64_t nt = local / mtiles_e, j = local % mtiles_e;
+        const uint32_t l32 = static_cast<uint32_t>(local), m32 = static_cast<uint32_t>(mtiles_e);
+        const int64_t nt = l32 / m32, j = l32 - static_cast<uint32_t>(nt) * m32;
         t.valid = 1;
         tile_row0 = p.a_row_pad ? fo0 + j * TM : (fo0 / TM + j) * TM;
         if (p.a_row_pad) srow0 = gt.pst[fe] + j * TM;
@@ -245,9 +269,10 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
         t.row_lo = max(fo0, tile_row0 + 128 * rank);
         t.row_hi = min(fo1, tile_row0 + 128 * rank + 128);
     } else if (p.mode == kGroupedK && gt.off != nullptr) {
-        const int64_t per = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-        const int e = static_cast<int>(bid / per);
-        const int64_t local = bid % per, mt = local % p.m_tiles, nt = local / p.m_tiles;
+        const uint32_t b32 = static_cast<uint32_t>(bid), e32 = fdiv(b32, p.fd_mn);
+        const int e = static_cast<int>(e32);
+        const uint32_t local = b32 - e32 * p.fd_mn.d, nt32 = fdiv(local, p.fd_m);
+        const int64_t nt = nt32, mt = local - nt32 * p.fd_m.d;
         const int64_t pe = gt.pre[e], ne = gt.off[e + 1] - gt.off[e];
         t.valid = 1;
         tile_row0 = mt * TM;
@@ -258,11 +283,14 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
         t.row_lo = tile_row0 + 128 * rank;
         t.row_hi = min(p.M, t.row_lo + 128);
         t.c_off = static_cast<int64_t>(e) * p.c_expert_stride;
+        t.c_row0 = static_cast<int64_t>(e) * p.c_expert_rows;
     } else if (p.mode == kDense) {
         // raster so that the smaller operand stays in L2 while the larger one
         // streams through once: concurrent CTAs share the larger operand's tile
-        const int64_t mt = p.n_fastest ? bid / p.n_tiles : bid % p.m_tiles;
-        const int64_t nt = p.n_fastest ? bid % p.n_tiles : bid / p.m_tiles;
+        const uint32_t b32 = static_cast<uint32_t>(bid);
+        const uint32_t q = fdiv(b32, p.n_fastest ? p.fd_n : p.fd_m), r = b32 - q * (p.n_fastest ? p.fd_n.d : p.fd_m.d);
+        const int64_t mt = p.n_fastest ? q : r;
+        const int64_t nt = p.n_fastest ? r : q;
         t.valid = 1;
         tile_row0 = mt * TM;
         bn0 = nt * BN;
@@ -304,7 +332,8 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
         if (fe < 0) { t.valid = 0; return t; }
         const int64_t mtiles_e = expert_row_tiles<TM>(p, fo0, fo1);
         const int64_t local = bid - fstart;
-        const int64_t nt = local / mtiles_e, j = local % mtiles_e;
+        const uint32_t l32 = static_cast<uint32_t>(local), m32 = static_cast<uint32_t>(mtiles_e);
+        const int64_t nt = l32 / m32, j = l32 - static_cast<uint32_t>(nt) * m32;
         t.valid = 1;
         tile_row0 = p.a_row_pad ? fo0 + j * TM : (fo0 / TM + j) * TM;
         if (p.a_row_pad) srow0 = fpst + j * TM;
@@ -314,9 +343,10 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
         t.row_lo = max(fo0, tile_row0 + 128 * rank);
         t.row_hi = min(fo1, tile_row0 + 128 * rank + 128);
     } else {  // kGroupedK
-        const int64_t per = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-        const int e = static_cast<int>(bid / per);
-        const int64_t local = bid % per, mt = local % p.m_tiles, nt = local / p.m_tiles;
+        const uint32_t b32 = static_cast<uint32_t>(bid), e32 = fdiv(b32, p.fd_mn);
+        const int e = static_cast<int>(e32);
+        const uint32_t local = b32 - e32 * p.fd_mn.d, nt32 = fdiv(local, p.fd_m);
+        const int64_t nt = nt32, mt = local - nt32 * p.fd_m.d;
         int64_t pe = 0;  // padded start of group e = sum_{j<e} ceil128(n_j)
         for (int base = 0; base < e; base += 32) {
             const int j = base + lane;
@@ -334,6 +364,7 @@ __device__ TileInfo resolve_tile(const Params &p, int64_t bid, int lane, uint32_
         t.row_lo = tile_row0 + 128 * rank;
         t.row_hi = min(p.M, t.row_lo + 128);
         t.c_off = static_cast<int64_t>(e) * p.c_expert_stride;
+        t.c_row0 = static_cast<int64_t>(e) * p.c_expert_rows;
     }
     t.a_row0 = tile_row0 + 128 * rank;  // this CTA's 128 rows of A (and of the output)
     t.a_ratom = (srow0 >= 0 ? srow0 + 128 * rank : t.a_row0) / 128;
@@ -924,7 +955,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmC, slot, static_cast<int>(col), static_cast<int>(ti.c_off / p.ldc + wrow0));
+                        tma_store_2d(&tmC, slot, static_cast<int>(col), static_cast<int>(ti.c_row0 + wrow0));
                         bulk_commit_group();
                     }
                     st_count++;
@@ -1104,6 +1135,11 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     else if (g.mode == kGroupedRows) p.total_tiles = ((g.T + kUnitRows - 1) / kUnitRows + g.E) * p.n_tiles;
     else p.total_tiles = static_cast<int64_t>(g.E) * p.m_tiles * p.n_tiles;
     if (p.total_tiles <= 0) return cudaSuccess;
+    if (p.total_tiles >= (1ll << 31)) return cudaErrorInvalidValue;  // the tile decode divides 31-bit indices
+    p.fd_m = make_fastdiv(static_cast<uint32_t>(p.m_tiles));
+    p.fd_n = make_fastdiv(static_cast<uint32_t>(p.n_tiles));
+    p.fd_mn = make_fastdiv(static_cast<uint32_t>(p.m_tiles) * static_cast<uint32_t>(p.n_tiles));
+    p.c_expert_rows = g.mode == kGroupedK ? p.c_expert_stride / p.ldc : 0;
 
     // persistent grid: as many CTAs (CTA pairs) as can be resident at once, one
     // per SM (a CTA needs ~200 KB of shared memory).  Per device, once, under a
