@@ -574,6 +574,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
+    pdl_launch_dependents();
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
 
@@ -1152,7 +1154,7 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cfg.stream = st;
@@ -1184,6 +1186,11 @@ cudaError_t launch_cg(const GemmProblem &g, Params p, cudaStream_t st) {
     }
     const int64_t units = p.total_tiles < units_max ? p.total_tiles : units_max;
     cfg.gridDim = dim3(static_cast<unsigned>(units * CG));
+    // programmatic dependent launch (see pdl_wait in the kernel)
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs++;
     return cudaLaunchKernelEx(&cfg, k_gemm<CG, KIND, BIAS>, tmA, tmB, tmSA, tmSB, tmC, p);
 }
 

@@ -684,6 +684,8 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
     __shared__ int abort_flag;
     __shared__ int64_t g_tab[GROUPED ? 2 * (kQuantTableE + 1) : 1];  // group offsets, padded starts
 
+    pdl_launch_dependents();
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t ring_s = smem_u32(ring), bar0 = smem_u32(&bars[0]);
     const ColExtents ext = col_extents(P);
@@ -1410,8 +1412,18 @@ bool launch_cols_tma(const ColParams &P, int64_t row_tiles, cudaStream_t st, cud
     const int64_t ct_tiles = (P.C + kTile - 1) / kTile;
     const int64_t n_tiles = row_tiles * ct_tiles;
     const int64_t grid = n_tiles < ctas ? n_tiles : ctas;
-    k_quant_cols_tma<ROWS, GROUPED, COLS, FMT><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(tm, P, n_tiles, ct_tiles, err);
-    *res = cudaGetLastError();
+    // programmatic dependent launch (see pdl_wait in the kernel)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    *res = cudaLaunchKernelEx(&cfg, k_quant_cols_tma<ROWS, GROUPED, COLS, FMT>, tm, P, n_tiles, ct_tiles, err);
     return true;
 }
 
