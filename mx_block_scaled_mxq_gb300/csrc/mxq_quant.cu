@@ -264,6 +264,8 @@ __global__ void __launch_bounds__(kThreads) k_quant_rows(const InT *__restrict__
                                                          int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
                                                          uint8_t *__restrict__ s, int64_t kb_tiles, float sf,
                                                          unsigned int *err) {
+    pdl_launch_dependents();
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
     // buffer extents in bytes (checked by debug builds)
     const uint64_t x_bytes = static_cast<uint64_t>((R - 1) * ldx + C) * sizeof(InT);
     const uint64_t q_bytes = static_cast<uint64_t>(R * ldq), s_bytes = static_cast<uint64_t>((R + 127) / 128 * kb_tiles * 512);
@@ -417,6 +419,8 @@ __device__ __forceinline__ ColExtents col_extents(const ColParams &P) {
 
 template <bool ROWS, bool GROUPED>
 __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
+    pdl_launch_dependents();
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
     __shared__ __align__(16) uint8_t tile[kTile * kTile * 2];
     __shared__ __align__(16) uint8_t srow_atom[512];
     __shared__ __align__(16) uint8_t scol_atom[512];
@@ -583,6 +587,24 @@ __global__ void __launch_bounds__(kThreads) k_quant_cols(ColParams P) {
         uint8_t *dst = P.sT + (ct * P.kb_col_tiles + rt) * 512 + 16 * l;
         if (MXQ_IN_BOUNDS(dst, 16, P.sT, ext.sT, P.err)) stg_v4(dst, v);
     }
+}
+
+// Launch with programmatic stream serialization: the kernel begins with
+// pdl_launch_dependents / pdl_wait (mxq_device.cuh), so the next launch in
+// the stream overlaps this one's last CTAs and touches memory only after it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // ============================================================================
@@ -984,6 +1006,8 @@ template <bool MASK>
 __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_vec(const float *__restrict__ x, float *y,
                                                             uint32_t *__restrict__ mask, int64_t nchunks, float sf,
                                                             unsigned int *err) {
+    pdl_launch_dependents();
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t xy_bytes = static_cast<uint64_t>(nchunks) * 32, m_bytes = static_cast<uint64_t>(nchunks);  // extents
     (void)xy_bytes; (void)m_bytes; (void)err;
@@ -1056,6 +1080,8 @@ template <bool MASK>
 __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restrict__ x, float *y,
                                                             uint32_t *__restrict__ mask, int64_t rows, int64_t cols,
                                                             float sf, unsigned int *err) {
+    pdl_launch_dependents();
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
     const uint64_t xy_bytes = static_cast<uint64_t>(rows * cols) * 4;  // extents (debug builds)
     (void)xy_bytes; (void)err;
     const int lane = threadIdx.x & 31;
@@ -1096,6 +1122,8 @@ __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_gen(const float *__restr
 constexpr int64_t kBlkWindow = static_cast<int64_t>(kThreads) * 2;
 __global__ void __launch_bounds__(kThreads) k_qdq_mxfp4_bf16(const uint16_t *__restrict__ x, uint16_t *y,
                                                              int64_t nblocks, float sf, unsigned int *err) {
+    pdl_launch_dependents();
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
     const uint64_t xy_bytes = static_cast<uint64_t>(nblocks) * 64;  // extent (debug builds)
     (void)xy_bytes; (void)err;
     for (int64_t w0 = static_cast<int64_t>(blockIdx.x) * kBlkWindow; w0 < nblocks;
@@ -1151,6 +1179,8 @@ __global__ void __launch_bounds__(kThreads) k_pack_mxfp4(const InT *__restrict__
                                                          uint8_t *__restrict__ q, int64_t ldq,
                                                          uint8_t *__restrict__ s, int64_t kb_tiles, float sf,
                                                          unsigned int *err) {
+    pdl_launch_dependents();
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
     // extents (debug builds): R = gridDim.y * 64 rows of C = gridDim.x * 128 columns
     const int64_t R = static_cast<int64_t>(gridDim.y) * 64, C = static_cast<int64_t>(gridDim.x) * 128;
     const uint64_t x_bytes = static_cast<uint64_t>((R - 1) * ldx + C) * sizeof(InT);
@@ -1230,6 +1260,8 @@ __global__ void __launch_bounds__(kThreads) k_pack_mxfp4(const InT *__restrict__
 __global__ void __launch_bounds__(kThreads) k_ste_backward_vec(const float *__restrict__ gy,
                                                                const uint32_t *__restrict__ mask, float *gx,
                                                                int64_t nchunks, unsigned int *err) {
+    pdl_launch_dependents();
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
     const uint64_t g_bytes = static_cast<uint64_t>(nchunks) * 32, m_bytes = static_cast<uint64_t>(nchunks);  // extents
     (void)g_bytes; (void)m_bytes; (void)err;
     const bool al32 = ((reinterpret_cast<uintptr_t>(gy) | reinterpret_cast<uintptr_t>(gx)) & 31) == 0;
@@ -1278,6 +1310,8 @@ __global__ void __launch_bounds__(kThreads) k_ste_backward_vec(const float *__re
 __global__ void __launch_bounds__(kThreads) k_ste_backward_gen(const float *__restrict__ gy,
                                                                const uint32_t *__restrict__ mask, float *gx,
                                                                int64_t rows, int64_t cols, unsigned int *err) {
+    pdl_launch_dependents();
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
     const uint64_t g_bytes = static_cast<uint64_t>(rows * cols) * 4;  // extent (debug builds)
     (void)g_bytes; (void)err;
     const int lane = threadIdx.x & 31;
@@ -1343,23 +1377,23 @@ cudaError_t launch_quant_rows(const void *x, bool fp32_in, int fmt, int64_t R, i
             return res;
     }
     if (fmt == 0) {
-        k_quant_rows<uint16_t, 0><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf, err);
+        (void)launch_pdl(k_quant_rows<uint16_t, 0>, grid, kThreads, 0, st, xb, R, C, ldx, q, C, s, kb_tiles, sf, err);
     } else if (fmt == 2) {
-        k_quant_rows<uint16_t, 2><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C, s, kb_tiles, sf, err);
+        (void)launch_pdl(k_quant_rows<uint16_t, 2>, grid, kThreads, 0, st, xb, R, C, ldx, q, C, s, kb_tiles, sf, err);
     } else if (R % kTile == 0 && C % kTile == 0 &&
                ((reinterpret_cast<uintptr_t>(x) | static_cast<uintptr_t>(ldx * (fp32_in ? 4 : 2))) & 31) == 0) {
         // whole scale tiles: 64 x 128 blocks
         const dim3 g2(static_cast<unsigned>(C / kTile), static_cast<unsigned>(R / 64));
         if (fp32_in)
-            k_pack_mxfp4<float><<<g2, kThreads, 0, st>>>(static_cast<const float *>(x), ldx, q, C / 2, s, kb_tiles, sf,
+            (void)launch_pdl(k_pack_mxfp4<float>, g2, kThreads, 0, st, static_cast<const float *>(x), ldx, q, C / 2, s, kb_tiles, sf,
                                                           err);
         else
-            k_pack_mxfp4<uint16_t><<<g2, kThreads, 0, st>>>(xb, ldx, q, C / 2, s, kb_tiles, sf, err);
+            (void)launch_pdl(k_pack_mxfp4<uint16_t>, g2, kThreads, 0, st, xb, ldx, q, C / 2, s, kb_tiles, sf, err);
     } else if (fp32_in) {
-        k_quant_rows<float, 1><<<grid, kThreads, 0, st>>>(static_cast<const float *>(x), R, C, ldx, q, C / 2, s,
+        (void)launch_pdl(k_quant_rows<float, 1>, grid, kThreads, 0, st, static_cast<const float *>(x), R, C, ldx, q, C / 2, s,
                                                           kb_tiles, sf, err);
     } else {
-        k_quant_rows<uint16_t, 1><<<grid, kThreads, 0, st>>>(xb, R, C, ldx, q, C / 2, s, kb_tiles, sf, err);
+        (void)launch_pdl(k_quant_rows<uint16_t, 1>, grid, kThreads, 0, st, xb, R, C, ldx, q, C / 2, s, kb_tiles, sf, err);
     }
     return cudaGetLastError();
 }
@@ -1441,8 +1475,8 @@ cudaError_t launch_quant_cols(const uint16_t *x, int64_t R, int64_t C, int64_t l
     if (q_row ? launch_cols_tma<true, false>(P, row_tiles, st, &res) : launch_cols_tma<false, false>(P, row_tiles, st, &res))
         return res;
     const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>(row_tiles));
-    if (q_row) k_quant_cols<true, false><<<grid, kThreads, 0, st>>>(P);
-    else k_quant_cols<false, false><<<grid, kThreads, 0, st>>>(P);
+    if (q_row) (void)launch_pdl(k_quant_cols<true, false>, grid, kThreads, 0, st, P);
+    else (void)launch_pdl(k_quant_cols<false, false>, grid, kThreads, 0, st, P);
     return cudaGetLastError();
 }
 
@@ -1475,7 +1509,7 @@ cudaError_t launch_quant_cols_grouped(const uint16_t *x, int64_t T, int64_t C, c
         return res;
     }
     const dim3 grid(static_cast<unsigned>((C + kTile - 1) / kTile), static_cast<unsigned>(t_pad / kTile));
-    k_quant_cols<false, true><<<grid, kThreads, 0, st>>>(P);
+    (void)launch_pdl(k_quant_cols<false, true>, grid, kThreads, 0, st, P);
     return cudaGetLastError();
 }
 
@@ -1488,13 +1522,13 @@ cudaError_t launch_qdq_mxfp4(const float *x, float *y, uint32_t *mask, int64_t r
     if (vec) {
         const int64_t nchunks = rows * cols / 8;
         const int grid = grid_windows(nchunks);
-        if (mask) k_qdq_mxfp4_vec<true><<<grid, kThreads, 0, st>>>(x, y, mask, nchunks, sf, err);
-        else k_qdq_mxfp4_vec<false><<<grid, kThreads, 0, st>>>(x, y, nullptr, nchunks, sf, err);
+        if (mask) (void)launch_pdl(k_qdq_mxfp4_vec<true>, grid, kThreads, 0, st, x, y, mask, nchunks, sf, err);
+        else (void)launch_pdl(k_qdq_mxfp4_vec<false>, grid, kThreads, 0, st, x, y, nullptr, nchunks, sf, err);
     } else {
         const int64_t nblocks = rows * ((cols + 31) / 32);
         const int grid = grid_for(nblocks, kThreads / 32);
-        if (mask) k_qdq_mxfp4_gen<true><<<grid, kThreads, 0, st>>>(x, y, mask, rows, cols, sf, err);
-        else k_qdq_mxfp4_gen<false><<<grid, kThreads, 0, st>>>(x, y, nullptr, rows, cols, sf, err);
+        if (mask) (void)launch_pdl(k_qdq_mxfp4_gen<true>, grid, kThreads, 0, st, x, y, mask, rows, cols, sf, err);
+        else (void)launch_pdl(k_qdq_mxfp4_gen<false>, grid, kThreads, 0, st, x, y, nullptr, rows, cols, sf, err);
     }
     return cudaGetLastError();
 }
@@ -1505,7 +1539,7 @@ cudaError_t launch_qdq_mxfp4_bf16(const uint16_t *x, uint16_t *y, int64_t rows, 
     cudaError_t ee = device_error_word(&err);
     if (ee != cudaSuccess) return ee;
     const int64_t nblocks = rows * cols / 32;
-    k_qdq_mxfp4_bf16<<<grid_windows(nblocks, kBlkWindow), kThreads, 0, st>>>(x, y, nblocks, sf, err);
+    (void)launch_pdl(k_qdq_mxfp4_bf16, grid_windows(nblocks, kBlkWindow), kThreads, 0, st, x, y, nblocks, sf, err);
     return cudaGetLastError();
 }
 
@@ -1517,10 +1551,10 @@ cudaError_t launch_ste_backward(const float *gy, const uint32_t *mask, float *gx
     const bool vec = (cols % 32 == 0) && ((reinterpret_cast<uintptr_t>(gy) | reinterpret_cast<uintptr_t>(gx)) & 15) == 0;
     if (vec) {
         const int64_t nchunks = rows * cols / 8;
-        k_ste_backward_vec<<<grid_windows(nchunks), kThreads, 0, st>>>(gy, mask, gx, nchunks, err);
+        (void)launch_pdl(k_ste_backward_vec, grid_windows(nchunks), kThreads, 0, st, gy, mask, gx, nchunks, err);
     } else {
         const int64_t nblocks = rows * ((cols + 31) / 32);
-        k_ste_backward_gen<<<grid_for(nblocks, kThreads / 32), kThreads, 0, st>>>(gy, mask, gx, rows, cols, err);
+        (void)launch_pdl(k_ste_backward_gen, grid_for(nblocks, kThreads / 32), kThreads, 0, st, gy, mask, gx, rows, cols, err);
     }
     return cudaGetLastError();
 }
