@@ -19,13 +19,13 @@ constexpr unsigned kErrTmemAlloc = 2u;
 constexpr unsigned kErrBadOffsets = 4u;
 constexpr unsigned kErrBounds = 8u;
 
-// Programmatic dependent launch.  The persistent kernels are launched with
-// the programmatic stream-serialization attribute: each CTA first lets the
-// next kernel in the stream start launching (its CTAs find room on an SM only
-// as this grid's CTAs leave it, so the launch overlaps this grid's last wave),
-// then waits until the previous kernel in the stream has completed and its
-// writes are visible, before it reads or writes any global memory.  Without
-// the attribute both are no-ops.
+// Programmatic dependent launch.  The kernels are launched with the
+// programmatic stream-serialization attribute: a CTA lets the next kernel in
+// the stream start launching (pdl_launch_dependents; its CTAs find room on an
+// SM only as this grid's CTAs leave it, so the launch overlaps this grid's last
+// wave), and waits until the previous kernel in the stream has completed and
+// its writes are visible (pdl_wait) before it reads or writes any global
+// memory.  Without the attribute both are no-ops.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -706,7 +706,6 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
     __shared__ int abort_flag;
     __shared__ int64_t g_tab[GROUPED ? 2 * (kQuantTableE + 1) : 1];  // group offsets, padded starts
 
-    pdl_launch_dependents();
     pdl_wait();  // no global access before the previous kernel in the stream has completed
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t ring_s = smem_u32(ring), bar0 = smem_u32(&bars[0]);
@@ -801,6 +800,10 @@ __global__ void __launch_bounds__(kThreads, QuantRing<GROUPED>::kCtasPerSm)
     }
     uint32_t k = 0;
     for (; t < n_tiles; t += gridDim.x, k++) {
+        // the next launch may begin once every CTA has started its last tile
+        // (triggering at the start let a run of small launches pile their
+        // waiting CTAs onto the idle SMs, which measured slower)
+        if (t + static_cast<int64_t>(gridDim.x) >= n_tiles) pdl_launch_dependents();
         const int buf = static_cast<int>(k % kRing);
         const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * buf, (k / kRing) & 1, abort_v, err));
         uint8_t *srow_atom = srow_atoms[k & 1], *scol_atom = scol_atoms[k & 1];
