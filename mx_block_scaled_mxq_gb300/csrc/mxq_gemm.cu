@@ -575,7 +575,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     pdl_launch_dependents();
-    pdl_wait();  // no global access before the previous kernel in the stream has completed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);
 
@@ -598,14 +597,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int64_t first = CLUSTER ? blockIdx.x >> 1 : blockIdx.x;
     const int64_t step = CLUSTER ? gridDim.x >> 1 : gridDim.x;
 
-    // once any CTA has given up, the rest of the grid does no work
-    if (threadIdx.x == 0) *abort_flag = *reinterpret_cast<volatile unsigned int *>(&g_device_error) != 0 ? 1 : 0;
-    __syncthreads();
-    // (a CTA pair must pass its cluster barriers together, so only lone CTAs return here)
-    if constexpr (!CLUSTER) {
-        if (*abort_flag) return;  // before any TMEM allocation
-    }
-
+    // The prologue below touches no global memory (tensor maps are kernel
+    // parameters), so it runs before pdl_wait, overlapping the previous
+    // kernel's last wave: this CTA only lands on an SM that kernel's CTAs have
+    // left, so the tensor memory is free.
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -644,6 +639,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     if constexpr (CLUSTER) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();  // no global access before the previous kernel in the stream has completed
+    // once any CTA has given up, the rest of the grid does no work (it still
+    // leaves through the teardown below, which frees the tensor memory)
+    if (threadIdx.x == 0) *abort_flag = *reinterpret_cast<volatile unsigned int *>(&g_device_error) != 0 ? 1 : 0;
+    __syncthreads();
     GroupTables gt{nullptr, nullptr, nullptr};
     if (p.mode != kDense) {
         // malformed offsets: no tile is decoded from them, no load or store is issued
