@@ -52,8 +52,8 @@ GEMM_SOURCES = [os.path.join(ROOT, "mx_block_scaled_mxq_gb300", "csrc", f) for f
 # same full-size launches in the parity tests, keyed by a hash of the kernel
 # source; when the source has changed since, traffic is null.
 GEMM_DRAM_TRAFFIC = {
-    "65f28742011fe704": {"linear_dw_gemm": 260980736, "moe_fwd_gemm": 1506134272,
-                         "moe_dx_gemm": 1536239616, "moe_dw_gemm": 2236950016},
+    "07342afad1665483": {"linear_dw_gemm": 259970560, "moe_fwd_gemm": 1491981056,
+                         "moe_dx_gemm": 1538263296, "moe_dw_gemm": 2237048576},
 }
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
